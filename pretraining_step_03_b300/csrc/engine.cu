@@ -1,0 +1,693 @@
+// The step engine and the C ABI of libnc.so.
+//
+// One model = one caller-owned device arena laid out here (parameters,
+// optimizer state, activation stash, scratch) and one CUDA stream.  The
+// schedule follows the nanochat speedrun walkthrough (lyylswood.com):
+//   section 预搜检 (pretraining): token embedding; per layer a pre-norm
+//   attention block and a pre-norm 4x MLP block, both residual; a final norm
+//   and an untied LM head; next-token cross-entropy reported as bits per
+//   byte; backward; Muon on the block matrices, AdamW on the embedding and
+//   unembedding; no biases and no norm gains;
+//   section 该你了 (depth scaling): gradient accumulation over micro-batches.
+// Readings where the pages are silent (RoPE, ReLU^2, eps, Muon/AdamW details)
+// are the same as the fp64 oracle's and are stated next to each kernel.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <vector>
+
+#include "kernels.cuh"
+
+namespace nc {
+extern uint32_t* g_gemm_flag;
+}
+
+using namespace nc;
+
+struct nc_model {
+    int depth, d, H, Dh, V, F, dtype, maxB, maxT;
+    long maxM;
+    cudaStream_t stream;
+    char* arena;
+    size_t arena_bytes;
+    // parameters
+    int nparams;
+    std::vector<long> poff, prows, pcols;
+    std::vector<int> pkind;
+    long P;
+    float* master;
+    bf16* shadow;      // bf16 compute copy (bf16 mode)
+    float* grads;
+    float* momentum;   // Muon buffers (same offsets as master)
+    float* adam_m;     // [2, V*d]: wte then lm_head
+    float* adam_v;
+    // Muon
+    MuonMat* mats;
+    int nmat;
+    float* muon_partial;
+    int muon_chunks;
+    void* nsX;         // [square group | wide group], act type
+    void* nsX2;
+    void* nsA;         // [6L, d, d]
+    void* nsB;
+    // misc
+    float2* rope;      // [maxT, Dh/2]
+    float* loss;       // [2 * 64] micro-step {loss, bpb}
+    uint32_t* flag;
+    int32_t* tok_stage;  // [2, maxM] tokens, targets (nc_train_step)
+    // activations (act type unless noted)
+    struct Layer {
+        void *y1, *qkv, *o, *y2, *h, *a;
+        float *r1, *r2, *lse;
+    };
+    std::vector<Layer> L;
+    float* x;          // residual stream fp32 [M, d]
+    void* yf;
+    float* rf;
+    void* logits;      // [M, V]
+    float* nll;
+    float* g;          // residual gradient fp32 [M, d]
+    void* gT;          // its act-type copy (bf16 mode)
+    float* dy;         // fp32 [M, d]
+    void* dqkv;
+    void* dO;
+    void* dh;
+    float* delta;      // attention row statistics [M * H]
+    void* ebws;
+    size_t ebws_bytes;
+    void* splitk;
+    size_t splitk_bytes;
+};
+
+namespace {
+
+size_t al(size_t b) { return (b + 255) & ~(size_t)255; }
+
+struct Carver {
+    size_t off = 0;
+    char* base = nullptr;
+    void* take(size_t bytes) {
+        void* p = base ? base + off : nullptr;
+        off += al(bytes);
+        return p;
+    }
+};
+
+int check_dims(int depth, int d, int H, int V, int maxB, int maxT, int dtype) {
+    if (depth < 1 || depth > 1024) return set_error(NC_ERR_ARG, "depth %d out of range", depth);
+    if (d < 32 || d % 32) return set_error(NC_ERR_ARG, "d_model %d must be a positive multiple of 32", d);
+    if (H < 1 || d % H) return set_error(NC_ERR_ARG, "d_model %d not divisible by n_head %d", d, H);
+    int Dh = d / H;
+    if (Dh % 2 || Dh > 128) return set_error(NC_ERR_ARG, "head_dim %d must be even and <= 128", Dh);
+    if (V < 8 || V % 8) return set_error(NC_ERR_ARG, "vocab %d must be a positive multiple of 8", V);
+    if (maxB < 0 || maxT < 0 || (long)maxB * maxT > (1L << 24))
+        return set_error(NC_ERR_ARG, "max_B*max_T out of range");
+    if (dtype != NC_BF16 && dtype != NC_FP32) return set_error(NC_ERR_ARG, "dtype %d", dtype);
+    return NC_OK;
+}
+
+// Lays the arena out; with base == nullptr only measures.
+void layout(nc_model* m, char* base, size_t* total) {
+    Carver c;
+    c.base = base;
+    const int d = m->d, V = m->V, Ld = m->depth;
+    const size_t act = m->dtype == NC_BF16 ? 2 : 4;
+    const long P = m->P;
+    m->master = (float*)c.take(P * 4);
+    m->shadow = m->dtype == NC_BF16 ? (bf16*)c.take(P * 2) : nullptr;
+    m->grads = (float*)c.take(P * 4);
+    m->momentum = (float*)c.take(P * 4);
+    m->adam_m = (float*)c.take((size_t)2 * V * d * 4);
+    m->adam_v = (float*)c.take((size_t)2 * V * d * 4);
+    m->nmat = 6 * Ld;
+    m->muon_chunks = 32;
+    m->mats = (MuonMat*)c.take(sizeof(MuonMat) * m->nmat);
+    m->muon_partial = (float*)c.take((size_t)m->nmat * m->muon_chunks * 4);
+    const size_t nsx = ((size_t)4 * Ld * d * d + (size_t)2 * Ld * d * 4 * d) * act;
+    m->nsX = c.take(nsx);
+    m->nsX2 = c.take(nsx);
+    m->nsA = c.take((size_t)6 * Ld * d * d * act);
+    m->nsB = c.take((size_t)6 * Ld * d * d * act);
+    m->rope = (float2*)c.take((size_t)(m->maxT > 0 ? m->maxT : 1) * (m->Dh / 2) * 8);
+    m->loss = (float*)c.take(128 * 4);
+    m->flag = (uint32_t*)c.take(16);
+    const long M = m->maxM;
+    m->L.assign(Ld, nc_model::Layer{});
+    m->tok_stage = nullptr;
+    if (M > 0) {
+        m->tok_stage = (int32_t*)c.take((size_t)2 * M * 4);
+        for (int l = 0; l < Ld; ++l) {
+            auto& y = m->L[l];
+            y.y1 = c.take(M * d * act);
+            y.r1 = (float*)c.take(M * 4);
+            y.qkv = c.take(M * 3 * d * act);
+            y.o = c.take(M * d * act);
+            y.lse = (float*)c.take(M * m->H * 4);
+            y.y2 = c.take(M * d * act);
+            y.r2 = (float*)c.take(M * 4);
+            y.h = c.take(M * 4 * d * act);
+            y.a = c.take(M * 4 * d * act);
+        }
+        m->x = (float*)c.take(M * d * 4);
+        m->yf = c.take(M * d * act);
+        m->rf = (float*)c.take(M * 4);
+        m->logits = c.take(M * V * act);
+        m->nll = (float*)c.take(M * 4);
+        m->g = (float*)c.take(M * d * 4);
+        m->gT = m->dtype == NC_BF16 ? c.take(M * d * act) : nullptr;
+        m->dy = (float*)c.take(M * d * 4);
+        m->dqkv = c.take(M * 3 * d * act);
+        m->dO = c.take(M * d * act);
+        m->dh = c.take(M * 4 * d * act);
+        m->delta = (float*)c.take(M * m->H * 4);
+        m->ebws_bytes = embed_backward_ws_bytes((int)M, d, V);
+        m->ebws = c.take(m->ebws_bytes);
+    }
+    // split-K scratch: the largest need among the step's GEMMs
+    size_t sk = 0;
+    if (m->dtype == NC_BF16) {
+        const long mm = M > 0 ? M : 1;
+        const int shapes[][3] = {{3 * d, d, (int)mm}, {d, d, (int)mm}, {4 * d, d, (int)mm},
+                                 {d, 4 * d, (int)mm}, {V, d, (int)mm}};
+        for (auto& s : shapes) {
+            Gemm g;
+            g.M = s[0]; g.N = s[1]; g.K = s[2];
+            size_t b = gemm_tc_splitk_bytes(g);
+            if (b > sk) sk = b;
+        }
+    }
+    m->splitk_bytes = sk;
+    m->splitk = sk ? c.take(sk) : nullptr;
+    *total = c.off;
+}
+
+template <typename T> T* W(nc_model* m, int i) {
+    if (m->dtype == NC_BF16) return (T*)(m->shadow + m->poff[i]);
+    return (T*)(m->master + m->poff[i]);
+}
+
+int run_gemm(nc_model* m, const Gemm& g) {
+    if (g.in_dtype == NC_BF16) return gemm_tc(g, m->splitk, m->splitk_bytes, m->stream);
+    return gemm_simt(g, m->stream);
+}
+
+// C[M,N] = A[M,K] (row-major, lda) * B[N,K]^T, or with a_t/b_t as stored [K, .]
+Gemm mk(nc_model* m, int M, int N, int K, const void* A, long lda, bool a_t, const void* B, long ldb,
+        bool b_t, void* C, long ldc, int c_dtype) {
+    Gemm g;
+    g.M = M; g.N = N; g.K = K;
+    g.A = A; g.lda = lda; g.a_t = a_t;
+    g.B = B; g.ldb = ldb; g.b_t = b_t;
+    g.in_dtype = m->dtype;
+    g.C = C; g.ldc = ldc; g.c_dtype = c_dtype;
+    return g;
+}
+
+// weight gradient dW[N_out, K_out] (+)= dY^T X over M rows
+int weight_grad(nc_model* m, float* dW, int rows, int cols, const void* dY, long ldy, const void* X,
+                long ldx, int M, int accumulate) {
+    Gemm g = mk(m, rows, cols, M, dY, ldy, true, X, ldx, true, dW, cols, NC_FP32);
+    g.aux = dW; g.ldaux = cols; g.aux_dtype = NC_FP32; g.beta = accumulate ? 1.f : 0.f;
+    return run_gemm(m, g);
+}
+
+template <typename T>
+int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const int32_t* tb, int B,
+                     int T_, int accumulate, float grad_scale, float* out) {
+    const int d = m->d, H = m->H, Dh = m->Dh, V = m->V, F = m->F;
+    const int M = B * T_;
+    const int act = m->dtype;
+    cudaStream_t s = m->stream;
+    const int iw = 0, iu = 1 + 6 * m->depth;
+    T* gop = m->dtype == NC_BF16 ? (T*)m->gT : (T*)m->g;  // residual gradient as GEMM operand
+    T* gT = m->dtype == NC_BF16 ? (T*)m->gT : nullptr;
+
+    // ------------------------------------------------ forward
+    NC_TRY(embed_forward<T>(tok, W<T>(m, iw), m->x, M, d, V, m->flag, s));
+    for (int l = 0; l < m->depth; ++l) {
+        auto& Ly = m->L[l];
+        const int b0 = 1 + 6 * l;
+        NC_TRY(rmsnorm_forward<T>(m->x, (T*)Ly.y1, Ly.r1, M, d, s));
+        NC_TRY(run_gemm(m, mk(m, M, 3 * d, d, Ly.y1, d, false, W<T>(m, b0), d, false, Ly.qkv, 3 * d, act)));
+        NC_TRY(rope_apply<T>((T*)Ly.qkv, 3 * d, M, T_, H, Dh, m->rope, 1.f, s));
+        T* q = (T*)Ly.qkv;
+        NC_TRY(attention_forward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, d, Ly.lse, B, T_, H, Dh, s));
+        {   // x += o Wo^T
+            Gemm g = mk(m, M, d, d, Ly.o, d, false, W<T>(m, b0 + 3), d, false, m->x, d, NC_FP32);
+            g.aux = m->x; g.ldaux = d; g.aux_dtype = NC_FP32; g.beta = 1.f;
+            NC_TRY(run_gemm(m, g));
+        }
+        NC_TRY(rmsnorm_forward<T>(m->x, (T*)Ly.y2, Ly.r2, M, d, s));
+        {   // h = y2 W1^T, a = relu(h)^2
+            Gemm g = mk(m, M, F, d, Ly.y2, d, false, W<T>(m, b0 + 4), d, false, Ly.h, F, act);
+            g.epi = EPI_RELU2; g.C2 = Ly.a;
+            NC_TRY(run_gemm(m, g));
+        }
+        {   // x += a W2^T
+            Gemm g = mk(m, M, d, F, Ly.a, F, false, W<T>(m, b0 + 5), F, false, m->x, d, NC_FP32);
+            g.aux = m->x; g.ldaux = d; g.aux_dtype = NC_FP32; g.beta = 1.f;
+            NC_TRY(run_gemm(m, g));
+        }
+    }
+    NC_TRY(rmsnorm_forward<T>(m->x, (T*)m->yf, m->rf, M, d, s));
+    NC_TRY(run_gemm(m, mk(m, M, V, d, m->yf, d, false, W<T>(m, iu), d, false, m->logits, V, act)));
+    NC_TRY(cross_entropy<T>((T*)m->logits, tgt, m->nll, M, V, grad_scale / (float)M, m->flag, s));
+    NC_TRY(loss_reduce(m->nll, tgt, tb, M, V, out, m->flag, s));
+
+    // ------------------------------------------------ backward
+    float* G = m->grads;
+    NC_TRY(weight_grad(m, G + m->poff[iu], V, d, m->logits, V, m->yf, d, M, accumulate));
+    NC_TRY(run_gemm(m, mk(m, M, d, V, m->logits, V, false, W<T>(m, iu), d, true, m->dy, d, NC_FP32)));
+    NC_TRY(rmsnorm_backward<T>(m->dy, (T*)m->yf, m->rf, nullptr, m->g, gT, M, d, s));
+    for (int l = m->depth - 1; l >= 0; --l) {
+        auto& Ly = m->L[l];
+        const int b0 = 1 + 6 * l;
+        // MLP block
+        NC_TRY(weight_grad(m, G + m->poff[b0 + 5], d, F, gop, d, Ly.a, F, M, accumulate));
+        {   // dh = (g W2) * 2 relu(h)
+            Gemm g = mk(m, M, F, d, gop, d, false, W<T>(m, b0 + 5), F, true, m->dh, F, act);
+            g.epi = EPI_RELU2_BWD; g.aux = Ly.h; g.ldaux = F; g.aux_dtype = act;
+            NC_TRY(run_gemm(m, g));
+        }
+        NC_TRY(weight_grad(m, G + m->poff[b0 + 4], F, d, m->dh, F, Ly.y2, d, M, accumulate));
+        NC_TRY(run_gemm(m, mk(m, M, d, F, m->dh, F, false, W<T>(m, b0 + 4), d, true, m->dy, d, NC_FP32)));
+        NC_TRY(rmsnorm_backward<T>(m->dy, (T*)Ly.y2, Ly.r2, m->g, m->g, gT, M, d, s));
+        // attention block
+        NC_TRY(weight_grad(m, G + m->poff[b0 + 3], d, d, gop, d, Ly.o, d, M, accumulate));
+        NC_TRY(run_gemm(m, mk(m, M, d, d, gop, d, false, W<T>(m, b0 + 3), d, true, m->dO, d, act)));
+        T* q = (T*)Ly.qkv;
+        T* dq = (T*)m->dqkv;
+        NC_TRY(attention_backward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, (T*)m->dO, d, Ly.lse, dq,
+                                     dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s));
+        NC_TRY(rope_apply<T>(dq, 3 * d, M, T_, H, Dh, m->rope, -1.f, s));
+        NC_TRY(weight_grad(m, G + m->poff[b0], 3 * d, d, m->dqkv, 3 * d, Ly.y1, d, M, accumulate));
+        NC_TRY(run_gemm(m, mk(m, M, d, 3 * d, m->dqkv, 3 * d, false, W<T>(m, b0), d, true, m->dy, d, NC_FP32)));
+        NC_TRY(rmsnorm_backward<T>(m->dy, (T*)Ly.y1, Ly.r1, m->g, m->g, gT, M, d, s));
+    }
+    NC_TRY(embed_backward(tok, m->g, G + m->poff[iw], M, d, V, accumulate,
+                          embed_backward_ws(m->ebws, M, d, V), s));
+    return NC_OK;
+}
+
+template <typename T>
+int muon(nc_model* m, float lr, float mu, int nesterov, int steps, const float* coef) {
+    cudaStream_t s = m->stream;
+    const int d = m->d, Ld = m->depth;
+    NC_TRY(muon_momentum(m->grads, m->momentum, m->mats, m->nmat, mu, nesterov, m->muon_partial,
+                         m->muon_chunks, s));
+    NC_TRY(muon_normalize<T>(m->grads, m->mats, m->nmat, m->muon_partial, m->muon_chunks, (T*)m->nsX,
+                             32, s));
+    T* X = (T*)m->nsX;
+    T* Y = (T*)m->nsX2;
+    const long sq = (long)4 * Ld * d * d;  // elements of the square group
+    const int act = m->dtype;
+    for (int it = 0; it < steps; ++it) {
+        for (int grp = 0; grp < 2; ++grp) {
+            const int n = grp == 0 ? 4 * Ld : 2 * Ld, r = d, c = grp == 0 ? d : 4 * d;
+            T* x = X + (grp == 0 ? 0 : sq);
+            T* y = Y + (grp == 0 ? 0 : sq);
+            T* A = (T*)m->nsA + (grp == 0 ? 0 : (long)4 * Ld * d * d);
+            T* Bm = (T*)m->nsB + (grp == 0 ? 0 : (long)4 * Ld * d * d);
+            {   // A = X X^T
+                Gemm g = mk(m, r, r, c, x, c, false, x, c, false, A, r, act);
+                g.batch = n; g.sA = g.sB = (long)r * c; g.sC = (long)r * r;
+                NC_TRY(run_gemm(m, g));
+            }
+            {   // B = c2 A A + c1 A
+                Gemm g = mk(m, r, r, r, A, r, false, A, r, true, Bm, r, act);
+                g.batch = n; g.sA = g.sB = g.sC = (long)r * r;
+                g.alpha = coef[2]; g.aux = A; g.ldaux = r; g.sAux = (long)r * r; g.aux_dtype = act;
+                g.beta = coef[1];
+                NC_TRY(run_gemm(m, g));
+            }
+            {   // Y = B X + c0 X
+                Gemm g = mk(m, r, c, r, Bm, r, false, x, c, true, y, c, act);
+                g.batch = n; g.sA = (long)r * r; g.sB = (long)r * c; g.sC = (long)r * c;
+                g.aux = x; g.ldaux = c; g.sAux = (long)r * c; g.aux_dtype = act; g.beta = coef[0];
+                NC_TRY(run_gemm(m, g));
+            }
+        }
+        T* t = X; X = Y; Y = t;
+    }
+    NC_TRY(muon_apply<T>(m->master, m->shadow, m->mats, m->nmat, X, lr, 32, s));
+    return NC_OK;
+}
+
+int upload_f32(nc_model* m, float* dst, const float* host, size_t n) {
+    NC_TRY(cuda_check(cudaMemcpyAsync(dst, host, n * 4, cudaMemcpyHostToDevice, m->stream), "H2D"));
+    return cuda_check(cudaStreamSynchronize(m->stream), "sync");
+}
+int download_f32(nc_model* m, float* host, const float* src, size_t n) {
+    NC_TRY(cuda_check(cudaMemcpyAsync(host, src, n * 4, cudaMemcpyDeviceToHost, m->stream), "D2H"));
+    return cuda_check(cudaStreamSynchronize(m->stream), "sync");
+}
+
+uint64_t splitmix(uint64_t& s) {
+    uint64_t z = (s += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+int check_param(nc_model* m, int index, size_t n) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    if (index < 0 || index >= m->nparams) return set_error(NC_ERR_ARG, "param index %d", index);
+    if (n != (size_t)(m->prows[index] * m->pcols[index]))
+        return set_error(NC_ERR_ARG, "param %d has %ld elements, got %zu", index,
+                         m->prows[index] * m->pcols[index], n);
+    return NC_OK;
+}
+
+void init_geometry(nc_model* m, int depth, int d, int H, int V, int dtype, int maxB, int maxT) {
+    m->depth = depth; m->d = d; m->H = H; m->Dh = d / H; m->V = V; m->F = 4 * d;
+    m->dtype = dtype; m->maxB = maxB; m->maxT = maxT; m->maxM = (long)maxB * maxT;
+    m->nparams = 6 * depth + 2;
+    m->poff.clear(); m->prows.clear(); m->pcols.clear(); m->pkind.clear();
+    long off = 0;
+    auto add = [&](long r, long c, int k) {
+        m->poff.push_back(off); m->prows.push_back(r); m->pcols.push_back(c); m->pkind.push_back(k);
+        off += (r * c + 63) / 64 * 64;
+    };
+    add(V, d, NC_KIND_EMB);
+    for (int l = 0; l < depth; ++l) {
+        for (int j = 0; j < 4; ++j) add(d, d, NC_KIND_MATRIX);
+        add(4 * d, d, NC_KIND_MATRIX);
+        add(d, 4 * d, NC_KIND_MATRIX);
+    }
+    add(V, d, NC_KIND_UNEMB);
+    m->P = off;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+int nc_arena_bytes(int depth, int d_model, int n_head, int vocab, int max_B, int max_T, int dtype,
+                   size_t* out_bytes) {
+    NC_TRY(check_dims(depth, d_model, n_head, vocab, max_B, max_T, dtype));
+    if (!out_bytes) return set_error(NC_ERR_ARG, "null out_bytes");
+    nc_model m{};
+    init_geometry(&m, depth, d_model, n_head, vocab, dtype, max_B, max_T);
+    size_t total = 0;
+    layout(&m, nullptr, &total);
+    *out_bytes = total;
+    return NC_OK;
+}
+
+int nc_init_model(int depth, int d_model, int n_head, int vocab, uint64_t seed, void* arena,
+                  size_t arena_bytes, int dtype, int max_B, int max_T, void* stream, nc_model** out) {
+    NC_TRY(check_dims(depth, d_model, n_head, vocab, max_B, max_T, dtype));
+    if (!out) return set_error(NC_ERR_ARG, "null out");
+    if (!arena || (uintptr_t)arena % 256) return set_error(NC_ERR_ARG, "arena must be 256-byte aligned device memory");
+    nc_model* m = new nc_model();
+    init_geometry(m, depth, d_model, n_head, vocab, dtype, max_B, max_T);
+    size_t need = 0;
+    layout(m, nullptr, &need);
+    if (arena_bytes < need) {
+        delete m;
+        return set_error(NC_ERR_OOM, "arena has %zu bytes, the model needs %zu", arena_bytes, need);
+    }
+    m->arena = (char*)arena;
+    m->arena_bytes = arena_bytes;
+    m->stream = (cudaStream_t)stream;
+    layout(m, m->arena, &need);
+    int rc = NC_OK;
+    do {
+        cudaStream_t s = m->stream;
+        // weights N(0, 0.02): splitmix64 -> Box-Muller, one tensor at a time
+        uint64_t st = seed;
+        std::vector<float> h;
+        for (int i = 0; i < m->nparams && rc == NC_OK; ++i) {
+            const size_t n = (size_t)(m->prows[i] * m->pcols[i]);
+            h.resize(n);
+            for (size_t j = 0; j < n; j += 2) {
+                double u1 = ((splitmix(st) >> 11) + 1.0) * (1.0 / 9007199254740993.0);
+                double u2 = (splitmix(st) >> 11) * (1.0 / 9007199254740992.0);
+                double rr = sqrt(-2.0 * log(u1)) * 0.02;
+                h[j] = (float)(rr * cos(6.283185307179586 * u2));
+                if (j + 1 < n) h[j + 1] = (float)(rr * sin(6.283185307179586 * u2));
+            }
+            rc = upload_f32(m, m->master + m->poff[i], h.data(), n);
+        }
+        if (rc) break;
+        if (m->shadow && (rc = cast_f32_bf16(m->master, m->shadow, m->P, s))) break;
+        if ((rc = cuda_check(cudaMemsetAsync(m->grads, 0, m->P * 4, s), "memset"))) break;
+        if ((rc = cuda_check(cudaMemsetAsync(m->momentum, 0, m->P * 4, s), "memset"))) break;
+        if ((rc = cuda_check(cudaMemsetAsync(m->adam_m, 0, (size_t)2 * m->V * m->d * 4, s), "memset"))) break;
+        if ((rc = cuda_check(cudaMemsetAsync(m->adam_v, 0, (size_t)2 * m->V * m->d * 4, s), "memset"))) break;
+        if ((rc = cuda_check(cudaMemsetAsync(m->flag, 0, 16, s), "memset"))) break;
+        // Muon table: q, k, v, o, w2 in the wide orientation already; w1 transposed
+        std::vector<MuonMat> mats;
+        long sq = 0, wide = (long)4 * depth * d_model * d_model;
+        for (int l = 0; l < depth; ++l)
+            for (int j = 0; j < 6; ++j) {
+                const int idx = 1 + 6 * l + j;
+                MuonMat mm;
+                mm.off = m->poff[idx];
+                mm.rows = (int)m->prows[idx];
+                mm.cols = (int)m->pcols[idx];
+                mm.tr = mm.rows > mm.cols;
+                mm.scale = (float)sqrt(mm.rows > mm.cols ? (double)mm.rows / mm.cols : 1.0);
+                if (j < 4) { mm.x_off = sq; sq += (long)d_model * d_model; }
+                else { mm.x_off = wide; wide += (long)4 * d_model * d_model; }
+                mats.push_back(mm);
+            }
+        if ((rc = cuda_check(cudaMemcpyAsync(m->mats, mats.data(), mats.size() * sizeof(MuonMat),
+                                             cudaMemcpyHostToDevice, s), "H2D mats"))) break;
+        // RoPE table: angle t * 10000^(-2j/Dh), computed in double
+        const int half = m->Dh / 2, Tt = m->maxT > 0 ? m->maxT : 1;
+        std::vector<float2> rt((size_t)Tt * half);
+        for (int t = 0; t < Tt; ++t)
+            for (int j = 0; j < half; ++j) {
+                double ang = t * pow(10000.0, -2.0 * j / m->Dh);
+                rt[(size_t)t * half + j] = make_float2((float)cos(ang), (float)sin(ang));
+            }
+        if ((rc = cuda_check(cudaMemcpyAsync(m->rope, rt.data(), rt.size() * 8, cudaMemcpyHostToDevice, s),
+                             "H2D rope"))) break;
+        rc = cuda_check(cudaStreamSynchronize(s), "init sync");
+    } while (0);
+    if (rc) { delete m; return rc; }
+    *out = m;
+    return NC_OK;
+}
+
+int nc_free(nc_model* m) {
+    delete m;
+    return NC_OK;
+}
+
+int nc_num_params(nc_model* m, int* out_n) {
+    if (!m || !out_n) return set_error(NC_ERR_ARG, "null argument");
+    *out_n = m->nparams;
+    return NC_OK;
+}
+
+int nc_param_info(nc_model* m, int index, int* rows, int* cols, int* kind) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    if (index < 0 || index >= m->nparams) return set_error(NC_ERR_ARG, "param index %d", index);
+    if (rows) *rows = (int)m->prows[index];
+    if (cols) *cols = (int)m->pcols[index];
+    if (kind) *kind = m->pkind[index];
+    return NC_OK;
+}
+
+int nc_forward_backward(nc_model* m, const int32_t* tokens, const int32_t* targets,
+                        const int32_t* token_bytes, int B, int T, int accumulate, float grad_scale,
+                        float* loss_bpb_out) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    if (!tokens || !targets || !token_bytes || !loss_bpb_out) return set_error(NC_ERR_ARG, "null pointer");
+    if (B < 1 || T < 1 || T > m->maxT || (long)B * T > m->maxM)
+        return set_error(NC_ERR_ARG, "B=%d T=%d exceeds the arena's max_B*max_T=%ld / max_T=%d", B, T,
+                         m->maxM, m->maxT);
+    if (accumulate != 0 && accumulate != 1) return set_error(NC_ERR_ARG, "accumulate must be 0 or 1");
+    g_gemm_flag = m->flag;
+    if (m->dtype == NC_BF16)
+        return forward_backward<bf16>(m, tokens, targets, token_bytes, B, T, accumulate, grad_scale, loss_bpb_out);
+    return forward_backward<float>(m, tokens, targets, token_bytes, B, T, accumulate, grad_scale, loss_bpb_out);
+}
+
+int nc_muon_step(nc_model* m, float lr, float momentum, int nesterov, int ns_steps, const float ns_coef[3]) {
+    if (!m || !ns_coef) return set_error(NC_ERR_ARG, "null argument");
+    if (ns_steps < 0 || ns_steps > 100) return set_error(NC_ERR_ARG, "ns_steps %d", ns_steps);
+    g_gemm_flag = m->flag;
+    if (m->dtype == NC_BF16) return muon<bf16>(m, lr, momentum, nesterov, ns_steps, ns_coef);
+    return muon<float>(m, lr, momentum, nesterov, ns_steps, ns_coef);
+}
+
+int nc_adamw_step(nc_model* m, float lr_emb, float lr_unemb, float beta1, float beta2, float eps,
+                  float weight_decay, int step) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    if (step < 1) return set_error(NC_ERR_ARG, "step must be >= 1");
+    const float bc1 = (float)(1.0 - pow((double)beta1, step));
+    const float bc2 = (float)(1.0 - pow((double)beta2, step));
+    const long n = (long)m->V * m->d;
+    const int idx[2] = {0, m->nparams - 1};
+    const float lrs[2] = {lr_emb, lr_unemb};
+    for (int k = 0; k < 2; ++k) {
+        const long o = m->poff[idx[k]];
+        NC_TRY(adamw(m->master + o, m->shadow ? m->shadow + o : nullptr, m->grads + o,
+                     m->adam_m + k * n, m->adam_v + k * n, n, lrs[k], beta1, beta2, eps,
+                     weight_decay, bc1, bc2, m->stream));
+    }
+    return NC_OK;
+}
+
+int nc_train_step(nc_model* m, const int32_t* tokens_host, const int32_t* targets_host,
+                  const int32_t* token_bytes, int B, int T, int n_micro, float muon_lr,
+                  float muon_momentum, int ns_steps, const float ns_coef[3], float lr_emb,
+                  float lr_unemb, float beta1, float beta2, float eps, float weight_decay,
+                  int adam_step, float* loss_bpb_host) {
+    if (!m || !tokens_host || !targets_host || !loss_bpb_host) return set_error(NC_ERR_ARG, "null argument");
+    if (n_micro < 1 || n_micro > 64) return set_error(NC_ERR_ARG, "n_micro %d out of [1, 64]", n_micro);
+    if (B < 1 || T < 1 || (long)B * T > m->maxM || T > m->maxT) return set_error(NC_ERR_ARG, "batch too large");
+    const long n = (long)B * T;
+    for (int i = 0; i < n_micro; ++i) {
+        NC_TRY(cuda_check(cudaMemcpyAsync(m->tok_stage, tokens_host + i * n, n * 4, cudaMemcpyHostToDevice,
+                                          m->stream), "H2D tokens"));
+        NC_TRY(cuda_check(cudaMemcpyAsync(m->tok_stage + m->maxM, targets_host + i * n, n * 4,
+                                          cudaMemcpyHostToDevice, m->stream), "H2D targets"));
+        NC_TRY(nc_forward_backward(m, m->tok_stage, m->tok_stage + m->maxM, token_bytes, B, T, i > 0,
+                                   1.0f / n_micro, m->loss + 2 * i));
+    }
+    NC_TRY(nc_muon_step(m, muon_lr, muon_momentum, 1, ns_steps, ns_coef));
+    NC_TRY(nc_adamw_step(m, lr_emb, lr_unemb, beta1, beta2, eps, weight_decay, adam_step));
+    float tmp[128];
+    NC_TRY(cuda_check(cudaMemcpyAsync(tmp, m->loss, (size_t)n_micro * 2 * 4, cudaMemcpyDeviceToHost, m->stream),
+                      "D2H loss"));
+    NC_TRY(cuda_check(cudaStreamSynchronize(m->stream), "sync"));
+    double a = 0, b = 0;
+    for (int i = 0; i < n_micro; ++i) { a += tmp[2 * i]; b += tmp[2 * i + 1]; }
+    loss_bpb_host[0] = (float)(a / n_micro);
+    loss_bpb_host[1] = (float)(b / n_micro);
+    return NC_OK;
+}
+
+int nc_get_params(nc_model* m, int index, float* host, size_t n) {
+    NC_TRY(check_param(m, index, n));
+    if (!host) return set_error(NC_ERR_ARG, "null host buffer");
+    return download_f32(m, host, m->master + m->poff[index], n);
+}
+
+int nc_set_params(nc_model* m, int index, const float* host, size_t n) {
+    NC_TRY(check_param(m, index, n));
+    if (!host) return set_error(NC_ERR_ARG, "null host buffer");
+    NC_TRY(upload_f32(m, m->master + m->poff[index], host, n));
+    if (m->shadow) {
+        NC_TRY(cast_f32_bf16(m->master + m->poff[index], m->shadow + m->poff[index], (long)n, m->stream));
+        return cuda_check(cudaStreamSynchronize(m->stream), "sync");
+    }
+    return NC_OK;
+}
+
+int nc_get_grads(nc_model* m, int index, float* host, size_t n) {
+    NC_TRY(check_param(m, index, n));
+    if (!host) return set_error(NC_ERR_ARG, "null host buffer");
+    return download_f32(m, host, m->grads + m->poff[index], n);
+}
+
+int nc_set_grads(nc_model* m, int index, const float* host, size_t n) {
+    NC_TRY(check_param(m, index, n));
+    if (!host) return set_error(NC_ERR_ARG, "null host buffer");
+    return upload_f32(m, m->grads + m->poff[index], host, n);
+}
+
+static float* state_ptr(nc_model* m, int index, int slot) {
+    const int kind = m->pkind[index];
+    if (kind == NC_KIND_MATRIX) return slot == NC_STATE_MOMENTUM ? m->momentum + m->poff[index] : nullptr;
+    if (slot != NC_STATE_ADAM_M && slot != NC_STATE_ADAM_V) return nullptr;
+    const long n = (long)m->V * m->d;
+    float* base = slot == NC_STATE_ADAM_M ? m->adam_m : m->adam_v;
+    return base + (kind == NC_KIND_EMB ? 0 : n);
+}
+
+int nc_get_state(nc_model* m, int index, int slot, float* host, size_t n) {
+    NC_TRY(check_param(m, index, n));
+    float* p = state_ptr(m, index, slot);
+    if (!p || !host) return set_error(NC_ERR_ARG, "param %d has no state slot %d", index, slot);
+    return download_f32(m, host, p, n);
+}
+
+int nc_set_state(nc_model* m, int index, int slot, const float* host, size_t n) {
+    NC_TRY(check_param(m, index, n));
+    float* p = state_ptr(m, index, slot);
+    if (!p || !host) return set_error(NC_ERR_ARG, "param %d has no state slot %d", index, slot);
+    return upload_f32(m, p, host, n);
+}
+
+int nc_check_device_flag(nc_model* m, uint32_t* flags) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    uint32_t f = 0;
+    NC_TRY(cuda_check(cudaMemcpyAsync(&f, m->flag, 4, cudaMemcpyDeviceToHost, m->stream), "D2H flag"));
+    NC_TRY(cuda_check(cudaMemsetAsync(m->flag, 0, 4, m->stream), "clear flag"));
+    NC_TRY(cuda_check(cudaStreamSynchronize(m->stream), "sync"));
+    if (flags) *flags = f;
+    if (f) return set_error(NC_ERR_DEVICE_FLAG, "device flag 0x%x", f);
+    return NC_OK;
+}
+
+// ------------------------------------------------------------ kernel-level
+int nc_attention_forward(const void* q, const void* k, const void* v, int ld_qkv, void* o, int ld_o,
+                         float* lse, int B, int T, int H, int D, int dtype, void* stream) {
+    if (!q || !k || !v || !o || !lse) return set_error(NC_ERR_ARG, "null pointer");
+    if (B < 0 || T < 0 || H < 1 || D < 2 || D > 128 || D % 2 || ld_qkv < H * D || ld_o < H * D)
+        return set_error(NC_ERR_ARG, "bad attention shape");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == NC_BF16)
+        return attention_forward<bf16>((const bf16*)q, (const bf16*)k, (const bf16*)v, ld_qkv, (bf16*)o,
+                                       ld_o, lse, B, T, H, D, s);
+    if (dtype == NC_FP32)
+        return attention_forward<float>((const float*)q, (const float*)k, (const float*)v, ld_qkv,
+                                        (float*)o, ld_o, lse, B, T, H, D, s);
+    return set_error(NC_ERR_ARG, "dtype %d", dtype);
+}
+
+size_t nc_attention_workspace_bytes(int B, int T, int H) { return (size_t)B * T * H * 4; }
+
+int nc_attention_backward(const void* q, const void* k, const void* v, int ld_qkv, const void* o,
+                          const void* dout, int ld_o, const float* lse, void* dq, void* dk, void* dv,
+                          int ld_dqkv, void* workspace, int B, int T, int H, int D, int dtype,
+                          void* stream) {
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+        return set_error(NC_ERR_ARG, "null pointer");
+    if (B < 0 || T < 0 || H < 1 || D < 2 || D > 128 || D % 2 || ld_qkv < H * D || ld_o < H * D ||
+        ld_dqkv < H * D)
+        return set_error(NC_ERR_ARG, "bad attention shape");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == NC_BF16)
+        return attention_backward<bf16>((const bf16*)q, (const bf16*)k, (const bf16*)v, ld_qkv,
+                                        (const bf16*)o, (const bf16*)dout, ld_o, lse, (bf16*)dq,
+                                        (bf16*)dk, (bf16*)dv, ld_dqkv, (float*)workspace, B, T, H, D, s);
+    if (dtype == NC_FP32)
+        return attention_backward<float>((const float*)q, (const float*)k, (const float*)v, ld_qkv,
+                                         (const float*)o, (const float*)dout, ld_o, lse, (float*)dq,
+                                         (float*)dk, (float*)dv, ld_dqkv, (float*)workspace, B, T, H, D,
+                                         s);
+    return set_error(NC_ERR_ARG, "dtype %d", dtype);
+}
+
+int nc_gemm_bf16(int M, int N, int K, int batch, const void* A, long lda, long stride_a, int trans_a,
+                 const void* B, long ldb, long stride_b, int trans_b, void* C, long ldc, long stride_c,
+                 int c_dtype, float alpha, float beta, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+    if (!A || !B || !C) return set_error(NC_ERR_ARG, "null pointer");
+    if (M < 1 || N < 1 || K < 1 || batch < 1) return set_error(NC_ERR_ARG, "bad GEMM shape");
+    if (c_dtype != NC_BF16 && c_dtype != NC_FP32) return set_error(NC_ERR_ARG, "c_dtype");
+    if (lda < (trans_a ? M : K) || ldb < (trans_b ? N : K) || ldc < N)
+        return set_error(NC_ERR_ARG, "leading dimension too small");
+    Gemm g;
+    g.M = M; g.N = N; g.K = K; g.batch = batch;
+    g.A = A; g.lda = lda; g.sA = stride_a; g.a_t = trans_a != 0;
+    g.B = B; g.ldb = ldb; g.sB = stride_b; g.b_t = trans_b != 0;
+    g.in_dtype = NC_BF16;
+    g.C = C; g.ldc = ldc; g.sC = stride_c; g.c_dtype = c_dtype;
+    g.alpha = alpha; g.beta = beta;
+    if (beta != 0.f) { g.aux = C; g.ldaux = ldc; g.sAux = stride_c; g.aux_dtype = c_dtype; }
+    if (!gemm_tc_supported(g))
+        return set_error(NC_ERR_UNSUPPORTED, "operands must be 16-byte aligned with leading dims % 8 == 0");
+    g_gemm_flag = nullptr;
+    return gemm_tc(g, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,506 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM, TMA-fed).
+//
+// C = alpha * op(A) op(B)^T with the step's fused epilogues (residual add,
+// ReLU^2 forward/backward, axpby, fp32/bf16 stores).  It serves every dense
+// contraction of the step: the q|k|v, attention-output, MLP and LM-head
+// projections (nanochat speedrun walkthrough, lyylswood.com, section 预搜检:
+// 1280 channels, 4x MLP at d20), their two backward products, and the
+// batched Newton-Schulz matmuls of Muon.
+//
+// Design (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A and B k-slices (64 wide, 128-byte swizzle)
+//               into a ring of shared-memory stages;
+//   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16)
+//               from one thread; commits free smem stages and finished
+//               accumulators;
+//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulator (one row per
+//               thread), fused elementwise work, vector stores.
+// The accumulator is double-buffered in TMEM (2 x BN columns) so the
+// epilogue of one tile overlaps the MMAs of the next.  Operands can be
+// K-major or MN-major, so backward products read activations and weights
+// in place (no transposes).  Small-output GEMMs (weight gradients) split K
+// over CTAs into an fp32 scratch and reduce in a fixed order.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace nc {
+namespace {
+
+constexpr int BM = 128, BK = 64, NTHREADS = 192, GROUP_M = 8;
+
+struct TcParams {
+    int M, N, K, batch;
+    int tiles_m, tiles_n, splits, num_kb;
+    long units;
+    void* C; long ldc, sC; int c_dtype;
+    const void* aux; long ldaux, sAux; int aux_dtype;
+    void* C2;
+    float alpha, beta;
+    int epi;
+    float* ws;        // split-K partials [splits][batch][M][N], or null
+    uint32_t* flag;   // device flag word for timeouts (may be null)
+};
+
+template <int BN> struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+};
+
+__device__ __forceinline__ void decode(const TcParams& p, long u, int& b, int& split, int& tm,
+                                       int& tn) {
+    const long tiles = (long)p.tiles_m * p.tiles_n;
+    const long t = u % tiles, bs = u / tiles;
+    split = (int)(bs % p.splits);
+    b = (int)(bs / p.splits);
+    const long per_group = (long)GROUP_M * p.tiles_n;
+    const int g = (int)(t / per_group);
+    const int first_m = g * GROUP_M;
+    const int gsize = min(p.tiles_m - first_m, GROUP_M);
+    const int r = (int)(t % per_group);
+    tm = first_m + r % gsize;
+    tn = r / gsize;
+}
+
+__device__ __forceinline__ void kb_range(const TcParams& p, int split, int& kb0, int& kb1) {
+    kb0 = (int)((long)split * p.num_kb / p.splits);
+    kb1 = (int)((long)(split + 1) * p.num_kb / p.splits);
+}
+
+__device__ __forceinline__ float ld_elem(const void* base, long i, int dt) {
+    return dt == NC_FP32 ? reinterpret_cast<const float*>(base)[i]
+                         : __bfloat162float(reinterpret_cast<const bf16*>(base)[i]);
+}
+
+// load 32 consecutive elements (16-byte aligned) as fp32
+__device__ __forceinline__ void ld32(const void* base, long i, int dt, float* v) {
+    if (dt == NC_FP32) {
+        const float4* s = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + i);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 f = s[j];
+            v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+        }
+    } else {
+        const uint4* s = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(base) + i);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 u = s[j];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+                float2 f = __bfloat1622float2(h);
+                v[8 * j + 2 * e] = f.x;
+                v[8 * j + 2 * e + 1] = f.y;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void st32(void* base, long i, int dt, const float* v) {
+    if (dt == NC_FP32) {
+        float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + i);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    } else {
+        uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(base) + i);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * j + 2 * e], v[8 * j + 2 * e + 1]);
+                w[e] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            d[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+__device__ __forceinline__ void st_elem(void* base, long i, int dt, float v) {
+    if (dt == NC_FP32) reinterpret_cast<float*>(base)[i] = v;
+    else reinterpret_cast<bf16*>(base)[i] = __float2bfloat16_rn(v);
+}
+
+// Epilogue of 32 consecutive columns n0.. of one row.
+__device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, int row, int n0,
+                                           float* v) {
+    const bool full = n0 + 32 <= p.N;
+    const int nv = full ? 32 : p.N - n0;
+    if (p.ws) {
+        const long i = ((long)(split * p.batch + b) * p.M + row) * p.N + n0;
+        if (full) st32(p.ws, i, NC_FP32, v);
+        else for (int j = 0; j < nv; ++j) p.ws[i + j] = v[j];
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] *= p.alpha;
+    const long ci = (long)b * p.sC + (long)row * p.ldc + n0;
+    const long ai = (long)b * p.sAux + (long)row * p.ldaux + n0;
+    if (p.epi == EPI_STORE) {
+        if (p.aux && p.beta != 0.f) {
+            float a[32];
+            if (full) ld32(p.aux, ai, p.aux_dtype, a);
+            else for (int j = 0; j < nv; ++j) a[j] = ld_elem(p.aux, ai + j, p.aux_dtype);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += p.beta * a[j];
+        }
+        if (full) st32(p.C, ci, p.c_dtype, v);
+        else for (int j = 0; j < nv; ++j) st_elem(p.C, ci + j, p.c_dtype, v[j]);
+    } else if (p.epi == EPI_RELU2) {
+        float a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float r = fmaxf(v[j], 0.f);
+            a[j] = r * r;
+        }
+        if (full) {
+            st32(p.C, ci, p.c_dtype, v);
+            st32(p.C2, ci, p.c_dtype, a);
+        } else {
+            for (int j = 0; j < nv; ++j) {
+                st_elem(p.C, ci + j, p.c_dtype, v[j]);
+                st_elem(p.C2, ci + j, p.c_dtype, a[j]);
+            }
+        }
+    } else {  // EPI_RELU2_BWD: dh = da * 2 relu(h)
+        float h[32];
+        if (full) ld32(p.aux, ai, p.aux_dtype, h);
+        else for (int j = 0; j < nv; ++j) h[j] = ld_elem(p.aux, ai + j, p.aux_dtype);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= 2.f * fmaxf(h[j], 0.f);
+        if (full) st32(p.C, ci, p.c_dtype, v);
+        else for (int j = 0; j < nv; ++j) st_elem(p.C, ci + j, p.c_dtype, v[j]);
+    }
+}
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+    using C = Cfg<BN>;
+    constexpr int S = C::STAGES;
+    constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, A_MN, B_MN);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE);
+    uint64_t* empty = full + S;
+    uint64_t* tfull = empty + S;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&tfull[a], 1);
+            tc::mbar_init(&tempty[a], 128);
+        }
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch(&tmA);
+        tc::tma_prefetch(&tmB);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- TMA producer
+        int stage = 0;
+        uint32_t ph = 0;
+        long issued = 0;
+        for (long u = blockIdx.x; u < p.units; u += gridDim.x) {
+            int b, split, tm, tn, kb0, kb1;
+            decode(p, u, b, split, tm, tn);
+            kb_range(p, split, kb0, kb1);
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!tc::mbar_wait(&empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
+                uint8_t* sa = smem + stage * C::STAGE;
+                uint8_t* sb = sa + C::A_BYTES;
+                tc::mbar_expect_tx(&full[stage], C::STAGE);
+                if (!A_MN) {
+                    tc::tma_load_3d(sa, &tmA, &full[stage], kb * BK, tm * BM, b);
+                } else {
+                    tc::tma_load_3d(sa, &tmA, &full[stage], tm * BM, kb * BK, b);
+                    tc::tma_load_3d(sa + 8192, &tmA, &full[stage], tm * BM + 64, kb * BK, b);
+                }
+                if (!B_MN) {
+                    tc::tma_load_3d(sb, &tmB, &full[stage], kb * BK, tn * BN, b);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tc::tma_load_3d(sb + j * 8192, &tmB, &full[stage], tn * BN + j * 64, kb * BK, b);
+                }
+                ++issued;
+                if (++stage == S) { stage = 0; ph ^= 1; }
+            }
+            if (!ok) break;
+        }
+        if (*abort_flag) {
+            // let the copies still in flight land before the CTA exits
+            int st = stage;
+            uint32_t sp = ph;
+            for (long i = 0; i < issued && i < S; ++i) {
+                if (st == 0) { st = S - 1; sp ^= 1; } else { --st; }
+                tc::mbar_wait_drain(&full[st], sp);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------- MMA issuer
+        int stage = 0, acc = 0;
+        uint32_t ph = 0, aph = 0;
+        for (long u = blockIdx.x; u < p.units; u += gridDim.x) {
+            int b, split, tm, tn, kb0, kb1;
+            decode(p, u, b, split, tm, tn);
+            kb_range(p, split, kb0, kb1);
+            if (!tc::mbar_wait(&tempty[acc], aph ^ 1, abort_flag)) break;
+            tc::fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * BN);
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!tc::mbar_wait(&full[stage], ph, abort_flag)) { ok = false; break; }
+                tc::fence_after();
+                const uint32_t a0 = tc::smem_u32(smem + stage * C::STAGE);
+                const uint32_t b0 = a0 + C::A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t ad = A_MN ? tc::sdesc(a0 + kk * 2048, 8192, 1024)
+                                             : tc::sdesc(a0 + kk * 32, 16, 1024);
+                    const uint64_t bd = B_MN ? tc::sdesc(b0 + kk * 2048, 8192, 1024)
+                                             : tc::sdesc(b0 + kk * 32, 16, 1024);
+                    tc::mma_bf16(d, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(&empty[stage]);
+                if (++stage == S) { stage = 0; ph ^= 1; }
+            }
+            if (!ok) break;
+            tc::mma_commit(&tfull[acc]);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1;
+        }
+        if (*abort_flag) {
+            tc::mma_commit(drain);
+            tc::mbar_wait_drain(drain, 0);
+        }
+    } else if (warp >= 2) {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (long u = blockIdx.x; u < p.units; u += gridDim.x) {
+            int b, split, tm, tn;
+            decode(p, u, b, split, tm, tn);
+            if (!tc::mbar_wait(&tfull[acc], aph, abort_flag)) break;
+            tc::fence_after();
+            const int row = tm * BM + q * 32 + lane;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tc::tmem_ld32(tbase + c * 32, r);
+                tc::tmem_wait_ld();
+                const int n0 = tn * BN + c * 32;
+                if (row < p.M && n0 < p.N) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    epilogue32(p, b, split, row, n0, v);
+                }
+            }
+            tc::fence_before();
+            tc::mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1;
+        }
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag && p.flag) atomicOr(p.flag, NC_FLAG_TIMEOUT);
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// C = alpha * sum_s ws[s] + beta * aux, fixed summation order.
+__global__ void splitk_reduce_kernel(const float* ws, int splits, int batch, int M, int N, void* C,
+                                     long ldc, long sC, int c_dtype, const void* aux, long ldaux,
+                                     long sAux, int aux_dtype, float alpha, float beta) {
+    const long total = (long)batch * M * N;
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const long n = i % N, m = (i / N) % M, b = i / ((long)N * M);
+    float s = 0.f;
+    for (int k = 0; k < splits; ++k) s += ws[(long)k * total + i];
+    s *= alpha;
+    if (aux && beta != 0.f) s += beta * ld_elem(aux, b * sAux + m * ldaux + n, aux_dtype);
+    st_elem(C, b * sC + m * ldc + n, c_dtype, s);
+}
+
+// ------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map over [batch][outer][inner] (row stride ld, batch stride bs, in elements).
+int make_map(CUtensorMap* m, const void* ptr, long inner, long outer, long batch, long ld, long bs,
+             int box_inner, int box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return set_error(NC_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    if (batch <= 1) bs = ld * outer;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)(batch < 1 ? 1 : batch)};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)bs * 2};
+    cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(NC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d): inner %ld outer %ld ld %ld",
+                         (int)r, inner, outer, ld);
+    return NC_OK;
+}
+
+int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+template <int BN, bool A_MN, bool B_MN>
+int launch(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cudaStream_t s) {
+    using C = Cfg<BN>;
+    static bool attr = false;
+    if (!attr) {
+        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
+                          "gemm_tc smem attribute"));
+        attr = true;
+    }
+    const long grid = p.units < num_sms() ? p.units : num_sms();
+    gemm_tc_kernel<BN, A_MN, B_MN><<<(int)grid, NTHREADS, C::SMEM, s>>>(ma, mb, p);
+    note_launch();
+    NC_LAUNCH_CHECK("gemm_tc");
+    return NC_OK;
+}
+
+int pick_splits(const Gemm& g, int tiles, int num_kb) {
+    const long work = (long)tiles * g.batch;
+    const int sms = num_sms();
+    if (work >= sms || num_kb < 8 || g.epi != EPI_STORE) return 1;
+    int s = (int)((2L * sms + work - 1) / work);
+    s = s < num_kb / 4 ? s : num_kb / 4;
+    s = s < 32 ? s : 32;
+    return s < 1 ? 1 : s;
+}
+
+}  // namespace
+
+uint32_t* g_gemm_flag = nullptr;  // device flag word of the current model (set by the engine)
+
+bool gemm_tc_supported(const Gemm& g) {
+    if (g.in_dtype != NC_BF16) return false;
+    if (g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
+    if (g.lda % 8 || g.ldb % 8 || g.ldc % 8 || (g.aux && g.ldaux % 8)) return false;
+    if (g.batch > 1 && (g.sA % 8 || g.sB % 8)) return false;
+    if ((uintptr_t)g.A % 16 || (uintptr_t)g.B % 16 || (uintptr_t)g.C % 16) return false;
+    if (g.C2 && (uintptr_t)g.C2 % 16) return false;
+    if (g.aux && (uintptr_t)g.aux % 16) return false;
+    if (g.N % 8) return false;
+    return true;
+}
+
+size_t gemm_tc_splitk_bytes(const Gemm& g) {
+    const int bn = g.N > 128 ? 256 : 128;
+    const int tiles = ceil_div(g.M, BM) * ceil_div(g.N, bn);
+    const int s = pick_splits(g, tiles, ceil_div(g.K, BK));
+    return s > 1 ? (size_t)s * g.batch * g.M * g.N * 4 : 0;
+}
+
+int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
+    if (!gemm_tc_supported(g)) return set_error(NC_ERR_UNSUPPORTED, "gemm_tc: unsupported operands");
+    const int bn = g.N > 128 ? 256 : 128;
+    TcParams p{};
+    p.M = g.M; p.N = g.N; p.K = g.K; p.batch = g.batch;
+    p.tiles_m = ceil_div(g.M, BM);
+    p.tiles_n = ceil_div(g.N, bn);
+    p.num_kb = ceil_div(g.K, BK);
+    p.splits = pick_splits(g, p.tiles_m * p.tiles_n, p.num_kb);
+    size_t need = p.splits > 1 ? (size_t)p.splits * g.batch * g.M * g.N * 4 : 0;
+    if (need > ws_bytes || ws == nullptr) p.splits = 1;
+    p.units = (long)p.tiles_m * p.tiles_n * p.splits * g.batch;
+    p.C = g.C; p.ldc = g.ldc; p.sC = g.sC; p.c_dtype = g.c_dtype;
+    p.aux = g.aux; p.ldaux = g.ldaux; p.sAux = g.sAux; p.aux_dtype = g.aux_dtype;
+    p.C2 = g.C2; p.alpha = g.alpha; p.beta = g.beta; p.epi = g.epi;
+    p.ws = p.splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+    p.flag = g_gemm_flag;
+
+    CUtensorMap ma, mb;
+    if (!g.a_t) NC_TRY(make_map(&ma, g.A, g.K, g.M, g.batch, g.lda, g.sA, 64, BM));
+    else        NC_TRY(make_map(&ma, g.A, g.M, g.K, g.batch, g.lda, g.sA, 64, 64));
+    if (!g.b_t) NC_TRY(make_map(&mb, g.B, g.K, g.N, g.batch, g.ldb, g.sB, 64, bn));
+    else        NC_TRY(make_map(&mb, g.B, g.N, g.K, g.batch, g.ldb, g.sB, 64, 64));
+
+    int rc;
+    if (bn == 256) {
+        if (!g.a_t && !g.b_t) rc = launch<256, false, false>(ma, mb, p, s);
+        else if (!g.a_t && g.b_t) rc = launch<256, false, true>(ma, mb, p, s);
+        else if (g.a_t && !g.b_t) rc = launch<256, true, false>(ma, mb, p, s);
+        else rc = launch<256, true, true>(ma, mb, p, s);
+    } else {
+        if (!g.a_t && !g.b_t) rc = launch<128, false, false>(ma, mb, p, s);
+        else if (!g.a_t && g.b_t) rc = launch<128, false, true>(ma, mb, p, s);
+        else if (g.a_t && !g.b_t) rc = launch<128, true, false>(ma, mb, p, s);
+        else rc = launch<128, true, true>(ma, mb, p, s);
+    }
+    NC_TRY(rc);
+    if (p.splits > 1) {
+        const long total = (long)g.batch * g.M * g.N;
+        splitk_reduce_kernel<<<ceil_div(total, 256), 256, 0, s>>>(
+            p.ws, p.splits, g.batch, g.M, g.N, g.C, g.ldc, g.sC, g.c_dtype, g.aux, g.ldaux, g.sAux,
+            g.aux_dtype, g.alpha, g.beta);
+        note_launch();
+        NC_LAUNCH_CHECK("splitk_reduce");
+    }
+    return NC_OK;
+}
+
+}  // namespace nc

@@ -1,0 +1,94 @@
+// Internal launch interface of libnc's kernels (raw pointers + a stream).
+#pragma once
+
+#include "common.cuh"
+#include "optim.cuh"
+
+namespace nc {
+
+// ------------------------------------------------------------ GEMM
+// C = alpha * op(A) op(B)^T (+ epilogue), op(A) [M, K], op(B) [N, K].
+enum EpiKind {
+    EPI_STORE = 0,      // C = alpha*acc + beta*aux            (aux may alias C)
+    EPI_RELU2 = 1,      // C = alpha*acc (pre-activation h), C2 = relu(h)^2
+    EPI_RELU2_BWD = 2,  // C = alpha*acc * 2*relu(aux)          (aux = h)
+};
+
+struct Gemm {
+    int M = 0, N = 0, K = 0, batch = 1;
+    const void* A = nullptr; long lda = 0, sA = 0; bool a_t = false;  // a_t: A stored [K, M]
+    const void* B = nullptr; long ldb = 0, sB = 0; bool b_t = false;  // b_t: B stored [K, N]
+    int in_dtype = NC_BF16;
+    void* C = nullptr; long ldc = 0, sC = 0; int c_dtype = NC_BF16;
+    const void* aux = nullptr; long ldaux = 0, sAux = 0; int aux_dtype = NC_BF16;
+    void* C2 = nullptr;
+    float alpha = 1.f, beta = 0.f;
+    int epi = EPI_STORE;
+};
+
+int gemm_simt(const Gemm& g, cudaStream_t s);
+// tcgen05/TMA path (bf16 operands).  ws: fp32 split-K scratch (may be null).
+int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s);
+size_t gemm_tc_splitk_bytes(const Gemm& g);
+bool gemm_tc_supported(const Gemm& g);
+
+// ------------------------------------------------------------ row ops
+template <typename T>
+int embed_forward(const int32_t* tok, const T* wte, float* x, int M, int d, int V,
+                  uint32_t* flag, cudaStream_t s);
+template <typename T>
+int rmsnorm_forward(const float* x, T* y, float* r, int M, int d, cudaStream_t s);
+// g_out = g_in + r*(dy - y*mean(dy*y)); g_out may alias g_in; gT optional copy
+template <typename T>
+int rmsnorm_backward(const float* dy, const T* y, const float* r, const float* g_in,
+                     float* g_out, T* gT, int M, int d, cudaStream_t s);
+// in place on the q and k thirds of qkv rows (row stride ld): sign +1 fwd, -1 bwd
+template <typename T>
+int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* table, float sign,
+               cudaStream_t s);
+// logits [M, V] -> dlogits in place; nll [M]
+template <typename T>
+int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float scale,
+                  uint32_t* flag, cudaStream_t s);
+int loss_reduce(const float* nll, const int32_t* tgt, const int32_t* token_bytes, int M, int V,
+                float* out, uint32_t* flag, cudaStream_t s);
+struct EmbedBwdWs {
+    int* hist;       // [nchunks * V]
+    int* rank;       // [M]
+    int* offsets;    // [V + 1]
+    int* sorted;     // [M]
+    float* head;     // [npieces * d]
+    float* tail;     // [npieces * d]
+};
+size_t embed_backward_ws_bytes(int M, int d, int V);
+EmbedBwdWs embed_backward_ws(void* base, int M, int d, int V);
+int embed_backward(const int32_t* tok, const float* g, float* dwte, int M, int d, int V,
+                   int accumulate, const EmbedBwdWs& ws, cudaStream_t s);
+
+// ------------------------------------------------------------ attention
+template <typename T>
+int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ldo, float* lse,
+                      int B, int T_, int H, int D, cudaStream_t s);
+template <typename T>
+int attention_backward(const T* q, const T* k, const T* v, long ld, const T* o, const T* dout,
+                       long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
+                       int B, int T_, int H, int D, cudaStream_t s);
+
+// ------------------------------------------------------------ optimizers
+// Muon, phase 1: buf = mu*buf + g; g <- g + mu*buf (nesterov) or buf; per-CTA
+// sums of squares of the new g into partial[mat * chunks + chunk].
+int muon_momentum(float* g, float* buf, const MuonMat* mats, int nmat, float mu, int nesterov,
+                  float* partial, int chunks, cudaStream_t s);
+// Muon, phase 2: X = g / (|g|_F + 1e-7), written (transposed when tr) into x.
+template <typename T>
+int muon_normalize(const float* g, const MuonMat* mats, int nmat, const float* partial, int chunks,
+                   T* x, int blocks_per_mat, cudaStream_t s);
+// Muon, phase 4: W -= lr*scale*X (X read transposed when tr); refresh the bf16 copy.
+template <typename T>
+int muon_apply(float* w, bf16* w16, const MuonMat* mats, int nmat, const T* x, float lr,
+               int blocks_per_mat, cudaStream_t s);
+int adamw(float* w, bf16* w16, const float* g, float* m, float* v, long n, float lr, float b1,
+          float b2, float eps, float wd, float bc1, float bc2, cudaStream_t s);
+int cast_f32_bf16(const float* x, bf16* y, long n, cudaStream_t s);
+
+}  // namespace nc

@@ -1,0 +1,458 @@
+// Row-wise, HBM-bound kernels of the step: embedding lookup and its sorted
+// segment-sum backward, parameter-free RMSNorm forward/backward, RoPE, the
+// softmax cross-entropy with its bits-per-byte reduction, and casts.
+//
+// Source: nanochat speedrun walkthrough (lyylswood.com), section 预搜检
+// (pretraining): no RMSNorm gains, no biases, validation bits per byte =
+// per-token loss normalised by the bytes each token stands for.
+#include "kernels.cuh"
+
+#include <math.h>
+
+namespace nc {
+namespace {
+
+constexpr float RMS_EPS = 1e-6f;
+
+__device__ __forceinline__ void flag_set(uint32_t* flag, uint32_t bits) {
+    if (flag) atomicOr(flag, bits);
+}
+
+template <typename T> __device__ __forceinline__ void store4(T* p, float4 v);
+template <> __device__ __forceinline__ void store4<float>(float* p, float4 v) {
+    *reinterpret_cast<float4*>(p) = v;
+}
+template <> __device__ __forceinline__ void store4<bf16>(bf16* p, float4 v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+template <typename T> __device__ __forceinline__ float4 load4(const T* p);
+template <> __device__ __forceinline__ float4 load4<float>(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <> __device__ __forceinline__ float4 load4<bf16>(const bf16* p) {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&u.x);
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+    float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+
+// ------------------------------------------------------------ embedding
+template <typename T>
+__global__ void embed_fwd_kernel(const int32_t* tok, const T* wte, float* x, int M, int d, int V,
+                                 uint32_t* flag) {
+    const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (row >= M) return;
+    int t = tok[row];
+    float* xr = x + (long)row * d;
+    if (t < 0 || t >= V) {
+        if (lane == 0) flag_set(flag, NC_FLAG_TOKEN_RANGE);
+        for (int i = lane * 4; i < d; i += 128) store4<float>(xr + i, make_float4(0, 0, 0, 0));
+        return;
+    }
+    const T* wr = wte + (long)t * d;
+    for (int i = lane * 4; i < d; i += 128) store4<float>(xr + i, load4<T>(wr + i));
+}
+
+// ------------------------------------------------------------ RMSNorm
+// One warp per row: y = x / sqrt(mean(x^2) + eps), r = 1 / sqrt(mean(x^2) + eps).
+template <typename T>
+__global__ void rmsnorm_fwd_kernel(const float* x, T* y, float* r, int M, int d) {
+    const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (row >= M) return;
+    const float* xr = x + (long)row * d;
+    float ss = 0.f;
+    for (int i = lane * 4; i < d; i += 128) {
+        float4 v = load4<float>(xr + i);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = warp_sum(ss);
+    float rr = 1.0f / sqrtf(ss / (float)d + RMS_EPS);
+    if (lane == 0) r[row] = rr;
+    T* yr = y + (long)row * d;
+    for (int i = lane * 4; i < d; i += 128) {
+        float4 v = load4<float>(xr + i);
+        store4<T>(yr + i, make_float4(v.x * rr, v.y * rr, v.z * rr, v.w * rr));
+    }
+}
+
+// g_out = g_in + r * (dy - y * mean(dy * y)) (g_in null = 0); optional low-precision copy gT.
+template <typename T>
+__global__ void rmsnorm_bwd_kernel(const float* dy, const T* y, const float* r, const float* g_in,
+                                   float* g_out, T* gT, int M, int d) {
+    const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (row >= M) return;
+    const long o = (long)row * d;
+    float dot = 0.f;
+    for (int i = lane * 4; i < d; i += 128) {
+        float4 a = load4<float>(dy + o + i), b = load4<T>(y + o + i);
+        dot += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+    }
+    dot = warp_sum(dot) / (float)d;
+    const float rr = r[row];
+    for (int i = lane * 4; i < d; i += 128) {
+        float4 a = load4<float>(dy + o + i), b = load4<T>(y + o + i);
+        float4 g = g_in ? load4<float>(g_in + o + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 out = make_float4(g.x + rr * (a.x - b.x * dot), g.y + rr * (a.y - b.y * dot),
+                                 g.z + rr * (a.z - b.z * dot), g.w + rr * (a.w - b.w * dot));
+        store4<float>(g_out + o + i, out);
+        if (gT) store4<T>(gT + o + i, out);
+    }
+}
+
+// ------------------------------------------------------------ RoPE
+// Rotates pairs (j, j + Dh/2) of every q and k head by sign * angle(t, j).
+template <typename T>
+__global__ void rope_kernel(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* table,
+                            float sign) {
+    const int half = Dh / 2;
+    long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    long total = (long)M * H * half;
+    if (idx >= total) return;
+    int j = idx % half;
+    long rh = idx / half;
+    int h = rh % H;
+    long row = rh / H;
+    int t = row % T_;
+    float2 cs = table[(long)t * half + j];
+    float c = cs.x, sn = sign * cs.y;
+    T* base = qkv + row * ld + (long)h * Dh;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {  // q, then k (offset H*Dh)
+        T* p = base + (long)part * H * Dh;
+        float x1 = to_f<T>(p[j]), x2 = to_f<T>(p[j + half]);
+        p[j] = from_f<T>(x1 * c - x2 * sn);
+        p[j + half] = from_f<T>(x2 * c + x1 * sn);
+    }
+}
+
+// ------------------------------------------------------------ cross-entropy
+constexpr int CE_THREADS = 512;
+
+__device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
+    const int lane = threadIdx.x % 32, w = threadIdx.x / 32, nw = blockDim.x / 32;
+    v = is_max ? warp_max(v) : warp_sum(v);
+    __syncthreads();
+    if (lane == 0) sh[w] = v;
+    __syncthreads();
+    float t = lane < nw ? sh[lane] : (is_max ? -INFINITY : 0.f);
+    t = is_max ? warp_max(t) : warp_sum(t);
+    return t;
+}
+
+// One CTA per row: lse = logsumexp(z); nll = lse - z[target];
+// z <- scale * (softmax(z) - onehot(target)) in place.
+template <typename T>
+__global__ void __launch_bounds__(CE_THREADS) ce_kernel(T* z, const int32_t* tgt, float* nll, int V,
+                                                        float scale, uint32_t* flag) {
+    __shared__ float sh[32];
+    __shared__ float zt_s;
+    const long row = blockIdx.x;
+    T* zr = z + row * V;
+    const int t = tgt[row];
+    const bool ok = t >= 0 && t < V;
+    if (threadIdx.x == 0) {
+        if (!ok) flag_set(flag, NC_FLAG_TOKEN_RANGE);
+        zt_s = ok ? to_f<T>(zr[t]) : 0.f;
+    }
+    float mx = -INFINITY;
+    for (int j = threadIdx.x; j < V; j += blockDim.x) mx = fmaxf(mx, to_f<T>(zr[j]));
+    mx = block_reduce(mx, sh, true);
+    float se = 0.f;
+    for (int j = threadIdx.x; j < V; j += blockDim.x) se += expf(to_f<T>(zr[j]) - mx);
+    se = block_reduce(se, sh, false);
+    const float lse = mx + logf(se);
+    __syncthreads();  // zt_s was read before any thread overwrites z
+    if (threadIdx.x == 0) nll[row] = ok ? lse - zt_s : 0.f;
+    for (int j = threadIdx.x; j < V; j += blockDim.x) {
+        float p = expf(to_f<T>(zr[j]) - lse);
+        if (j == t) p -= 1.f;
+        zr[j] = from_f<T>(p * scale);
+    }
+}
+
+// Single CTA, fixed summation order: loss = mean nll; bpb = sum(nll | bytes>0) / (ln2 * sum bytes).
+__global__ void loss_reduce_kernel(const float* nll, const int32_t* tgt, const int32_t* tb, int M,
+                                   int V, float* out, uint32_t* flag) {
+    __shared__ double s_nll[1024], s_pos[1024], s_bytes[1024];
+    double a = 0, b = 0, c = 0;
+    for (int i = threadIdx.x; i < M; i += blockDim.x) {
+        double l = nll[i];
+        int t = tgt[i];
+        int nb = (t >= 0 && t < V) ? tb[t] : 0;
+        a += l;
+        if (nb > 0) { b += l; c += nb; }
+    }
+    s_nll[threadIdx.x] = a;
+    s_pos[threadIdx.x] = b;
+    s_bytes[threadIdx.x] = c;
+    __syncthreads();
+    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+        if (threadIdx.x < s) {
+            s_nll[threadIdx.x] += s_nll[threadIdx.x + s];
+            s_pos[threadIdx.x] += s_pos[threadIdx.x + s];
+            s_bytes[threadIdx.x] += s_bytes[threadIdx.x + s];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        float loss = (float)(s_nll[0] / M);
+        float bpb = s_bytes[0] > 0 ? (float)(s_pos[0] / (0.6931471805599453 * s_bytes[0])) : 0.f;
+        if (!isfinite(loss)) flag_set(flag, NC_FLAG_NONFINITE);
+        out[0] = loss;
+        out[1] = bpb;
+    }
+}
+
+// ------------------------------------------------------------ embedding backward
+// dwte[v] = sum of g rows whose token is v, summed in row order (deterministic):
+// a stable counting sort of rows by token id, then fixed-size pieces of the
+// sorted list are summed; runs cut by piece borders are combined in order.
+constexpr int EB_CHUNK = 1024;  // rows per rank chunk
+constexpr int EB_PIECE = 64;    // sorted rows per summation piece
+constexpr int EB_COLS = 256;    // columns per summation CTA
+
+__global__ void __launch_bounds__(EB_CHUNK) eb_hist_rank_kernel(const int32_t* tok, int* hist,
+                                                                 int* rank, int M, int V) {
+    __shared__ int st[EB_CHUNK];
+    const int c = blockIdx.x, i = threadIdx.x;
+    const long r = (long)c * EB_CHUNK + i;
+    int t = r < M ? tok[r] : -1;
+    if (t >= V) t = -1;
+    st[i] = t;
+    __syncthreads();
+    if (t < 0) return;
+    int cnt = 0;
+    for (int j = 0; j < i; ++j) cnt += (st[j] == t);
+    rank[r] = cnt;
+    atomicAdd(&hist[(long)c * V + t], 1);
+}
+
+__global__ void eb_colscan_kernel(int* hist, int* counts, int nchunks, int V) {
+    int v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= V) return;
+    int run = 0;
+    for (int c = 0; c < nchunks; ++c) {
+        int h = hist[(long)c * V + v];
+        hist[(long)c * V + v] = run;
+        run += h;
+    }
+    counts[v] = run;
+}
+
+// exclusive scan of counts[0..V) in place, offsets[V] = total; one CTA of 1024
+__global__ void __launch_bounds__(1024) eb_scan_kernel(int* offsets, int V) {
+    __shared__ int part[1024];
+    const int per = (V + 1023) / 1024;
+    const int b = threadIdx.x * per, e = min(V, b + per);
+    int s = 0;
+    for (int i = b; i < e; ++i) s += offsets[i];
+    part[threadIdx.x] = s;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {
+        int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int run = part[threadIdx.x] - s;
+    for (int i = b; i < e; ++i) {
+        int c = offsets[i];
+        offsets[i] = run;
+        run += c;
+    }
+    if (threadIdx.x == 1023) offsets[V] = part[1023];
+}
+
+__global__ void eb_scatter_kernel(const int32_t* tok, const int* hist, const int* rank,
+                                  const int* offsets, int* sorted, int M, int V) {
+    long r = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= M) return;
+    int t = tok[r];
+    if (t < 0 || t >= V) return;
+    long c = r / EB_CHUNK;
+    sorted[offsets[t] + hist[c * V + t] + rank[r]] = (int)r;
+}
+
+__global__ void __launch_bounds__(EB_COLS) eb_piece_kernel(const int32_t* tok, const int* sorted,
+                                                           const int* offsets, const float* g,
+                                                           float* dwte, float* head, float* tail,
+                                                           int d, int V, int accumulate) {
+    const int piece = blockIdx.x, col = blockIdx.y * EB_COLS + threadIdx.x;
+    const int Mv = offsets[V];
+    const int p0 = piece * EB_PIECE, p1 = min(p0 + EB_PIECE, Mv);
+    if (p0 >= Mv || col >= d) return;
+    float acc = 0.f;
+    int run_start = p0;
+    int id = tok[sorted[p0]];
+    for (int p = p0; p < p1; ++p) {
+        const int r = sorted[p];
+        acc += g[(long)r * d + col];
+        const int next = (p + 1 < p1) ? tok[sorted[p + 1]] : -1;
+        if (next != id) {
+            const int off = offsets[id], cnt = offsets[id + 1] - off;
+            if (off >= p0 && off + cnt <= p1) {
+                float* dst = dwte + (long)id * d + col;
+                *dst = accumulate ? *dst + acc : acc;
+            } else if (run_start == p0) {
+                head[(long)piece * d + col] = acc;
+            } else {
+                tail[(long)piece * d + col] = acc;
+            }
+            acc = 0.f;
+            run_start = p + 1;
+            id = next;
+        }
+    }
+}
+
+__global__ void eb_fixup_kernel(const int* offsets, const float* head, const float* tail,
+                                float* dwte, int d, int accumulate) {
+    const int id = blockIdx.x;
+    const int off = offsets[id], cnt = offsets[id + 1] - off;
+    if (cnt == 0) return;
+    const int pa = off / EB_PIECE, pb = (off + cnt - 1) / EB_PIECE;
+    if (pa == pb) return;
+    for (int col = threadIdx.x; col < d; col += blockDim.x) {
+        float s = (off == pa * EB_PIECE) ? head[(long)pa * d + col] : tail[(long)pa * d + col];
+        for (int p = pa + 1; p <= pb; ++p) s += head[(long)p * d + col];
+        float* dst = dwte + (long)id * d + col;
+        *dst = accumulate ? *dst + s : s;
+    }
+}
+
+__global__ void cast_kernel(const float* x, bf16* y, long n) {
+    long i = ((long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i + 3 < n) {
+        store4<bf16>(y + i, load4<float>(x + i));
+    } else {
+        for (; i < n; ++i) y[i] = __float2bfloat16_rn(x[i]);
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ launchers
+template <typename T>
+int embed_forward(const int32_t* tok, const T* wte, float* x, int M, int d, int V, uint32_t* flag,
+                  cudaStream_t s) {
+    if (M <= 0) return NC_OK;
+    embed_fwd_kernel<T><<<ceil_div(M, 8), 256, 0, s>>>(tok, wte, x, M, d, V, flag);
+    note_launch();
+    NC_LAUNCH_CHECK("embed_forward");
+    return NC_OK;
+}
+
+template <typename T>
+int rmsnorm_forward(const float* x, T* y, float* r, int M, int d, cudaStream_t s) {
+    if (M <= 0) return NC_OK;
+    rmsnorm_fwd_kernel<T><<<ceil_div(M, 8), 256, 0, s>>>(x, y, r, M, d);
+    note_launch();
+    NC_LAUNCH_CHECK("rmsnorm_forward");
+    return NC_OK;
+}
+
+template <typename T>
+int rmsnorm_backward(const float* dy, const T* y, const float* r, const float* g_in, float* g_out,
+                     T* gT, int M, int d, cudaStream_t s) {
+    if (M <= 0) return NC_OK;
+    rmsnorm_bwd_kernel<T><<<ceil_div(M, 8), 256, 0, s>>>(dy, y, r, g_in, g_out, gT, M, d);
+    note_launch();
+    NC_LAUNCH_CHECK("rmsnorm_backward");
+    return NC_OK;
+}
+
+template <typename T>
+int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* table, float sign,
+               cudaStream_t s) {
+    long total = (long)M * H * (Dh / 2);
+    if (total <= 0) return NC_OK;
+    rope_kernel<T><<<ceil_div(total, 256), 256, 0, s>>>(qkv, ld, M, T_, H, Dh, table, sign);
+    note_launch();
+    NC_LAUNCH_CHECK("rope_apply");
+    return NC_OK;
+}
+
+template <typename T>
+int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float scale,
+                  uint32_t* flag, cudaStream_t s) {
+    if (M <= 0) return NC_OK;
+    ce_kernel<T><<<M, CE_THREADS, 0, s>>>(logits, tgt, nll, V, scale, flag);
+    note_launch();
+    NC_LAUNCH_CHECK("cross_entropy");
+    return NC_OK;
+}
+
+int loss_reduce(const float* nll, const int32_t* tgt, const int32_t* token_bytes, int M, int V,
+                float* out, uint32_t* flag, cudaStream_t s) {
+    loss_reduce_kernel<<<1, 1024, 0, s>>>(nll, tgt, token_bytes, M, V, out, flag);
+    note_launch();
+    NC_LAUNCH_CHECK("loss_reduce");
+    return NC_OK;
+}
+
+static size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+size_t embed_backward_ws_bytes(int M, int d, int V) {
+    long nchunks = ceil_div(M, EB_CHUNK), npieces = ceil_div(M, EB_PIECE);
+    return al256(nchunks * V * 4) + al256((size_t)M * 4) + al256(((size_t)V + 1) * 4) +
+           al256((size_t)M * 4) + 2 * al256((size_t)npieces * d * 4);
+}
+
+EmbedBwdWs embed_backward_ws(void* base, int M, int d, int V) {
+    long nchunks = ceil_div(M, EB_CHUNK), npieces = ceil_div(M, EB_PIECE);
+    char* p = (char*)base;
+    EmbedBwdWs w;
+    w.hist = (int*)p;    p += al256(nchunks * V * 4);
+    w.rank = (int*)p;    p += al256((size_t)M * 4);
+    w.offsets = (int*)p; p += al256(((size_t)V + 1) * 4);
+    w.sorted = (int*)p;  p += al256((size_t)M * 4);
+    w.head = (float*)p;  p += al256((size_t)npieces * d * 4);
+    w.tail = (float*)p;
+    return w;
+}
+
+int embed_backward(const int32_t* tok, const float* g, float* dwte, int M, int d, int V,
+                   int accumulate, const EmbedBwdWs& ws, cudaStream_t s) {
+    const int nchunks = ceil_div(M, EB_CHUNK), npieces = ceil_div(M, EB_PIECE);
+    if (!accumulate) NC_TRY(cuda_check(cudaMemsetAsync(dwte, 0, (size_t)V * d * 4, s), "memset dwte"));
+    if (M <= 0) return NC_OK;
+    NC_TRY(cuda_check(cudaMemsetAsync(ws.hist, 0, (size_t)nchunks * V * 4, s), "memset hist"));
+    eb_hist_rank_kernel<<<nchunks, EB_CHUNK, 0, s>>>(tok, ws.hist, ws.rank, M, V);
+    eb_colscan_kernel<<<ceil_div(V, 256), 256, 0, s>>>(ws.hist, ws.offsets, nchunks, V);
+    eb_scan_kernel<<<1, 1024, 0, s>>>(ws.offsets, V);
+    eb_scatter_kernel<<<ceil_div(M, 256), 256, 0, s>>>(tok, ws.hist, ws.rank, ws.offsets, ws.sorted, M, V);
+    eb_piece_kernel<<<dim3(npieces, ceil_div(d, EB_COLS)), EB_COLS, 0, s>>>(
+        tok, ws.sorted, ws.offsets, g, dwte, ws.head, ws.tail, d, V, accumulate);
+    eb_fixup_kernel<<<V, 256, 0, s>>>(ws.offsets, ws.head, ws.tail, dwte, d, accumulate);
+    note_launch(6);
+    NC_LAUNCH_CHECK("embed_backward");
+    return NC_OK;
+}
+
+int cast_f32_bf16(const float* x, bf16* y, long n, cudaStream_t s) {
+    if (n <= 0) return NC_OK;
+    cast_kernel<<<ceil_div(ceil_div(n, 4), 256), 256, 0, s>>>(x, y, n);
+    note_launch();
+    NC_LAUNCH_CHECK("cast_f32_bf16");
+    return NC_OK;
+}
+
+#define NC_INST(T)                                                                              \
+    template int embed_forward<T>(const int32_t*, const T*, float*, int, int, int, uint32_t*,   \
+                                  cudaStream_t);                                                \
+    template int rmsnorm_forward<T>(const float*, T*, float*, int, int, cudaStream_t);          \
+    template int rmsnorm_backward<T>(const float*, const T*, const float*, const float*, float*, \
+                                     T*, int, int, cudaStream_t);                               \
+    template int rope_apply<T>(T*, long, int, int, int, int, const float2*, float, cudaStream_t); \
+    template int cross_entropy<T>(T*, const int32_t*, float*, int, int, float, uint32_t*,       \
+                                  cudaStream_t);
+NC_INST(float)
+NC_INST(bf16)
+#undef NC_INST
+
+}  // namespace nc

@@ -1,0 +1,84 @@
+"""Causal attention kernels through the C ABI against the fp64 oracle.
+
+bf16 inputs ~ N(0, 1) (the attention microbenchmark's distribution), fp32
+softmax statistics.  Tolerances: bf16 cosine >= 0.999, max-rel <= 2e-2;
+fp32 max-rel <= 1e-5 (outputs) / 1e-4 (gradients).
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from tests._util import assert_close, bf16_round
+
+pytestmark = pytest.mark.gpu
+
+
+def _attn(B, T, H, D, mode, seed=0, sample=None):
+    import torch
+    from pretraining_step_03_b300 import _lib as L
+    rng = np.random.default_rng(seed)
+    q, k, v, do = (rng.normal(size=(B, T, H, D)).astype(np.float32) for _ in range(4))
+    if mode == "bf16":
+        q, k, v, do = (bf16_round(x) for x in (q, k, v, do))
+    tdt = torch.bfloat16 if mode == "bf16" else torch.float32
+    dev = torch.device("cuda")
+    Q, K, Vv, DO = (torch.from_numpy(x).to(dev, tdt) for x in (q, k, v, do))
+    O = torch.empty_like(Q)
+    lse = torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    dQ, dK, dV = (torch.empty_like(Q) for _ in range(3))
+    ws = torch.empty(L.nc_attention_workspace_bytes(B, T, H), dtype=torch.uint8, device=dev)
+    dtc = L.NC_BF16 if mode == "bf16" else L.NC_FP32
+    s = torch.cuda.current_stream().cuda_stream
+    L.nc_attention_forward(Q.data_ptr(), K.data_ptr(), Vv.data_ptr(), H * D, O.data_ptr(), H * D,
+                           lse.data_ptr(), B, T, H, D, dtc, s)
+    # the backward consumes the kernel's own O (as the training step does)
+    L.nc_attention_backward(Q.data_ptr(), K.data_ptr(), Vv.data_ptr(), H * D, O.data_ptr(), DO.data_ptr(),
+                            H * D, lse.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), H * D,
+                            ws.data_ptr(), B, T, H, D, dtc, s)
+    torch.cuda.synchronize()
+    got = [x.float().cpu().numpy() for x in (O, lse, dQ, dK, dV)]
+    bs = range(B) if sample is None else sample
+    refs = []
+    for b in bs:
+        sl = slice(b, b + 1)
+        o, p, l = oracle.causal_attention(q[sl], k[sl], v[sl])
+        dq, dk, dv = oracle.causal_attention_backward(do[sl], q[sl], k[sl], v[sl], p)
+        refs.append((b, o, l, dq, dk, dv))
+    return got, refs
+
+
+@pytest.mark.parametrize("B,T,H,D", [(2, 200, 3, 128), (1, 64, 2, 128), (2, 77, 2, 64)])
+def test_bf16(B, T, H, D):
+    got, refs = _attn(B, T, H, D, "bf16")
+    for b, o, l, dq, dk, dv in refs:
+        for name, g, r in (("O", got[0][b], o[0]), ("dq", got[2][b], dq[0]), ("dk", got[3][b], dk[0]),
+                           ("dv", got[4][b], dv[0])):
+            assert_close(g, r, 0.999, 2e-2, f"bf16 {name} b={b}")
+        np.testing.assert_allclose(got[1][b], l[0], rtol=0, atol=2e-2)
+
+
+@pytest.mark.parametrize("B,T,H,D", [(2, 77, 2, 64), (1, 130, 1, 128)])
+def test_fp32(B, T, H, D):
+    got, refs = _attn(B, T, H, D, "fp32")
+    for b, o, l, dq, dk, dv in refs:
+        assert_close(got[0][b], o[0], 0.999999, 1e-5, "fp32 O")
+        np.testing.assert_allclose(got[1][b], l[0], rtol=1e-6, atol=1e-5)
+        for name, g, r in (("dq", got[2][b], dq[0]), ("dk", got[3][b], dk[0]), ("dv", got[4][b], dv[0])):
+            assert_close(g, r, 0.99999, 1e-4, f"fp32 {name}")
+
+
+def test_single_position_is_v():
+    got, refs = _attn(3, 1, 2, 128, "bf16")
+    import torch  # noqa: F401
+    for b, o, l, dq, dk, dv in refs:
+        np.testing.assert_array_equal(got[0][b], o[0].astype(np.float32))
+
+
+def test_full_size_sampled():
+    """B=32, T=2048, H=10, D=128 (the attention microbenchmark), oracle on 2 sampled rows."""
+    got, refs = _attn(32, 2048, 10, 128, "bf16", sample=[0, 31])
+    for b, o, l, dq, dk, dv in refs:
+        for name, g, r in (("O", got[0][b], o[0]), ("dq", got[2][b], dq[0]), ("dk", got[3][b], dk[0]),
+                           ("dv", got[4][b], dv[0])):
+            assert_close(g, r, 0.999, 2e-2, f"full {name} b={b}")

@@ -1,0 +1,208 @@
+"""GPU-vs-oracle parity of the whole step on the tiny configuration.
+
+tiny: depth 2, d_model 128, 2 heads of 64, 4x MLP, vocab 512, batch 4 x 64,
+weights N(0, 0.02) from seed 0, tokens uniform in [0, 512), targets the
+next token, token_bytes uniform in [1, 8].
+
+Tolerances: loss relative error <= 1e-5 (fp32 mode) / 1e-3 (bf16 mode);
+per-tensor gradients and optimizer updates cosine >= 0.999 and
+max|gpu - oracle| / max|oracle| <= 2e-2 in bf16 mode.  In fp32 mode the
+arithmetic is fp32 against fp64, so gradients must agree to max-rel 1e-4
+(cosine >= 0.99999) and updates, which Newton-Schulz amplifies up to ~500x
+on the smallest singular values, to max-rel 1e-3.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.model import Config
+from pretraining_step_03_b300 import synth
+from tests._util import assert_close, bf16_round, cmp
+
+pytestmark = pytest.mark.gpu
+
+DEPTH, D, H, V, B, T = 2, 128, 2, 512, 4, 64
+CFG = Config(DEPTH, D, H, V)
+TOL = {
+    "fp32": dict(loss=1e-5, gcos=0.99999, grel=1e-4, ucos=0.9999, urel=1e-3),
+    "bf16": dict(loss=1e-3, gcos=0.999, grel=2e-2, ucos=0.999, urel=2e-2),
+}
+HP = dict(muon_lr=0.02, momentum=0.95, lr_emb=0.2, lr_unemb=0.004, beta1=0.8, beta2=0.95, eps=1e-10,
+          wd=0.0)
+
+
+@pytest.fixture(scope="module")
+def inputs():
+    params = synth.init_params(DEPTH, D, H, V, seed=0)
+    tok, tgt = synth.uniform_rows(B, T, V, seed=1)
+    tb = synth.token_bytes_uniform(V, 1, 8, seed=2)
+    return params, tok, tgt, tb
+
+
+def _model(mode, params):
+    from pretraining_step_03_b300.model import Model
+    m = Model(DEPTH, D, H, V, B, T, dtype=mode)
+    m.set_params(params)
+    return m
+
+
+def _oracle_params(mode, params):
+    return [bf16_round(p) if mode == "bf16" else p for p in params]
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+def test_tiny_forward_backward(mode, inputs):
+    import torch
+    params, tok, tgt, tb = inputs
+    m = _model(mode, params)
+    out = m.forward_backward(m.device_i32(tok), m.device_i32(tgt), m.device_i32(tb), B, T)
+    torch.cuda.synchronize()
+    loss, bpb = out.cpu().numpy().astype(np.float64)
+    assert m.check_flag() == 0
+    ref_loss, ref_bpb, ref_g = oracle.loss_and_grads(_oracle_params(mode, params), CFG, tok, tgt, tb)
+    tol = TOL[mode]
+    assert abs(loss - ref_loss) / ref_loss <= tol["loss"], (loss, ref_loss)
+    assert abs(bpb - ref_bpb) / ref_bpb <= tol["loss"], (bpb, ref_bpb)
+    for i in range(m.n_params):
+        assert_close(m.get_grad(i), ref_g[i], tol["gcos"], tol["grel"], f"{mode} grad {i}")
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+def test_tiny_optimizer_step_given_gradients(mode, inputs):
+    """Muon + AdamW from identical gradients (the oracle's), two steps."""
+    params, tok, tgt, tb = inputs
+    m = _model(mode, params)
+    _, _, g1 = oracle.loss_and_grads(params, CFG, tok, tgt, tb)
+    rng = np.random.default_rng(5)
+    g2 = [g * 0.5 + rng.normal(0, np.std(g) + 1e-12, g.shape) for g in g1]
+    w = [p.astype(np.float64) for p in params]
+    buf = [np.zeros_like(p) for p in w]
+    am = [np.zeros_like(p) for p in w]
+    av = [np.zeros_like(p) for p in w]
+    tol = TOL[mode]
+    for step, grads in ((1, g1), (2, g2)):
+        for i, g in enumerate(grads):
+            m.set_grad(i, g)
+        m.muon_step(HP["muon_lr"], HP["momentum"], True, 5)
+        m.adamw_step(HP["lr_emb"], HP["lr_unemb"], HP["beta1"], HP["beta2"], HP["eps"], HP["wd"], step)
+        prev = w
+        w = list(w)
+        for i, g in enumerate(grads):
+            if i == 0 or i == len(grads) - 1:
+                lr = HP["lr_emb"] if i == 0 else HP["lr_unemb"]
+                w[i], am[i], av[i] = oracle.adamw_step(w[i], g, am[i], av[i], lr, HP["beta1"], HP["beta2"],
+                                                       HP["eps"], HP["wd"], step)
+            else:
+                w[i], buf[i], _ = oracle.muon_step(w[i], g, buf[i], HP["muon_lr"], HP["momentum"], True, 5)
+        for i in range(m.n_params):
+            got = m.get_param(i).astype(np.float64)
+            assert_close(got, w[i], tol["ucos"], tol["urel"], f"{mode} step {step} weight {i}")
+            # the update itself, not just the weights
+            assert_close(got - prev[i], w[i] - prev[i], tol["ucos"], tol["urel"] * 5,
+                         f"{mode} step {step} update {i}")
+        # keep both sides on the same weights for the next step
+        for i in range(m.n_params):
+            w[i] = m.get_param(i).astype(np.float64)
+
+
+def test_tiny_full_step_fp32(inputs):
+    """fwd+bwd, Muon, AdamW, then fwd+bwd again: the second loss matches."""
+    import torch
+    params, tok, tgt, tb = inputs
+    m = _model("fp32", params)
+    dt = m.device_i32
+    m.forward_backward(dt(tok), dt(tgt), dt(tb), B, T)
+    m.muon_step(HP["muon_lr"], HP["momentum"], True, 5)
+    m.adamw_step(HP["lr_emb"], HP["lr_unemb"], HP["beta1"], HP["beta2"], HP["eps"], HP["wd"], 1)
+    out = m.forward_backward(dt(tok), dt(tgt), dt(tb), B, T)
+    torch.cuda.synchronize()
+    loss2 = float(out.cpu().numpy()[0])
+    _, _, g = oracle.loss_and_grads(params, CFG, tok, tgt, tb)
+    w = []
+    for i, p in enumerate(params):
+        if i in (0, len(params) - 1):
+            lr = HP["lr_emb"] if i == 0 else HP["lr_unemb"]
+            w.append(oracle.adamw_step(p, g[i], 0 * p, 0 * p, lr, HP["beta1"], HP["beta2"], HP["eps"],
+                                       HP["wd"], 1)[0])
+        else:
+            w.append(oracle.muon_step(p, g[i], 0 * p, HP["muon_lr"], HP["momentum"], True, 5)[0])
+    ref2 = oracle.forward(w, CFG, tok, tgt, tb)[0]
+    assert abs(loss2 - ref2) / ref2 <= 1e-4, (loss2, ref2)
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+def test_gradient_accumulation(mode, inputs):
+    """Two micro-batches with grad_scale 1/2 equal the oracle's two-half sum."""
+    params, tok, tgt, tb = inputs
+    tok2, tgt2 = synth.uniform_rows(B, T, V, seed=7)
+    m = _model(mode, params)
+    dt = m.device_i32
+    m.forward_backward(dt(tok), dt(tgt), dt(tb), B, T, accumulate=0, grad_scale=0.5)
+    m.forward_backward(dt(tok2), dt(tgt2), dt(tb), B, T, accumulate=1, grad_scale=0.5)
+    op = _oracle_params(mode, params)
+    _, _, ga = oracle.loss_and_grads(op, CFG, tok, tgt, tb, grad_scale=0.5)
+    _, _, gb = oracle.loss_and_grads(op, CFG, tok2, tgt2, tb, grad_scale=0.5)
+    tol = TOL[mode]
+    for i in range(m.n_params):
+        assert_close(m.get_grad(i), ga[i] + gb[i], tol["gcos"], tol["grel"], f"{mode} accum grad {i}")
+
+
+def test_step_is_deterministic(inputs):
+    import torch
+    params, tok, tgt, tb = inputs
+    m = _model("bf16", params)
+    dt = m.device_i32
+    res = []
+    for _ in range(2):
+        out = m.forward_backward(dt(tok), dt(tgt), dt(tb), B, T)
+        torch.cuda.synchronize()
+        res.append((out.cpu().numpy().copy(), [m.get_grad(i) for i in range(m.n_params)]))
+    assert np.array_equal(res[0][0], res[1][0])
+    for a, b in zip(res[0][1], res[1][1]):
+        assert np.array_equal(a, b)
+
+
+def test_out_of_range_token_sets_flag(inputs):
+    import torch
+    params, tok, tgt, tb = inputs
+    m = _model("bf16", params)
+    bad = tok.copy()
+    bad[1, 3] = V + 5
+    badt = tgt.copy()
+    badt[2, 7] = -1
+    m.forward_backward(m.device_i32(bad), m.device_i32(badt), m.device_i32(tb), B, T)
+    torch.cuda.synchronize()
+    from pretraining_step_03_b300 import _lib
+    assert m.check_flag() & _lib.NC_FLAG_TOKEN_RANGE
+    assert m.check_flag() == 0   # reading clears it
+
+
+def test_checkpoint_roundtrip_is_bitwise(inputs):
+    """get/set of params and optimizer state: a resumed step equals an uninterrupted one."""
+    import torch
+    from pretraining_step_03_b300 import _lib
+    params, tok, tgt, tb = inputs
+    a = _model("bf16", params)
+    dt = a.device_i32
+    for step in (1, 2):
+        a.forward_backward(dt(tok), dt(tgt), dt(tb), B, T)
+        a.muon_step(0.02)
+        a.adamw_step(0.2, 0.004, step=step)
+        if step == 1:
+            saved = ([a.get_param(i) for i in range(a.n_params)],
+                     [a.get_state(i, _lib.NC_STATE_MOMENTUM) for i in range(1, a.n_params - 1)],
+                     [(a.get_state(i, _lib.NC_STATE_ADAM_M), a.get_state(i, _lib.NC_STATE_ADAM_V))
+                      for i in (0, a.n_params - 1)])
+    b = _model("bf16", saved[0])
+    for j, i in enumerate(range(1, b.n_params - 1)):
+        b.set_state(i, _lib.NC_STATE_MOMENTUM, saved[1][j])
+    for j, i in enumerate((0, b.n_params - 1)):
+        b.set_state(i, _lib.NC_STATE_ADAM_M, saved[2][j][0])
+        b.set_state(i, _lib.NC_STATE_ADAM_V, saved[2][j][1])
+    b.forward_backward(dt(tok), dt(tgt), dt(tb), B, T)
+    b.muon_step(0.02)
+    b.adamw_step(0.2, 0.004, step=2)
+    torch.cuda.synchronize()
+    for i in range(a.n_params):
+        assert np.array_equal(a.get_param(i), b.get_param(i)), i
