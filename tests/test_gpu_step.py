@@ -5,11 +5,15 @@ weights N(0, 0.02) from seed 0, tokens uniform in [0, 512), targets the
 next token, token_bytes uniform in [1, 8].
 
 Tolerances: loss relative error <= 1e-5 (fp32 mode) / 1e-3 (bf16 mode);
-per-tensor gradients and optimizer updates cosine >= 0.999 and
+per-tensor gradients and updated weights cosine >= 0.999 and
 max|gpu - oracle| / max|oracle| <= 2e-2 in bf16 mode.  In fp32 mode the
 arithmetic is fp32 against fp64, so gradients must agree to max-rel 1e-4
-(cosine >= 0.99999) and updates, which Newton-Schulz amplifies up to ~500x
-on the smallest singular values, to max-rel 1e-3.
+(cosine >= 0.99999) and updates, which Newton-Schulz amplifies up to
+3.4445^5 ~ 490x on the smallest singular values, to max-rel 1e-3.
+The update W' - W alone is also checked; in bf16 mode its five
+Newton-Schulz iterations round X, A and B to bf16 (2^-9) fifteen times and
+the same ~490x gain applies to the smallest singular directions, so the
+update itself is held to cosine >= 0.998 and max-rel <= 0.1.
 """
 
 import numpy as np
@@ -25,8 +29,8 @@ pytestmark = pytest.mark.gpu
 DEPTH, D, H, V, B, T = 2, 128, 2, 512, 4, 64
 CFG = Config(DEPTH, D, H, V)
 TOL = {
-    "fp32": dict(loss=1e-5, gcos=0.99999, grel=1e-4, ucos=0.9999, urel=1e-3),
-    "bf16": dict(loss=1e-3, gcos=0.999, grel=2e-2, ucos=0.999, urel=2e-2),
+    "fp32": dict(loss=1e-5, gcos=0.99999, grel=1e-4, ucos=0.9999, urel=1e-3, dcos=0.9999, drel=5e-3),
+    "bf16": dict(loss=1e-3, gcos=0.999, grel=2e-2, ucos=0.999, urel=2e-2, dcos=0.998, drel=0.1),
 }
 HP = dict(muon_lr=0.02, momentum=0.95, lr_emb=0.2, lr_unemb=0.004, beta1=0.8, beta2=0.95, eps=1e-10,
           wd=0.0)
@@ -99,7 +103,7 @@ def test_tiny_optimizer_step_given_gradients(mode, inputs):
             got = m.get_param(i).astype(np.float64)
             assert_close(got, w[i], tol["ucos"], tol["urel"], f"{mode} step {step} weight {i}")
             # the update itself, not just the weights
-            assert_close(got - prev[i], w[i] - prev[i], tol["ucos"], tol["urel"] * 5,
+            assert_close(got - prev[i], w[i] - prev[i], tol["dcos"], tol["drel"],
                          f"{mode} step {step} update {i}")
         # keep both sides on the same weights for the next step
         for i in range(m.n_params):
