@@ -1,0 +1,323 @@
+#!/usr/bin/env python
+"""Throughput of one nanochat pretraining step (forward, loss/bpb, backward,
+Muon, AdamW) on B300, printed as one JSON line.
+
+Workload (default d20): 20 layers, d_model 1280, 10 heads x 128, 4x MLP,
+vocab 65536, bf16, 32 x 2048 tokens per step drawn from a Zipf(1.1) stream
+(nanochat speedrun walkthrough, lyylswood.com, section 预搜检: 32 rows of
+2048 tokens per GPU, ~560M parameters).  Synthetic data, random-init
+weights.  Replicas only: with --gpus N (under torchrun) every rank trains its
+own replica on its own data; there is no collective on the data path.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload d20|d30|tiny]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from pretraining_step_03_b300 import shapes, synth  # noqa: E402
+
+METRIC = "training tokens/sec and MFU (% of bf16 peak) for d20 step on 1 B300"
+WORKLOADS = {
+    "d20": dict(depth=20, d_model=1280, n_head=10, vocab=65536, B=32, T=2048, n_micro=1),
+    "d30": dict(depth=30, d_model=1920, n_head=15, vocab=65536, B=16, T=2048, n_micro=2),
+    "tiny": dict(depth=2, d_model=128, n_head=2, vocab=512, B=4, T=64, n_micro=1),
+}
+HP = dict(muon_lr=0.02, momentum=0.95, ns_steps=5, coefs=(3.4445, -4.7750, 2.0315), lr_emb=0.2,
+          lr_unemb=0.004, beta1=0.8, beta2=0.95, eps=1e-10, wd=0.0)
+NOMINAL_BF16_TFLOPS = 2250.0
+# Rooflines: the kernel class -> (bound, peak key).  Peaks are the measured
+# copy bandwidth and library bf16 GEMM rates of this GPU pool.
+ROOF = {"gemm": "tensor", "attn_fwd": "tensor", "attn_bwd": "tensor", "muon_ns": "tensor",
+        "norm": "hbm", "rope": "hbm", "ce": "hbm", "embed": "hbm", "muon_elem": "hbm", "adamw": "hbm"}
+# dram read+write bytes per launch of the dominant kernel class from the last
+# ncu capture of the current kernel code (profiles/), None when not measured.
+GEMM_TRAFFIC_PER_LAUNCH = None
+CPU_SAMPLE_T = 256
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], tensor=d["bf16_tflops_sustained"], tensor_burst=d["bf16_tflops"],
+                    source="measured")
+    return dict(hbm=6400.0, tensor=1400.0, tensor_burst=1800.0, source="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+class Clocks:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.p = None
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(torch, dev):
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return str(dev.index or 0)
+
+
+# ---------------------------------------------------------------- oracle timing
+def cpu_baseline(w, steps=1):
+    """The fp64 oracle as it stands, on a bounded sample, in a fresh process."""
+    code = (
+        "import sys, time, json, os\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import numpy as np\n"
+        "import oracle\n"
+        "from oracle.model import Config\n"
+        "from pretraining_step_03_b300 import synth\n"
+        f"w = {json.dumps(w)}\n"
+        f"T = min({CPU_SAMPLE_T}, w['T'])\n"
+        "cfg = Config(w['depth'], w['d_model'], w['n_head'], w['vocab'])\n"
+        "params = synth.init_params(w['depth'], w['d_model'], w['n_head'], w['vocab'], seed=0)\n"
+        "tok, tgt = synth.zipf_rows(1, T, w['vocab'], seed=1)\n"
+        "tb = synth.token_bytes_binomial(w['vocab'], seed=2)\n"
+        "ts = []\n"
+        f"for _ in range({steps}):\n"
+        "    t0 = time.perf_counter()\n"
+        "    oracle.loss_and_grads(params, cfg, tok, tgt, tb)\n"
+        "    ts.append(time.perf_counter() - t0)\n"
+        "print(json.dumps({'T': T, 'times': ts}))\n")
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores),
+               MKL_NUM_THREADS=str(cores), CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed:\n" + r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["T"], d["times"], cores
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="d20", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    tokens_per_step = w["B"] * w["T"] * w["n_micro"]
+    fpt = shapes.flops_per_token(w["depth"], w["d_model"], w["vocab"], w["T"])
+    fpt_causal = shapes.flops_per_token(w["depth"], w["d_model"], w["vocab"], w["T"], causal=True)
+    config = {"workload": args.workload, "depth": w["depth"], "d_model": w["d_model"],
+              "n_head": w["n_head"], "vocab": w["vocab"], "global_batch": w["B"] * w["n_micro"] * world,
+              "micro_batch": w["B"], "grad_accum": w["n_micro"], "seq_len": w["T"],
+              "parallelism": f"replicas{world}", "tokens": "zipf(1.1)",
+              "l2": "inputs larger than L2 (47+ GB activation stash per step)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        T, times, cores = cpu_baseline(w, steps=args.warmup + args.steps)
+        t = times[args.warmup:] if len(times) > args.warmup else times
+        v = T / (sum(t) / len(t))
+        line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0, "steps": len(t),
+                "warmup": args.warmup, "ms_per_step": 1000 * sum(t) / len(t), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config, "impl": "reference",
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"forward+backward of 1x{T} tokens at full widths (fp64 NumPy); "
+                                           "optimizer excluded"},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import numpy as np
+    import torch
+    from pretraining_step_03_b300 import _lib as L
+    from pretraining_step_03_b300.model import Model
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # ------------------------------------------------ inputs (seeded per rank)
+    nm, B, T = w["n_micro"], w["B"], w["T"]
+    tok, tgt = synth.zipf_rows(nm * B, T, w["vocab"], seed=1 + rank)
+    tb_host = synth.token_bytes_binomial(w["vocab"], seed=2)
+    m = Model(w["depth"], w["d_model"], w["n_head"], w["vocab"], B, T, dtype="bf16", seed=0, device=dev)
+    tb = torch.from_numpy(tb_host).to(dev)
+    tok_d = torch.from_numpy(tok.reshape(nm, B * T)).to(dev)
+    tgt_d = torch.from_numpy(tgt.reshape(nm, B * T)).to(dev)
+    loss_d = torch.zeros(nm, 2, dtype=torch.float32, device=dev)
+
+    def step(i):
+        for j in range(nm):
+            m.forward_backward(tok_d[j], tgt_d[j], tb, B, T, accumulate=int(j > 0), grad_scale=1.0 / nm,
+                               out=loss_d[j])
+        m.muon_step(HP["muon_lr"], HP["momentum"], True, HP["ns_steps"], HP["coefs"])
+        m.adamw_step(HP["lr_emb"], HP["lr_unemb"], HP["beta1"], HP["beta2"], HP["eps"], HP["wd"], i + 1)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    # ------------------------------------------------ device-timed region
+    stream = torch.cuda.current_stream(dev)
+    clocks = Clocks(gpu_id_for(torch, dev))
+    time.sleep(0.4)
+    L.nc_profile(m.h, 1)
+    launches0 = L.nc_launch_count()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    e1.record(stream)
+    barrier()
+    launches = L.nc_launch_count() - launches0
+    clk = clocks.stop()
+    L.nc_profile(m.h, 0)
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    loss = loss_d.cpu().numpy().mean(axis=0)
+    flag = m.check_flag()
+    pk = peaks()
+    kernels = {}
+    for c, name in enumerate(L.PROF_NAMES):
+        kms, n, fl, by = L.nc_profile_read(m.h, c)
+        if n == 0:
+            continue
+        if ROOF[name] == "tensor":
+            ach = fl / (kms * 1e-3) / 1e12
+            peak, unit = pk["tensor"], "TFLOP/s"
+        else:
+            ach = by / (kms * 1e-3) / 1e9
+            peak, unit = pk["hbm"], "GB/s"
+        kernels[name] = {"ms_per_step": kms / args.steps, "launch_sites_per_step": n / args.steps,
+                         "achieved": ach, "unit": unit, "peak": peak, "frac": ach / peak}
+    g = kernels.get("gemm")
+    roofline = None
+    if g:
+        kms, n, fl, by = L.nc_profile_read(m.h, 0)
+        roofline = {"bound": "tensor", "kernel": "gemm_tc_kernel (step GEMMs)", "achieved": g["achieved"],
+                    "peak": pk["tensor"], "unit": "TFLOP/s", "frac": g["frac"],
+                    "peak_kind": f"bf16 sustained ({pk['source']})",
+                    "traffic": GEMM_TRAFFIC_PER_LAUNCH,
+                    "flops_per_launch": fl / n}
+
+    # ------------------------------------------------ end to end through the C ABI (host buffers)
+    e2e = None
+    h2d = 2 * nm * B * T * 4
+    tok_h = torch.from_numpy(tok.reshape(-1).copy()).pin_memory()
+    tgt_h = torch.from_numpy(tgt.reshape(-1).copy()).pin_memory()
+
+    def host_step(i):
+        return m.train_step(tok_h, tgt_h, tb, B, T, nm, HP["muon_lr"], HP["lr_emb"], HP["lr_unemb"], i,
+                            HP["momentum"], HP["ns_steps"], HP["coefs"], HP["beta1"], HP["beta2"], HP["eps"],
+                            HP["wd"])
+
+    host_step(1000)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        host_step(1001 + i)
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * tokens_per_step / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": 8, "ms_per_step": 1000 * e2e_s}
+
+    value = world * tokens_per_step / (ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config,
+        "mfu": {"nominal_2250": value / world * fpt / (NOMINAL_BF16_TFLOPS * 1e12),
+                "measured_burst": value / world * fpt / (pk["tensor_burst"] * 1e12),
+                "measured_sustained": value / world * fpt / (pk["tensor"] * 1e12),
+                "causal_honest_nominal": value / world * fpt_causal / (NOMINAL_BF16_TFLOPS * 1e12),
+                "flop_per_token": fpt},
+        "loss": float(loss[0]), "bpb": float(loss[1]), "device_flag": flag,
+        "gpu_launches": int(launches),
+        "roofline": roofline,
+        "kernels": kernels,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        Tc, times, cores = cpu_baseline(w, steps=1)
+        line["cpu_baseline"] = {"value": Tc / times[0], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"forward+backward of 1x{Tc} tokens at full widths (fp64 NumPy); "
+                                          "optimizer excluded"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -205,6 +205,35 @@ NC_API int nc_gemm_bf16(int M, int N, int K, int batch, const void* A, long lda,
                  void* C, long ldc, long stride_c, int c_dtype, float alpha, float beta,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------ */
+/* Measurement: CUDA events around each kernel class of a model.       */
+/* ------------------------------------------------------------------ */
+enum {
+    NC_PROF_GEMM = 0,        /* step GEMMs (projections, LM head, their backward) */
+    NC_PROF_ATTN_FWD = 1,    /* causal attention forward */
+    NC_PROF_ATTN_BWD = 2,    /* causal attention backward */
+    NC_PROF_NORM = 3,        /* RMSNorm forward and backward */
+    NC_PROF_ROPE = 4,        /* RoPE on q, k and on their gradients */
+    NC_PROF_CE = 5,          /* softmax cross-entropy, loss and bpb reduction */
+    NC_PROF_EMBED = 6,       /* embedding lookup and its backward */
+    NC_PROF_MUON_NS = 7,     /* Newton-Schulz GEMMs */
+    NC_PROF_MUON_ELEM = 8,   /* Muon momentum, normalisation, update */
+    NC_PROF_ADAMW = 9,       /* AdamW */
+    NC_PROF_COUNT = 10
+};
+
+/* enable = 1 clears the counters and records a CUDA event pair around every
+ * kernel class launched on the model's stream from now on; 0 stops. */
+NC_API int nc_profile(nc_model* m, int enable);
+
+/* Totals since nc_profile(m, 1) for one class: device milliseconds (sum of
+ * event-pair durations), launch sites timed, algorithmic FLOPs and bytes
+ * (the work the class must do: 2*M*N*K per GEMM, the causal half of the
+ * attention products, the bytes an elementwise kernel must read and write).
+ * Synchronises the stream. */
+NC_API int nc_profile_read(nc_model* m, int category, double* ms, long* launches, double* flops,
+                           double* bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,6 +17,8 @@ NC_BF16, NC_FP32 = 0, 1
 NC_KIND_EMB, NC_KIND_MATRIX, NC_KIND_UNEMB = 0, 1, 2
 NC_STATE_MOMENTUM, NC_STATE_ADAM_M, NC_STATE_ADAM_V = 0, 1, 2
 NC_FLAG_TOKEN_RANGE, NC_FLAG_NONFINITE, NC_FLAG_TIMEOUT = 1, 2, 4
+PROF_NAMES = ["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "ce", "embed", "muon_ns", "muon_elem",
+              "adamw"]
 
 
 class NcError(RuntimeError):
@@ -53,6 +55,9 @@ SIGNATURES = {
     "nc_attention_workspace_bytes": (_SZ, [_I, _I, _I]),
     "nc_attention_backward": (_I, [_V, _V, _V, _I, _V, _V, _I, _V, _V, _V, _V, _I, _V, _I, _I, _I,
                                    _I, _I, _V]),
+    "nc_profile": (_I, [_V, _I]),
+    "nc_profile_read": (_I, [_V, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_L),
+                             ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
     "nc_gemm_bf16": (_I, [_I, _I, _I, _I, _V, _L, _L, _I, _V, _L, _L, _I, _V, _L, _L, _I, _F, _F,
                           _V, _SZ, _V]),
 }
@@ -198,3 +203,15 @@ def nc_gemm_bf16(M, N, K, batch, A, lda, stride_a, trans_a, B, ldb, stride_b, tr
                  c_dtype, alpha, beta, workspace, workspace_bytes, stream):
     _check(lib().nc_gemm_bf16(M, N, K, batch, A, lda, stride_a, trans_a, B, ldb, stride_b, trans_b, C,
                               ldc, stride_c, c_dtype, alpha, beta, workspace, workspace_bytes, stream))
+
+
+def nc_profile(m, enable):
+    _check(lib().nc_profile(m, int(enable)))
+
+
+def nc_profile_read(m, category):
+    """-> (device ms, launch sites, algorithmic FLOPs, algorithmic bytes) for one kernel class."""
+    ms, n, fl, by = ctypes.c_double(), ctypes.c_long(), ctypes.c_double(), ctypes.c_double()
+    _check(lib().nc_profile_read(m, category, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(fl),
+                                 ctypes.byref(by)))
+    return ms.value, n.value, fl.value, by.value

@@ -78,6 +78,12 @@ struct nc_model {
     size_t ebws_bytes;
     void* splitk;
     size_t splitk_bytes;
+    // measurement: CUDA event pairs around kernel classes
+    struct ProfRec { cudaEvent_t a, b; int cat; double flops, bytes; };
+    bool prof_on = false;
+    std::vector<cudaEvent_t> ev_pool;
+    size_t ev_used = 0;
+    std::vector<ProfRec> recs;
 };
 
 namespace {
@@ -182,12 +188,40 @@ void layout(nc_model* m, char* base, size_t* total) {
     *total = c.off;
 }
 
+cudaEvent_t prof_event(nc_model* m) {
+    if (m->ev_used == m->ev_pool.size()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        m->ev_pool.push_back(e);
+    }
+    return m->ev_pool[m->ev_used++];
+}
+
+// Records a CUDA event pair around the launches made during its lifetime.
+struct Prof {
+    nc_model* m;
+    int cat;
+    double flops, bytes;
+    cudaEvent_t a = nullptr;
+    Prof(nc_model* m_, int cat_, double flops_, double bytes_) : m(m_), cat(cat_), flops(flops_), bytes(bytes_) {
+        if (m->prof_on && (a = prof_event(m))) cudaEventRecord(a, m->stream);
+    }
+    ~Prof() {
+        if (!a) return;
+        cudaEvent_t b = prof_event(m);
+        if (!b) return;
+        cudaEventRecord(b, m->stream);
+        m->recs.push_back({a, b, cat, flops, bytes});
+    }
+};
+
 template <typename T> T* W(nc_model* m, int i) {
     if (m->dtype == NC_BF16) return (T*)(m->shadow + m->poff[i]);
     return (T*)(m->master + m->poff[i]);
 }
 
-int run_gemm(nc_model* m, const Gemm& g) {
+int run_gemm(nc_model* m, const Gemm& g, int cat = NC_PROF_GEMM) {
+    Prof pr(m, cat, 2.0 * g.M * g.N * g.K * g.batch, 0.0);
     if (g.in_dtype == NC_BF16) return gemm_tc(g, m->splitk, m->splitk_bytes, m->stream);
     return gemm_simt(g, m->stream);
 }
@@ -218,27 +252,48 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
     const int d = m->d, H = m->H, Dh = m->Dh, V = m->V, F = m->F;
     const int M = B * T_;
     const int act = m->dtype;
+    const double ab = m->dtype == NC_BF16 ? 2.0 : 4.0;   // bytes per activation element
+    const double Md = (double)M * d;
+    const double attn_fl = 4.0 * B * H * Dh * (0.5 * T_ * (T_ + 1.0));  // causal q.k and p.v
     cudaStream_t s = m->stream;
     const int iw = 0, iu = 1 + 6 * m->depth;
     T* gop = m->dtype == NC_BF16 ? (T*)m->gT : (T*)m->g;  // residual gradient as GEMM operand
     T* gT = m->dtype == NC_BF16 ? (T*)m->gT : nullptr;
+    auto norm_f = [&](const float* x, void* y, float* r) {
+        Prof pr(m, NC_PROF_NORM, 0, Md * (4 + ab) + M * 4.0);
+        return rmsnorm_forward<T>(x, (T*)y, r, M, d, s);
+    };
+    auto norm_b = [&](void* y, float* r, const float* gin) {
+        Prof pr(m, NC_PROF_NORM, 0, Md * (4 + ab + (gin ? 4 : 0) + 4 + (gT ? ab : 0)) + M * 4.0);
+        return rmsnorm_backward<T>(m->dy, (T*)y, r, gin, m->g, gT, M, d, s);
+    };
+    auto rope = [&](void* qkv, float sign) {
+        Prof pr(m, NC_PROF_ROPE, 0, 4.0 * Md * ab);
+        return rope_apply<T>((T*)qkv, 3 * d, M, T_, H, Dh, m->rope, sign, s);
+    };
 
     // ------------------------------------------------ forward
-    NC_TRY(embed_forward<T>(tok, W<T>(m, iw), m->x, M, d, V, m->flag, s));
+    {
+        Prof pr(m, NC_PROF_EMBED, 0, Md * (ab + 4) + M * 4.0);
+        NC_TRY(embed_forward<T>(tok, W<T>(m, iw), m->x, M, d, V, m->flag, s));
+    }
     for (int l = 0; l < m->depth; ++l) {
         auto& Ly = m->L[l];
         const int b0 = 1 + 6 * l;
-        NC_TRY(rmsnorm_forward<T>(m->x, (T*)Ly.y1, Ly.r1, M, d, s));
+        NC_TRY(norm_f(m->x, Ly.y1, Ly.r1));
         NC_TRY(run_gemm(m, mk(m, M, 3 * d, d, Ly.y1, d, false, W<T>(m, b0), d, false, Ly.qkv, 3 * d, act)));
-        NC_TRY(rope_apply<T>((T*)Ly.qkv, 3 * d, M, T_, H, Dh, m->rope, 1.f, s));
+        NC_TRY(rope(Ly.qkv, 1.f));
         T* q = (T*)Ly.qkv;
-        NC_TRY(attention_forward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, d, Ly.lse, B, T_, H, Dh, s));
+        {
+            Prof pr(m, NC_PROF_ATTN_FWD, attn_fl, 0);
+            NC_TRY(attention_forward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, d, Ly.lse, B, T_, H, Dh, s));
+        }
         {   // x += o Wo^T
             Gemm g = mk(m, M, d, d, Ly.o, d, false, W<T>(m, b0 + 3), d, false, m->x, d, NC_FP32);
             g.aux = m->x; g.ldaux = d; g.aux_dtype = NC_FP32; g.beta = 1.f;
             NC_TRY(run_gemm(m, g));
         }
-        NC_TRY(rmsnorm_forward<T>(m->x, (T*)Ly.y2, Ly.r2, M, d, s));
+        NC_TRY(norm_f(m->x, Ly.y2, Ly.r2));
         {   // h = y2 W1^T, a = relu(h)^2
             Gemm g = mk(m, M, F, d, Ly.y2, d, false, W<T>(m, b0 + 4), d, false, Ly.h, F, act);
             g.epi = EPI_RELU2; g.C2 = Ly.a;
@@ -250,16 +305,19 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
             NC_TRY(run_gemm(m, g));
         }
     }
-    NC_TRY(rmsnorm_forward<T>(m->x, (T*)m->yf, m->rf, M, d, s));
+    NC_TRY(norm_f(m->x, m->yf, m->rf));
     NC_TRY(run_gemm(m, mk(m, M, V, d, m->yf, d, false, W<T>(m, iu), d, false, m->logits, V, act)));
-    NC_TRY(cross_entropy<T>((T*)m->logits, tgt, m->nll, M, V, grad_scale / (float)M, m->flag, s));
-    NC_TRY(loss_reduce(m->nll, tgt, tb, M, V, out, m->flag, s));
+    {
+        Prof pr(m, NC_PROF_CE, 0, 2.0 * M * V * ab + M * 16.0);
+        NC_TRY(cross_entropy<T>((T*)m->logits, tgt, m->nll, M, V, grad_scale / (float)M, m->flag, s));
+        NC_TRY(loss_reduce(m->nll, tgt, tb, M, V, out, m->flag, s));
+    }
 
     // ------------------------------------------------ backward
     float* G = m->grads;
     NC_TRY(weight_grad(m, G + m->poff[iu], V, d, m->logits, V, m->yf, d, M, accumulate));
     NC_TRY(run_gemm(m, mk(m, M, d, V, m->logits, V, false, W<T>(m, iu), d, true, m->dy, d, NC_FP32)));
-    NC_TRY(rmsnorm_backward<T>(m->dy, (T*)m->yf, m->rf, nullptr, m->g, gT, M, d, s));
+    NC_TRY(norm_b(m->yf, m->rf, nullptr));
     for (int l = m->depth - 1; l >= 0; --l) {
         auto& Ly = m->L[l];
         const int b0 = 1 + 6 * l;
@@ -272,21 +330,27 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         }
         NC_TRY(weight_grad(m, G + m->poff[b0 + 4], F, d, m->dh, F, Ly.y2, d, M, accumulate));
         NC_TRY(run_gemm(m, mk(m, M, d, F, m->dh, F, false, W<T>(m, b0 + 4), d, true, m->dy, d, NC_FP32)));
-        NC_TRY(rmsnorm_backward<T>(m->dy, (T*)Ly.y2, Ly.r2, m->g, m->g, gT, M, d, s));
+        NC_TRY(norm_b(Ly.y2, Ly.r2, m->g));
         // attention block
         NC_TRY(weight_grad(m, G + m->poff[b0 + 3], d, d, gop, d, Ly.o, d, M, accumulate));
         NC_TRY(run_gemm(m, mk(m, M, d, d, gop, d, false, W<T>(m, b0 + 3), d, true, m->dO, d, act)));
         T* q = (T*)Ly.qkv;
         T* dq = (T*)m->dqkv;
-        NC_TRY(attention_backward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, (T*)m->dO, d, Ly.lse, dq,
-                                     dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s));
-        NC_TRY(rope_apply<T>(dq, 3 * d, M, T_, H, Dh, m->rope, -1.f, s));
+        {
+            Prof pr(m, NC_PROF_ATTN_BWD, 2.5 * attn_fl, 0);
+            NC_TRY(attention_backward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, (T*)m->dO, d, Ly.lse, dq,
+                                         dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s));
+        }
+        NC_TRY(rope(m->dqkv, -1.f));
         NC_TRY(weight_grad(m, G + m->poff[b0], 3 * d, d, m->dqkv, 3 * d, Ly.y1, d, M, accumulate));
         NC_TRY(run_gemm(m, mk(m, M, d, 3 * d, m->dqkv, 3 * d, false, W<T>(m, b0), d, true, m->dy, d, NC_FP32)));
-        NC_TRY(rmsnorm_backward<T>(m->dy, (T*)Ly.y1, Ly.r1, m->g, m->g, gT, M, d, s));
+        NC_TRY(norm_b(Ly.y1, Ly.r1, m->g));
     }
-    NC_TRY(embed_backward(tok, m->g, G + m->poff[iw], M, d, V, accumulate,
-                          embed_backward_ws(m->ebws, M, d, V), s));
+    {
+        Prof pr(m, NC_PROF_EMBED, 0, Md * 4.0 + (double)V * d * 4.0 + M * 24.0);
+        NC_TRY(embed_backward(tok, m->g, G + m->poff[iw], M, d, V, accumulate,
+                              embed_backward_ws(m->ebws, M, d, V), s));
+    }
     return NC_OK;
 }
 
@@ -294,10 +358,15 @@ template <typename T>
 int muon(nc_model* m, float lr, float mu, int nesterov, int steps, const float* coef) {
     cudaStream_t s = m->stream;
     const int d = m->d, Ld = m->depth;
-    NC_TRY(muon_momentum(m->grads, m->momentum, m->mats, m->nmat, mu, nesterov, m->muon_partial,
-                         m->muon_chunks, s));
-    NC_TRY(muon_normalize<T>(m->grads, m->mats, m->nmat, m->muon_partial, m->muon_chunks, (T*)m->nsX,
-                             32, s));
+    const double nm = 12.0 * d * d * Ld;   // matrix parameters
+    const double xb = m->dtype == NC_BF16 ? 2.0 : 4.0;
+    {
+        Prof pr(m, NC_PROF_MUON_ELEM, 0, nm * (16.0 + 4.0 + xb));
+        NC_TRY(muon_momentum(m->grads, m->momentum, m->mats, m->nmat, mu, nesterov, m->muon_partial,
+                             m->muon_chunks, s));
+        NC_TRY(muon_normalize<T>(m->grads, m->mats, m->nmat, m->muon_partial, m->muon_chunks, (T*)m->nsX,
+                                 32, s));
+    }
     T* X = (T*)m->nsX;
     T* Y = (T*)m->nsX2;
     const long sq = (long)4 * Ld * d * d;  // elements of the square group
@@ -312,25 +381,28 @@ int muon(nc_model* m, float lr, float mu, int nesterov, int steps, const float* 
             {   // A = X X^T
                 Gemm g = mk(m, r, r, c, x, c, false, x, c, false, A, r, act);
                 g.batch = n; g.sA = g.sB = (long)r * c; g.sC = (long)r * r;
-                NC_TRY(run_gemm(m, g));
+                NC_TRY(run_gemm(m, g, NC_PROF_MUON_NS));
             }
             {   // B = c2 A A + c1 A
                 Gemm g = mk(m, r, r, r, A, r, false, A, r, true, Bm, r, act);
                 g.batch = n; g.sA = g.sB = g.sC = (long)r * r;
                 g.alpha = coef[2]; g.aux = A; g.ldaux = r; g.sAux = (long)r * r; g.aux_dtype = act;
                 g.beta = coef[1];
-                NC_TRY(run_gemm(m, g));
+                NC_TRY(run_gemm(m, g, NC_PROF_MUON_NS));
             }
             {   // Y = B X + c0 X
                 Gemm g = mk(m, r, c, r, Bm, r, false, x, c, true, y, c, act);
                 g.batch = n; g.sA = (long)r * r; g.sB = (long)r * c; g.sC = (long)r * c;
                 g.aux = x; g.ldaux = c; g.sAux = (long)r * c; g.aux_dtype = act; g.beta = coef[0];
-                NC_TRY(run_gemm(m, g));
+                NC_TRY(run_gemm(m, g, NC_PROF_MUON_NS));
             }
         }
         T* t = X; X = Y; Y = t;
     }
-    NC_TRY(muon_apply<T>(m->master, m->shadow, m->mats, m->nmat, X, lr, 32, s));
+    {
+        Prof pr(m, NC_PROF_MUON_ELEM, 0, nm * (xb + 8.0 + (m->shadow ? 2.0 : 0.0)));
+        NC_TRY(muon_apply<T>(m->master, m->shadow, m->mats, m->nmat, X, lr, 32, s));
+    }
     return NC_OK;
 }
 
@@ -474,7 +546,38 @@ int nc_init_model(int depth, int d_model, int n_head, int vocab, uint64_t seed, 
 }
 
 int nc_free(nc_model* m) {
+    if (m) for (auto e : m->ev_pool) cudaEventDestroy(e);
     delete m;
+    return NC_OK;
+}
+
+int nc_profile(nc_model* m, int enable) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    if (enable) {
+        NC_TRY(cuda_check(cudaStreamSynchronize(m->stream), "sync"));
+        m->recs.clear();
+        m->ev_used = 0;
+    }
+    m->prof_on = enable != 0;
+    return NC_OK;
+}
+
+int nc_profile_read(nc_model* m, int category, double* ms, long* launches, double* flops, double* bytes) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    if (category < 0 || category >= NC_PROF_COUNT) return set_error(NC_ERR_ARG, "category %d", category);
+    NC_TRY(cuda_check(cudaStreamSynchronize(m->stream), "sync"));
+    double t = 0, fl = 0, by = 0;
+    long n = 0;
+    for (auto& r : m->recs) {
+        if (r.cat != category) continue;
+        float e = 0.f;
+        NC_TRY(cuda_check(cudaEventElapsedTime(&e, r.a, r.b), "event time"));
+        t += e; fl += r.flops; by += r.bytes; ++n;
+    }
+    if (ms) *ms = t;
+    if (launches) *launches = n;
+    if (flops) *flops = fl;
+    if (bytes) *bytes = by;
     return NC_OK;
 }
 
@@ -525,6 +628,7 @@ int nc_adamw_step(nc_model* m, float lr_emb, float lr_unemb, float beta1, float 
     const long n = (long)m->V * m->d;
     const int idx[2] = {0, m->nparams - 1};
     const float lrs[2] = {lr_emb, lr_unemb};
+    Prof pr(m, NC_PROF_ADAMW, 0, 2.0 * n * (28.0 + (m->shadow ? 2.0 : 0.0)));
     for (int k = 0; k < 2; ++k) {
         const long o = m->poff[idx[k]];
         NC_TRY(adamw(m->master + o, m->shadow ? m->shadow + o : nullptr, m->grads + o,
