@@ -12,10 +12,24 @@ int attention_backward_simt(const T* q, const T* k, const T* v, long ld, const T
                             long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
                             int B, int T_, int H, int D, cudaStream_t s);
 
+int attention_delta_simt_bf16(const bf16* o, const bf16* dout, long ldo, float* delta, int B, int T_,
+                              int H, int D, cudaStream_t s);
+bool attention_tc_supported(long ld, long ldo, long ldd, const void* q, const void* k, const void* v,
+                            int D);
+int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, bf16* o, long ldo,
+                         float* lse, int B, int T, int H, cudaStream_t s);
+int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, const bf16* dout,
+                          long ldo, const float* lse, const float* delta, bf16* dq, bf16* dk, bf16* dv,
+                          long ldd, int B, int T, int H, cudaStream_t s);
+
 template <typename T>
 int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ldo, float* lse,
                       int B, int T_, int H, int D, cudaStream_t s) {
     if (B <= 0 || T_ <= 0) return NC_OK;
+    if constexpr (sizeof(T) == 2) {
+        if (attention_tc_supported(ld, ldo, ldo, q, k, v, D))
+            return attention_forward_tc(q, k, v, ld, o, ldo, lse, B, T_, H, s);
+    }
     return attention_forward_simt<T>(q, k, v, ld, o, ldo, lse, B, T_, H, D, s);
 }
 
@@ -24,6 +38,12 @@ int attention_backward(const T* q, const T* k, const T* v, long ld, const T* o, 
                        long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
                        int B, int T_, int H, int D, cudaStream_t s) {
     if (B <= 0 || T_ <= 0) return NC_OK;
+    if constexpr (sizeof(T) == 2) {
+        if (attention_tc_supported(ld, ldo, ldd, q, k, v, D)) {
+            NC_TRY(attention_delta_simt_bf16(o, dout, ldo, delta, B, T_, H, D, s));
+            return attention_backward_tc(q, k, v, ld, dout, ldo, lse, delta, dq, dk, dv, ldd, B, T_, H, s);
+        }
+    }
     return attention_backward_simt<T>(q, k, v, ld, o, dout, ldo, lse, dq, dk, dv, ldd, delta, B, T_,
                                       H, D, s);
 }

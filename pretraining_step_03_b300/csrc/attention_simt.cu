@@ -204,6 +204,15 @@ int attention_backward_simt(const T* q, const T* k, const T* v, long ld, const T
     return NC_OK;
 }
 
+int attention_delta_simt_bf16(const bf16* o, const bf16* dout, long ldo, float* delta, int B, int T_,
+                              int H, int D, cudaStream_t s) {
+    dim3 grid(ceil_div(T_, WARPS), H, B);
+    attn_delta_simt<bf16><<<grid, WARPS * 32, 0, s>>>(o, dout, ldo, delta, T_, H, D);
+    note_launch();
+    NC_LAUNCH_CHECK("attention_delta");
+    return NC_OK;
+}
+
 template int attention_forward_simt<float>(const float*, const float*, const float*, long, float*,
                                            long, float*, int, int, int, int, cudaStream_t);
 template int attention_forward_simt<bf16>(const bf16*, const bf16*, const bf16*, long, bf16*, long,

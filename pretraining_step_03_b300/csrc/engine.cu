@@ -21,6 +21,7 @@
 
 namespace nc {
 extern uint32_t* g_gemm_flag;
+extern uint32_t* g_attn_flag;
 }
 
 using namespace nc;
@@ -606,6 +607,7 @@ int nc_forward_backward(nc_model* m, const int32_t* tokens, const int32_t* targe
                          m->maxM, m->maxT);
     if (accumulate != 0 && accumulate != 1) return set_error(NC_ERR_ARG, "accumulate must be 0 or 1");
     g_gemm_flag = m->flag;
+    g_attn_flag = m->flag;
     if (m->dtype == NC_BF16)
         return forward_backward<bf16>(m, tokens, targets, token_bytes, B, T, accumulate, grad_scale, loss_bpb_out);
     return forward_backward<float>(m, tokens, targets, token_bytes, B, T, accumulate, grad_scale, loss_bpb_out);

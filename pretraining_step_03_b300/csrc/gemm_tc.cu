@@ -138,7 +138,10 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
     if (p.ws) {
         const long i = ((long)(split * p.batch + b) * p.M + row) * p.N + n0;
         if (full) st32(p.ws, i, NC_FP32, v);
-        else for (int j = 0; j < nv; ++j) p.ws[i + j] = v[j];
+        else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) if (j < nv) p.ws[i + j] = v[j];
+        }
         return;
     }
 #pragma unroll
@@ -149,12 +152,18 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
         if (p.aux && p.beta != 0.f) {
             float a[32];
             if (full) ld32(p.aux, ai, p.aux_dtype, a);
-            else for (int j = 0; j < nv; ++j) a[j] = ld_elem(p.aux, ai + j, p.aux_dtype);
+            else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) a[j] = j < nv ? ld_elem(p.aux, ai + j, p.aux_dtype) : 0.f;
+            }
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] += p.beta * a[j];
         }
         if (full) st32(p.C, ci, p.c_dtype, v);
-        else for (int j = 0; j < nv; ++j) st_elem(p.C, ci + j, p.c_dtype, v[j]);
+        else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) if (j < nv) st_elem(p.C, ci + j, p.c_dtype, v[j]);
+        }
     } else if (p.epi == EPI_RELU2) {
         float a[32];
 #pragma unroll
@@ -166,19 +175,28 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
             st32(p.C, ci, p.c_dtype, v);
             st32(p.C2, ci, p.c_dtype, a);
         } else {
-            for (int j = 0; j < nv; ++j) {
-                st_elem(p.C, ci + j, p.c_dtype, v[j]);
-                st_elem(p.C2, ci + j, p.c_dtype, a[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j < nv) {
+                    st_elem(p.C, ci + j, p.c_dtype, v[j]);
+                    st_elem(p.C2, ci + j, p.c_dtype, a[j]);
+                }
             }
         }
     } else {  // EPI_RELU2_BWD: dh = da * 2 relu(h)
         float h[32];
         if (full) ld32(p.aux, ai, p.aux_dtype, h);
-        else for (int j = 0; j < nv; ++j) h[j] = ld_elem(p.aux, ai + j, p.aux_dtype);
+        else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) h[j] = j < nv ? ld_elem(p.aux, ai + j, p.aux_dtype) : 0.f;
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= 2.f * fmaxf(h[j], 0.f);
         if (full) st32(p.C, ci, p.c_dtype, v);
-        else for (int j = 0; j < nv; ++j) st_elem(p.C, ci + j, p.c_dtype, v[j]);
+        else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) if (j < nv) st_elem(p.C, ci + j, p.c_dtype, v[j]);
+        }
     }
 }
 
@@ -312,7 +330,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (long u = blockIdx.x; u < p.units; u += gridDim.x) {
             int b, split, tm, tn;
             decode(p, u, b, split, tm, tn);
-            if (!tc::mbar_wait(&tfull[acc], aph, abort_flag)) break;
+            if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
             const int row = tm * BM + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
@@ -360,7 +378,36 @@ __global__ void splitk_reduce_kernel(const float* ws, int splits, int batch, int
     st_elem(C, b * sC + m * ldc + n, c_dtype, s);
 }
 
-// ------------------------------------------------------------ host side
+template <int BN, bool A_MN, bool B_MN>
+int launch(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cudaStream_t s) {
+    using C = Cfg<BN>;
+    static bool attr = false;
+    if (!attr) {
+        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
+                          "gemm_tc smem attribute"));
+        attr = true;
+    }
+    const long grid = p.units < num_sms() ? p.units : num_sms();
+    gemm_tc_kernel<BN, A_MN, B_MN><<<(int)grid, NTHREADS, C::SMEM, s>>>(ma, mb, p);
+    note_launch();
+    NC_LAUNCH_CHECK("gemm_tc");
+    return NC_OK;
+}
+
+int pick_splits(const Gemm& g, int tiles, int num_kb) {
+    const long work = (long)tiles * g.batch;
+    const int sms = num_sms();
+    if (work >= sms || num_kb < 8 || g.epi != EPI_STORE) return 1;
+    int s = (int)((2L * sms + work - 1) / work);
+    s = s < num_kb / 4 ? s : num_kb / 4;
+    s = s < 32 ? s : 32;
+    return s < 1 ? 1 : s;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ host side (shared with attention)
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -405,34 +452,6 @@ int num_sms() {
     return n;
 }
 
-template <int BN, bool A_MN, bool B_MN>
-int launch(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cudaStream_t s) {
-    using C = Cfg<BN>;
-    static bool attr = false;
-    if (!attr) {
-        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
-                          "gemm_tc smem attribute"));
-        attr = true;
-    }
-    const long grid = p.units < num_sms() ? p.units : num_sms();
-    gemm_tc_kernel<BN, A_MN, B_MN><<<(int)grid, NTHREADS, C::SMEM, s>>>(ma, mb, p);
-    note_launch();
-    NC_LAUNCH_CHECK("gemm_tc");
-    return NC_OK;
-}
-
-int pick_splits(const Gemm& g, int tiles, int num_kb) {
-    const long work = (long)tiles * g.batch;
-    const int sms = num_sms();
-    if (work >= sms || num_kb < 8 || g.epi != EPI_STORE) return 1;
-    int s = (int)((2L * sms + work - 1) / work);
-    s = s < num_kb / 4 ? s : num_kb / 4;
-    s = s < 32 ? s : 32;
-    return s < 1 ? 1 : s;
-}
-
-}  // namespace
 
 uint32_t* g_gemm_flag = nullptr;  // device flag word of the current model (set by the engine)
 

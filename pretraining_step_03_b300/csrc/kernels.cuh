@@ -1,6 +1,8 @@
 // Internal launch interface of libnc's kernels (raw pointers + a stream).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 #include "optim.cuh"
 
@@ -27,6 +29,10 @@ struct Gemm {
 };
 
 int gemm_simt(const Gemm& g, cudaStream_t s);
+// 3-D bf16 TMA map over [batch][outer][inner], 128-byte swizzle, zero OOB fill.
+int make_map(CUtensorMap* m, const void* ptr, long inner, long outer, long batch, long ld, long bs,
+             int box_inner, int box_outer);
+int num_sms();
 // tcgen05/TMA path (bf16 operands).  ws: fp32 split-K scratch (may be null).
 int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t gemm_tc_splitk_bytes(const Gemm& g);
