@@ -11,6 +11,12 @@ own replica on its own data; there is no collective on the data path.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload d20|d30|tiny]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+Kernel-level workloads (profiling harnesses, not the headline):
+  --workload attn    causal attention forward+backward alone, B=32 (or --batch),
+                     T=2048, H=10, D=128, bf16 Q/K/V/dO ~ N(0, 1)
+  --workload optim   Muon on the 120 d20 block matrices (N(0,1) gradients) and
+                     AdamW on the 65536x1280 embedding and unembedding
 """
 
 import argparse
@@ -28,6 +34,8 @@ from pretraining_step_03_b300 import shapes, synth  # noqa: E402
 
 METRIC = "training tokens/sec and MFU (% of bf16 peak) for d20 step on 1 B300"
 WORKLOADS = {
+    "attn": dict(B=32, T=2048, H=10, D=128),
+    "optim": dict(depth=20, d_model=1280, n_head=10, vocab=65536),
     "d20": dict(depth=20, d_model=1280, n_head=10, vocab=65536, B=32, T=2048, n_micro=1),
     "d30": dict(depth=30, d_model=1920, n_head=15, vocab=65536, B=16, T=2048, n_micro=2),
     "tiny": dict(depth=2, d_model=128, n_head=2, vocab=512, B=4, T=64, n_micro=1),
@@ -139,6 +147,97 @@ def cpu_baseline(w, steps=1):
     return d["T"], d["times"], cores
 
 
+# ---------------------------------------------------------------- kernel workloads
+def kernel_workload(args):
+    import numpy as np
+    import torch
+    from pretraining_step_03_b300 import _lib as L
+    from pretraining_step_03_b300.model import Model
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    pk = peaks()
+    if args.workload == "attn":
+        B, T, H, D = args.batch, 2048, 10, 128
+        g = torch.Generator(device=dev).manual_seed(0)
+        qkv = torch.randn(B * T, 3 * H * D, device=dev, generator=g).to(torch.bfloat16)
+        dout = torch.randn(B * T, H * D, device=dev, generator=g).to(torch.bfloat16)
+        o = torch.empty(B * T, H * D, device=dev, dtype=torch.bfloat16)
+        dqkv = torch.empty_like(qkv)
+        lse = torch.empty(B, H, T, device=dev, dtype=torch.float32)
+        ws = torch.empty(L.nc_attention_workspace_bytes(B, T, H), device=dev, dtype=torch.uint8)
+        q, k, v = (qkv.data_ptr() + i * H * D * 2 for i in range(3))
+        dq, dk, dv = (dqkv.data_ptr() + i * H * D * 2 for i in range(3))
+
+        def fwd():
+            L.nc_attention_forward(q, k, v, 3 * H * D, o.data_ptr(), H * D, lse.data_ptr(), B, T, H, D,
+                                   L.NC_BF16, s)
+
+        def bwd():
+            L.nc_attention_backward(q, k, v, 3 * H * D, o.data_ptr(), dout.data_ptr(), H * D,
+                                    lse.data_ptr(), dq, dk, dv, 3 * H * D, ws.data_ptr(), B, T, H, D,
+                                    L.NC_BF16, s)
+
+        causal = 0.5 * T * (T + 1)
+        fl_f = 4.0 * B * H * D * causal
+        res = {}
+        for name, fn, fl in (("fwd", fwd, fl_f), ("bwd", bwd, 2.5 * fl_f)):
+            for _ in range(args.warmup):
+                fwd(); fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            res[name] = {"ms": ms, "tflops": fl / ms / 1e9, "frac": fl / ms / 1e9 / pk["tensor_burst"]}
+        tot_ms = res["fwd"]["ms"] + res["bwd"]["ms"]
+        line = {"metric": "causal attention fwd+bwd TFLOP/s (algorithmic, causal half)",
+                "value": 3.5 * fl_f / tot_ms / 1e9, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": tot_ms, "higher_is_better": True, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": "attn", "B": B, "T": T, "H": H, "D": D},
+                "parts": res, "peak_tflops_burst": pk["tensor_burst"]}
+    else:
+        m = Model(20, 1280, 10, 65536, 0, 0, dtype="bf16", seed=0, device=dev)
+        rng = np.random.default_rng(0)
+        for i in range(m.n_params):
+            r, c = m.shapes[i]
+            m.set_grad(i, rng.standard_normal((r, c), dtype=np.float32))
+
+        def step(i):
+            m.muon_step(HP["muon_lr"], HP["momentum"], True, HP["ns_steps"], HP["coefs"])
+            m.adamw_step(HP["lr_emb"], HP["lr_unemb"], HP["beta1"], HP["beta2"], HP["eps"], HP["wd"], i + 1)
+
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        L.nc_profile(m.h, 1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        kernels = {}
+        for c in (7, 8, 9):
+            kms, n, fl, by = L.nc_profile_read(m.h, c)
+            name = L.PROF_NAMES[c]
+            ach = (fl / kms / 1e9) if ROOF[name] == "tensor" else (by / kms / 1e6)
+            peak = pk["tensor_burst"] if ROOF[name] == "tensor" else pk["hbm"]
+            kernels[name] = {"ms": kms / args.steps, "achieved": ach,
+                             "unit": "TFLOP/s" if ROOF[name] == "tensor" else "GB/s", "frac": ach / peak}
+        line = {"metric": "Muon (120 d20 matrices, 5 NS steps) + AdamW (2 x 65536x1280) step time",
+                "value": ms, "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": False, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "optim"}, "kernels": kernels}
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -148,7 +247,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="d20", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=32, help="batch of the attn workload")
     args = ap.parse_args()
+    if args.workload in ("attn", "optim"):
+        return kernel_workload(args)
     w = WORKLOADS[args.workload]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -59,6 +59,7 @@ enum { NC_STATE_MOMENTUM = 0, NC_STATE_ADAM_M = 1, NC_STATE_ADAM_V = 2 };
 #define NC_FLAG_TOKEN_RANGE 0x1u  /* a token or target id outside [0, vocab) */
 #define NC_FLAG_NONFINITE   0x2u  /* the loss came out NaN or Inf */
 #define NC_FLAG_TIMEOUT     0x4u  /* a pipeline wait inside a kernel gave up */
+#define NC_FLAG_SMEM_ALIGN  0x8u  /* a kernel found its shared memory misaligned and skipped its work */
 
 typedef struct nc_model nc_model;   /* opaque, owned by the library (host memory) */
 

@@ -16,7 +16,7 @@ NC_OK, NC_ERR_ARG, NC_ERR_CUDA, NC_ERR_OOM, NC_ERR_DEVICE_FLAG, NC_ERR_TIMEOUT, 
 NC_BF16, NC_FP32 = 0, 1
 NC_KIND_EMB, NC_KIND_MATRIX, NC_KIND_UNEMB = 0, 1, 2
 NC_STATE_MOMENTUM, NC_STATE_ADAM_M, NC_STATE_ADAM_V = 0, 1, 2
-NC_FLAG_TOKEN_RANGE, NC_FLAG_NONFINITE, NC_FLAG_TIMEOUT = 1, 2, 4
+NC_FLAG_TOKEN_RANGE, NC_FLAG_NONFINITE, NC_FLAG_TIMEOUT, NC_FLAG_SMEM_ALIGN = 1, 2, 4, 8
 PROF_NAMES = ["gemm", "attn_fwd", "attn_bwd", "norm", "rope", "ce", "embed", "muon_ns", "muon_elem",
               "adamw"]
 

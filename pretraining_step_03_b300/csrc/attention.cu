@@ -20,7 +20,7 @@ int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, b
                          float* lse, int B, int T, int H, cudaStream_t s);
 int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, const bf16* dout,
                           long ldo, const float* lse, const float* delta, bf16* dq, bf16* dk, bf16* dv,
-                          long ldd, int B, int T, int H, cudaStream_t s);
+                          long ldd, int B, int T, int H, const float2* rope, cudaStream_t s);
 
 template <typename T>
 int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ldo, float* lse,
@@ -36,12 +36,15 @@ int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ld
 template <typename T>
 int attention_backward(const T* q, const T* k, const T* v, long ld, const T* o, const T* dout,
                        long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
-                       int B, int T_, int H, int D, cudaStream_t s) {
+                       int B, int T_, int H, int D, cudaStream_t s, const float2* rope, int* rope_done) {
+    if (rope_done) *rope_done = 0;
     if (B <= 0 || T_ <= 0) return NC_OK;
     if constexpr (sizeof(T) == 2) {
         if (attention_tc_supported(ld, ldo, ldd, q, k, v, D)) {
             NC_TRY(attention_delta_simt_bf16(o, dout, ldo, delta, B, T_, H, D, s));
-            return attention_backward_tc(q, k, v, ld, dout, ldo, lse, delta, dq, dk, dv, ldd, B, T_, H, s);
+            if (rope_done) *rope_done = rope != nullptr;
+            return attention_backward_tc(q, k, v, ld, dout, ldo, lse, delta, dq, dk, dv, ldd, B, T_, H,
+                                         rope, s);
         }
     }
     return attention_backward_simt<T>(q, k, v, ld, o, dout, ldo, lse, dq, dk, dv, ldd, delta, B, T_,
@@ -54,9 +57,10 @@ template int attention_forward<bf16>(const bf16*, const bf16*, const bf16*, long
                                      float*, int, int, int, int, cudaStream_t);
 template int attention_backward<float>(const float*, const float*, const float*, long, const float*,
                                        const float*, long, const float*, float*, float*, float*,
-                                       long, float*, int, int, int, int, cudaStream_t);
+                                       long, float*, int, int, int, int, cudaStream_t, const float2*,
+                                       int*);
 template int attention_backward<bf16>(const bf16*, const bf16*, const bf16*, long, const bf16*,
                                       const bf16*, long, const float*, bf16*, bf16*, bf16*, long,
-                                      float*, int, int, int, int, cudaStream_t);
+                                      float*, int, int, int, int, cudaStream_t, const float2*, int*);
 
 }  // namespace nc

@@ -23,6 +23,11 @@
 //   in TMEM.  The running max m is raised only when it grows by more than
 //   2^8, and O is then rescaled in TMEM (the rescale is rare after the first
 //   blocks; P stays <= 256).
+// Two groups of four softmax warps split each 128-column row (32-column
+// chunks g and g+2 go to group g), so every row has two threads; the forward
+// combines their row maxima through a shared-memory exchange guarded by an
+// mbarrier (bounded wait).  When given the RoPE table, the backward rotates
+// dq and dk back to the unrotated q, k frame in its epilogue.
 // backward, deterministic, no atomics:
 //   dK/dV kernel, one CTA per 128-key block, query blocks from the diagonal on:
 //     S^T = K Q^T, dP^T = V dO^T, P^T and dS^T through one shared tile,
@@ -39,7 +44,9 @@ constexpr int HD = 128;                 // head dim of this path
 constexpr int BR = 128;                 // rows per block
 constexpr int ATOM = BR * 64 * 2;       // 16 KB: 128 rows x 64 bf16, 128-byte swizzle
 constexpr int TILE = 2 * ATOM;          // 32 KB
-constexpr int NT = 192;
+constexpr int NT = 320;                 // producer warp, MMA warp, 8 softmax warps
+constexpr int NSM = 256;                // softmax threads: 2 groups x 128 rows
+constexpr int XCH_BYTES = 2048;         // [2 parities][2 groups][128] fp32 exchange / statistics
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr uint32_t IDESC_KK = tc::idesc_bf16(128, 128, false, false);
@@ -65,27 +72,52 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Row r of a tile from 64 packed bf16 pairs, in the 128-byte swizzle.
-__device__ __forceinline__ void store_row(uint8_t* tile, int r, const uint32_t* w) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        uint8_t* dst = tile + (c >> 3) * ATOM + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-    }
-}
+// A softmax thread of group g owns row r and the 32-column chunks g and g+2
+// of a 128-column tile: columns [32g, 32g+32) and [64+32g, 64+32g+32), so a
+// RoPE pair (j, j+64) of a head-dim row stays in one thread.
+__device__ __forceinline__ int col_of(int g, int i) { return i < 32 ? 32 * g + i : 64 + 32 * g + (i - 32); }
 
-__device__ __forceinline__ void ld_row128(uint32_t taddr, float* v) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tc::tmem_ld32(taddr + c * 32, reinterpret_cast<uint32_t*>(v) + c * 32);
+__device__ __forceinline__ void ld_half(uint32_t taddr, int g, float* v) {
+    tc::tmem_ld32(taddr + g * 32, reinterpret_cast<uint32_t*>(v));
+    tc::tmem_ld32(taddr + (g + 2) * 32, reinterpret_cast<uint32_t*>(v) + 32);
     tc::tmem_wait_ld();
 }
 
-__device__ __forceinline__ void store_out_row(bf16* dst, const float* v, float scale) {
+// 32 packed bf16 pairs (this thread's 64 columns) into row r of a tile, 128-byte swizzle.
+__device__ __forceinline__ void store_half(uint8_t* tile, int r, int g, const uint32_t* w) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        uint4 u = make_uint4(pack2(v[8 * c] * scale, v[8 * c + 1] * scale), pack2(v[8 * c + 2] * scale, v[8 * c + 3] * scale),
-                             pack2(v[8 * c + 4] * scale, v[8 * c + 5] * scale), pack2(v[8 * c + 6] * scale, v[8 * c + 7] * scale));
-        reinterpret_cast<uint4*>(dst)[c] = u;
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint8_t* dst = tile + a * ATOM + r * 128 + ((((4 * g + k) ^ (r & 7))) << 4);
+            const uint32_t* x = w + 16 * a + 4 * k;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(x[0], x[1], x[2], x[3]);
+        }
+}
+
+// this thread's 64 columns of an output row (bf16, row pointer at column 0)
+__device__ __forceinline__ void store_out_half(bf16* row, int g, const float* v, float scale) {
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+        uint4* dst = reinterpret_cast<uint4*>(row + 64 * a + 32 * g);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float* x = v + 32 * a + 8 * k;
+            dst[k] = make_uint4(pack2(x[0] * scale, x[1] * scale), pack2(x[2] * scale, x[3] * scale),
+                                pack2(x[4] * scale, x[5] * scale), pack2(x[6] * scale, x[7] * scale));
+        }
+    }
+}
+
+// inverse RoPE (rotation by -angle) of head-dim pairs (j, j+64), j in [32g, 32g+32)
+__device__ __forceinline__ void unrope_half(float* v, const float2* table, int t, int g) {
+    const float2* row = table + (long)t * 64 + 32 * g;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float2 cs = __ldg(row + i);
+        const float x1 = v[i], x2 = v[32 + i];
+        v[i] = x1 * cs.x + x2 * cs.y;
+        v[32 + i] = x2 * cs.x - x1 * cs.y;
     }
 }
 
@@ -97,6 +129,7 @@ struct AttnParams {
     float* lse;            // [B, H, T]
     const float* delta;    // [B, H, T] (backward)
     bf16 *dq, *dk, *dv;    // backward outputs
+    const float2* rope;    // [T, 64] (cos, sin); non-null: dq, dk leave rotated back
     float scale;           // 1/sqrt(D)
     uint32_t* flag;
 };
@@ -106,15 +139,25 @@ struct Smem {
     uint64_t* bar;
     uint32_t* tmem_slot;
     volatile int* abort;
+    float* xch;            // [2][2][128]
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw, int ntiles) {
     Smem s;
-    s.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023);
-    s.bar = reinterpret_cast<uint64_t*>(s.base + ntiles * TILE);
+    s.base = raw;
+    s.bar = reinterpret_cast<uint64_t*>(raw + ntiles * TILE);
     s.tmem_slot = reinterpret_cast<uint32_t*>(s.bar + 24);
     s.abort = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+    s.xch = reinterpret_cast<float*>(raw + ntiles * TILE + 256);
     return s;
+}
+
+// The swizzled tiles need a 1024-byte aligned base; the launch asks for no
+// slack, so a misaligned base is reported and the CTA does nothing.
+__device__ __forceinline__ bool misaligned(const uint8_t* raw, uint32_t* flag) {
+    if ((tc::smem_u32(raw) & 1023u) == 0) return false;
+    if (threadIdx.x == 0 && flag) atomicOr(flag, NC_FLAG_SMEM_ALIGN);
+    return true;
 }
 
 __device__ __forceinline__ void setup(Smem& s, int nbar, const uint32_t* counts) {
@@ -142,16 +185,28 @@ __device__ __forceinline__ void teardown(Smem& s, uint32_t tmem, uint32_t* flag)
     }
 }
 
+// exchange one float with the other group's thread of the same row (bounded wait)
+__device__ __forceinline__ bool exchange(Smem& sm, uint64_t* xbar, int it, int g, int r, float mine,
+                                         float* other) {
+    float* x = sm.xch + (it & 1) * 256;
+    x[g * 128 + r] = mine;
+    tc::mbar_arrive(&xbar[it & 1]);
+    if (!tc::mbar_wait_warp(&xbar[it & 1], (it >> 1) & 1, sm.abort)) return false;
+    *other = x[(1 - g) * 128 + r];
+    return true;
+}
+
 // ===================================================================== forward
 // smem tiles: 0 Q | 1,2 K/V stage 0 | 3,4 K/V stage 1 | 5,6 P buffers
-// barriers: 0 q_full, 1-2 kv_full, 3-4 kv_empty, 5-6 s_full, 7-8 p_full, 9-10 o_done
+// barriers: 0 q_full, 1-2 kv_full, 3-4 kv_empty, 5-6 s_full, 7-8 p_full, 9-10 o_done, 11-12 xbar
 // TMEM: S buffers at columns 0 and 128, O at 256.
 constexpr int FWD_TILES = 7;
 
 __global__ void __launch_bounds__(NT, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, const AttnParams p) {
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, FWD_TILES);
     const int qb = p.nblk - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int nkb = qb + 1;
@@ -162,8 +217,9 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* s_full = &sm.bar[5];
     uint64_t* p_full = &sm.bar[7];
     uint64_t* o_done = &sm.bar[9];
-    const uint32_t counts[11] = {1, 1, 1, 1, 1, 1, 1, 128, 128, 1, 1};
-    setup(sm, 11, counts);
+    uint64_t* xbar = &sm.bar[11];
+    const uint32_t counts[13] = {1, 1, 1, 1, 1, 1, 1, NSM, NSM, 1, 1, NSM, NSM};
+    setup(sm, 13, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* Q = sm.base;
     auto Kt = [&](int st) { return sm.base + (1 + 2 * st) * TILE; };
@@ -209,30 +265,25 @@ __global__ void __launch_bounds__(NT, 1)
             tc::mma_commit(&kv_empty[j & 1]);
         }
     } else if (warp >= 2) {
-        const int q = warp & 3, r = q * 32 + lane;
+        const int g = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
         const float c2 = p.scale * LOG2E;
         float m2 = -INFINITY, l = 0.f;
-        float s[128];
+        float s[64];
         bool ok = true;
         for (int j = 0; j < nkb; ++j) {
             if (!(ok = tc::mbar_wait_warp(&s_full[j & 1], (j >> 1) & 1, sm.abort))) break;
             tc::fence_after();
-            ld_row128(tmem + lanes + (j & 1) * 128, s);
+            ld_half(tmem + lanes + (j & 1) * 128, g, s);
             float mx = -INFINITY;
-            if (j == qb) {
 #pragma unroll
-                for (int i = 0; i < 128; ++i) {
-                    s[i] = i > r ? -INFINITY : s[i] * c2;
-                    mx = fmaxf(mx, s[i]);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 128; ++i) {
-                    s[i] *= c2;
-                    mx = fmaxf(mx, s[i]);
-                }
+            for (int i = 0; i < 64; ++i) {
+                s[i] = (j == qb && col_of(g, i) > r) ? -INFINITY : s[i] * c2;
+                mx = fmaxf(mx, s[i]);
             }
+            float mo;
+            if (!(ok = exchange(sm, xbar, j, g, r, mx, &mo))) break;
+            mx = fmaxf(mx, mo);
             if (j == 0) {
                 m2 = mx;
             } else {
@@ -243,13 +294,14 @@ __global__ void __launch_bounds__(NT, 1)
                     tc::fence_after();
                     const float alpha = need ? exp2f(m2 - mx) : 1.f;
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         uint32_t o[32];
-                        tc::tmem_ld32(tmem + lanes + 256 + c * 32, o);
+                        const uint32_t ta = tmem + lanes + 256 + (g + 2 * c) * 32;
+                        tc::tmem_ld32(ta, o);
                         tc::tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tc::tmem_st32(tmem + lanes + 256 + c * 32, o);
+                        tc::tmem_st32(ta, o);
                     }
                     tc::tmem_wait_st();
                     if (need) {
@@ -258,28 +310,31 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                 }
             }
-            uint32_t w[64];
+            uint32_t w[32];
             float sum = 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
+            for (int i = 0; i < 32; ++i) {
                 const float a = exp2f(s[2 * i] - m2), bb = exp2f(s[2 * i + 1] - m2);
                 sum += a + bb;
                 w[i] = pack2(a, bb);
             }
             l += sum;
             if (j >= 2 && !(ok = tc::mbar_wait_warp(&o_done[j & 1], ((j - 2) >> 1) & 1, sm.abort))) break;
-            store_row(Pt(j & 1), r, w);
+            store_half(Pt(j & 1), r, g, w);
             tc::fence_async_smem();
             tc::fence_before();
             tc::mbar_arrive(&p_full[j & 1]);
         }
-        if (ok && tc::mbar_wait_warp(&o_done[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1, sm.abort)) {
+        float lo = 0.f;
+        if (ok && tc::mbar_wait_warp(&o_done[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1, sm.abort) &&
+            exchange(sm, xbar, nkb, g, r, l, &lo)) {
             tc::fence_after();
-            ld_row128(tmem + lanes + 256, s);
+            const float lt = l + lo;
+            ld_half(tmem + lanes + 256, g, s);
             const int t = qb * BR + r;
             if (t < p.T) {
-                store_out_row(p.o + (long)(b * p.T + t) * p.ldo + col, s, 1.f / l);
-                p.lse[((long)b * p.H + h) * p.T + t] = (m2 + log2f(l)) * LN2;
+                store_out_half(p.o + (long)(b * p.T + t) * p.ldo + col, g, s, 1.f / lt);
+                if (g == 0) p.lse[((long)b * p.H + h) * p.T + t] = (m2 + log2f(lt)) * LN2;
             }
         }
     }
@@ -296,7 +351,8 @@ __global__ void __launch_bounds__(NT, 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                    const AttnParams p) {
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DQ_TILES);
     const int qb = p.nblk - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int nkb = qb + 1;
@@ -308,7 +364,7 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* s_free = &sm.bar[6];
     uint64_t* ds_full = &sm.bar[7];
     uint64_t* dq_done = &sm.bar[8];
-    const uint32_t counts[9] = {1, 1, 1, 1, 1, 1, 128, 128, 1};
+    const uint32_t counts[9] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1};
     setup(sm, 9, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* Q = sm.base;
@@ -354,45 +410,45 @@ __global__ void __launch_bounds__(NT, 1)
             tc::mma_commit(&kv_empty[st]);
         }
     } else if (warp >= 2) {
-        const int q = warp & 3, r = q * 32 + lane;
+        const int g = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
         const float c2 = p.scale * LOG2E;
         const int t = qb * BR + r;
         const long st_i = ((long)b * p.H + h) * p.T + (t < p.T ? t : 0);
         const float lse2 = t < p.T ? p.lse[st_i] * LOG2E : INFINITY;
         const float Dt = t < p.T ? p.delta[st_i] : 0.f;
-        float s[128];
+        float s[64];
         bool ok = true;
         for (int j = 0; j < nkb; ++j) {
             if (!(ok = tc::mbar_wait_warp(s_full, j & 1, sm.abort))) break;
             tc::fence_after();
-            ld_row128(tmem + lanes, s);
+            ld_half(tmem + lanes, g, s);
 #pragma unroll
-            for (int i = 0; i < 128; ++i) s[i] = (j == qb && i > r) ? 0.f : exp2f(s[i] * c2 - lse2);
-            uint32_t w[64];
+            for (int i = 0; i < 64; ++i) s[i] = (j == qb && col_of(g, i) > r) ? 0.f : exp2f(s[i] * c2 - lse2);
+            uint32_t w[32];
+            {
+                float d[64];
+                ld_half(tmem + lanes + 128, g, d);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t d[32];
-                tc::tmem_ld32(tmem + lanes + 128 + c * 32, d);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[16 * c + i] = pack2(s[32 * c + 2 * i] * (__uint_as_float(d[2 * i]) - Dt),
-                                          s[32 * c + 2 * i + 1] * (__uint_as_float(d[2 * i + 1]) - Dt));
+                for (int i = 0; i < 32; ++i)
+                    w[i] = pack2(s[2 * i] * (d[2 * i] - Dt), s[2 * i + 1] * (d[2 * i + 1] - Dt));
             }
             tc::fence_before();
             tc::mbar_arrive(s_free);
             // the previous dQ MMA must be done reading the dS tile
             if (j > 0 && !(ok = tc::mbar_wait_warp(dq_done, (j - 1) & 1, sm.abort))) break;
-            store_row(dS, r, w);
+            store_half(dS, r, g, w);
             tc::fence_async_smem();
             tc::fence_before();
             tc::mbar_arrive(ds_full);
         }
         if (ok && tc::mbar_wait_warp(dq_done, (nkb - 1) & 1, sm.abort)) {
             tc::fence_after();
-            ld_row128(tmem + lanes + 256, s);
-            if (t < p.T) store_out_row(p.dq + (long)(b * p.T + t) * p.ldd + col, s, p.scale);
+            ld_half(tmem + lanes + 256, g, s);
+            if (t < p.T) {
+                if (p.rope) unrope_half(s, p.rope, t, g);
+                store_out_half(p.dq + (long)(b * p.T + t) * p.ldd + col, g, s, p.scale);
+            }
         }
     }
     teardown(sm, tmem, p.flag);
@@ -401,7 +457,7 @@ __global__ void __launch_bounds__(NT, 1)
 // ===================================================================== dK, dV
 // smem tiles: 0 K | 1 V | 2,3 Q/dO stage 0 | 4,5 Q/dO stage 1 | 6 P^T then dS^T
 // barriers: 0 kv_full, 1-2 qd_full, 3-4 qd_empty, 5 s_full, 6 s_free, 7 p_full, 8 dv_done,
-//           9 ds_full, 10 dk_done
+//           9 ds_full, 10 dk_done, 11-12 stat barriers
 // TMEM: S^T at 0, dP^T at 128, dV at 256, dK at 384.
 constexpr int DKV_TILES = 7;
 
@@ -409,7 +465,8 @@ __global__ void __launch_bounds__(NT, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                      const AttnParams p) {
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DKV_TILES);
     const int kb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int nq = p.nblk - kb;        // query blocks kb .. nblk-1
@@ -423,8 +480,9 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* dv_done = &sm.bar[8];
     uint64_t* ds_full = &sm.bar[9];
     uint64_t* dk_done = &sm.bar[10];
-    const uint32_t counts[11] = {1, 1, 1, 1, 1, 1, 128, 128, 1, 128, 1};
-    setup(sm, 11, counts);
+    uint64_t* sbar = &sm.bar[11];
+    const uint32_t counts[13] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1, NSM, 1, NSM, NSM};
+    setup(sm, 13, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* K = sm.base;
     uint8_t* V = sm.base + TILE;
@@ -481,53 +539,51 @@ __global__ void __launch_bounds__(NT, 1)
             tc::mma_commit(&qd_empty[st]);
         }
     } else if (warp >= 2) {
-        const int q = warp & 3, r = q * 32 + lane;   // r = key row within the block
+        const int g = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;   // r = key row of the block
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
         const float c2 = p.scale * LOG2E;
-        float s[128];
+        const long srow = ((long)b * p.H + h) * p.T;
+        float s[64];
         bool ok = true;
-        const long srow = ((long)b * p.H + h) * p.T;   // statistics of this (b, h)
         for (int i = 0; i < nq; ++i) {
             const int j = kb + i;
-            const int tq = j * BR;                       // first query of the block
-            const int nvalid = p.T - tq;                 // queries c >= nvalid are padding
+            float* stat = sm.xch + (i & 1) * 256;          // [lse2 | D] of this query block
+            {
+                const int t = j * BR + r;
+                if (g == 0) stat[r] = t < p.T ? p.lse[srow + t] * LOG2E : INFINITY;
+                else stat[128 + r] = t < p.T ? p.delta[srow + t] : 0.f;
+            }
+            tc::mbar_arrive(&sbar[i & 1]);
+            if (!(ok = tc::mbar_wait_warp(&sbar[i & 1], (i >> 1) & 1, sm.abort))) break;
             if (!(ok = tc::mbar_wait_warp(s_full, i & 1, sm.abort))) break;
             tc::fence_after();
-            ld_row128(tmem + lanes, s);
+            ld_half(tmem + lanes, g, s);
             // P^T[r][c] = exp2(S^T*c2 - lse2[c]), zero where key r > query c
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                // every thread reads the same statistic: one broadcast load per warp
-                const float l2 = c < nvalid ? __ldg(p.lse + srow + tq + c) * LOG2E : INFINITY;
-                s[c] = (i == 0 && r > c) ? 0.f : exp2f(s[c] * c2 - l2);
+            for (int e = 0; e < 64; ++e) {
+                const int c = col_of(g, e);
+                s[e] = (i == 0 && r > c) ? 0.f : exp2f(s[e] * c2 - stat[c]);
             }
-            uint32_t w[64];
+            uint32_t w[32];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) w[c] = pack2(s[2 * c], s[2 * c + 1]);
+            for (int e = 0; e < 32; ++e) w[e] = pack2(s[2 * e], s[2 * e + 1]);
             if (i > 0 && !(ok = tc::mbar_wait_warp(dk_done, (i - 1) & 1, sm.abort))) break;
-            store_row(PS, r, w);
+            store_half(PS, r, g, w);
             tc::fence_async_smem();
             tc::fence_before();
             tc::mbar_arrive(p_full);
-            // dS^T = P^T (dP^T - D[c])
+            {   // dS^T = P^T (dP^T - D[c])
+                float d[64];
+                ld_half(tmem + lanes + 128, g, d);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t d[32];
-                tc::tmem_ld32(tmem + lanes + 128 + c * 32, d);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c0 = 32 * c + 2 * e;
-                    const float d0 = c0 < nvalid ? __ldg(p.delta + srow + tq + c0) : 0.f;
-                    const float d1 = c0 + 1 < nvalid ? __ldg(p.delta + srow + tq + c0 + 1) : 0.f;
-                    w[16 * c + e] = pack2(s[c0] * (__uint_as_float(d[2 * e]) - d0),
-                                          s[c0 + 1] * (__uint_as_float(d[2 * e + 1]) - d1));
-                }
+                for (int e = 0; e < 32; ++e)
+                    w[e] = pack2(s[2 * e] * (d[2 * e] - stat[128 + col_of(g, 2 * e)]),
+                                 s[2 * e + 1] * (d[2 * e + 1] - stat[128 + col_of(g, 2 * e + 1)]));
             }
             tc::fence_before();
             tc::mbar_arrive(s_free);
             if (!(ok = tc::mbar_wait_warp(dv_done, i & 1, sm.abort))) break;
-            store_row(PS, r, w);
+            store_half(PS, r, g, w);
             tc::fence_async_smem();
             tc::fence_before();
             tc::mbar_arrive(ds_full);
@@ -535,16 +591,19 @@ __global__ void __launch_bounds__(NT, 1)
         if (ok && tc::mbar_wait_warp(dk_done, (nq - 1) & 1, sm.abort)) {
             tc::fence_after();
             const int key = kb * BR + r;
-            ld_row128(tmem + lanes + 256, s);
-            if (key < p.T) store_out_row(p.dv + (long)(b * p.T + key) * p.ldd + col, s, 1.f);
-            ld_row128(tmem + lanes + 384, s);
-            if (key < p.T) store_out_row(p.dk + (long)(b * p.T + key) * p.ldd + col, s, p.scale);
+            ld_half(tmem + lanes + 256, g, s);
+            if (key < p.T) store_out_half(p.dv + (long)(b * p.T + key) * p.ldd + col, g, s, 1.f);
+            ld_half(tmem + lanes + 384, g, s);
+            if (key < p.T) {
+                if (p.rope) unrope_half(s, p.rope, key, g);
+                store_out_half(p.dk + (long)(b * p.T + key) * p.ldd + col, g, s, p.scale);
+            }
         }
     }
     teardown(sm, tmem, p.flag);
 }
 
-int smem_bytes(int tiles) { return tiles * TILE + 1024 + 256; }
+int smem_bytes(int tiles) { return tiles * TILE + 256 + XCH_BYTES; }
 
 template <typename K>
 int set_smem(K kern, int bytes) {
@@ -591,7 +650,7 @@ int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, b
 
 int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, const bf16* dout,
                           long ldo, const float* lse, const float* delta, bf16* dq, bf16* dk, bf16* dv,
-                          long ldd, int B, int T, int H, cudaStream_t s) {
+                          long ldd, int B, int T, int H, const float2* rope, cudaStream_t s) {
     static bool init = false;
     if (!init) {
         NC_TRY(set_smem(attn_dq_kernel, smem_bytes(DQ_TILES)));
@@ -606,7 +665,7 @@ int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, 
     NC_TRY(maps(&mdo, dout, rows, ldo, H));
     AttnParams p{};
     p.T = T; p.H = H; p.nblk = ceil_div(T, BR); p.ldo = ldo; p.ldd = ldd;
-    p.lse = const_cast<float*>(lse); p.delta = delta; p.dq = dq; p.dk = dk; p.dv = dv;
+    p.lse = const_cast<float*>(lse); p.delta = delta; p.dq = dq; p.dk = dk; p.dv = dv; p.rope = rope;
     p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
     attn_dkdv_kernel<<<dim3(p.nblk, H, B), NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);
     attn_dq_kernel<<<dim3(p.nblk, H, B), NT, smem_bytes(DQ_TILES), s>>>(mq, mk, mv, mdo, p);

@@ -260,6 +260,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
     const int iw = 0, iu = 1 + 6 * m->depth;
     T* gop = m->dtype == NC_BF16 ? (T*)m->gT : (T*)m->g;  // residual gradient as GEMM operand
     T* gT = m->dtype == NC_BF16 ? (T*)m->gT : nullptr;
+    const bool fuse_rope = m->dtype == NC_BF16 && Dh == 128;
     auto norm_f = [&](const float* x, void* y, float* r) {
         Prof pr(m, NC_PROF_NORM, 0, Md * (4 + ab) + M * 4.0);
         return rmsnorm_forward<T>(x, (T*)y, r, M, d, s);
@@ -282,8 +283,14 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         auto& Ly = m->L[l];
         const int b0 = 1 + 6 * l;
         NC_TRY(norm_f(m->x, Ly.y1, Ly.r1));
-        NC_TRY(run_gemm(m, mk(m, M, 3 * d, d, Ly.y1, d, false, W<T>(m, b0), d, false, Ly.qkv, 3 * d, act)));
-        NC_TRY(rope(Ly.qkv, 1.f));
+        {   // q|k|v = y1 Wqkv^T, RoPE on q and k (in the GEMM epilogue when it can)
+            Gemm g = mk(m, M, 3 * d, d, Ly.y1, d, false, W<T>(m, b0), d, false, Ly.qkv, 3 * d, act);
+            if (fuse_rope) {
+                g.epi = EPI_ROPE; g.rope = m->rope; g.rope_T = T_; g.rope_cols = 2 * d;
+            }
+            NC_TRY(run_gemm(m, g));
+            if (!fuse_rope) NC_TRY(rope(Ly.qkv, 1.f));
+        }
         T* q = (T*)Ly.qkv;
         {
             Prof pr(m, NC_PROF_ATTN_FWD, attn_fl, 0);
@@ -337,12 +344,14 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         NC_TRY(run_gemm(m, mk(m, M, d, d, gop, d, false, W<T>(m, b0 + 3), d, true, m->dO, d, act)));
         T* q = (T*)Ly.qkv;
         T* dq = (T*)m->dqkv;
+        int unroped = 0;
         {
             Prof pr(m, NC_PROF_ATTN_BWD, 2.5 * attn_fl, 0);
             NC_TRY(attention_backward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, (T*)m->dO, d, Ly.lse, dq,
-                                         dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s));
+                                         dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s, m->rope,
+                                         &unroped));
         }
-        NC_TRY(rope(m->dqkv, -1.f));
+        if (!unroped) NC_TRY(rope(m->dqkv, -1.f));
         NC_TRY(weight_grad(m, G + m->poff[b0], 3 * d, d, m->dqkv, 3 * d, Ly.y1, d, M, accumulate));
         NC_TRY(run_gemm(m, mk(m, M, d, 3 * d, m->dqkv, 3 * d, false, W<T>(m, b0), d, true, m->dy, d, NC_FP32)));
         NC_TRY(norm_b(Ly.y1, Ly.r1, m->g));

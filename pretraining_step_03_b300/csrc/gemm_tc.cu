@@ -43,6 +43,8 @@ struct TcParams {
     int epi;
     float* ws;        // split-K partials [splits][batch][M][N], or null
     uint32_t* flag;   // device flag word for timeouts (may be null)
+    const float2* rope;
+    int rope_T, rope_cols;
 };
 
 template <int BN> struct Cfg {
@@ -334,6 +336,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_after();
             const int row = tm * BM + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            if (p.epi == EPI_ROPE) {
+                // chunk pairs (a, a+2) hold head-dim pairs (j, j+64) of one 128-wide head
+#pragma unroll 1
+                for (int pr = 0; pr < BN / 64; ++pr) {
+                    const int a = (pr >> 1) * 4 + (pr & 1);
+                    uint32_t ra[32], rb[32];
+                    tc::tmem_ld32(tbase + a * 32, ra);
+                    tc::tmem_ld32(tbase + (a + 2) * 32, rb);
+                    tc::tmem_wait_ld();
+                    const int na = tn * BN + a * 32;
+                    if (row < p.M && na < p.N) {
+                        float va[32], vb[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            va[j] = __uint_as_float(ra[j]) * p.alpha;
+                            vb[j] = __uint_as_float(rb[j]) * p.alpha;
+                        }
+                        if (na < p.rope_cols) {
+                            const float2* cs = p.rope + (long)(row % p.rope_T) * 64 + (pr & 1) * 32;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const float2 c = __ldg(cs + j);
+                                const float x1 = va[j], x2 = vb[j];
+                                va[j] = x1 * c.x - x2 * c.y;
+                                vb[j] = x2 * c.x + x1 * c.y;
+                            }
+                        }
+                        const long ci = (long)b * p.sC + (long)row * p.ldc + na;
+                        st32(p.C, ci, p.c_dtype, va);
+                        st32(p.C, ci + 64, p.c_dtype, vb);
+                    }
+                }
+            } else
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
@@ -464,6 +499,7 @@ bool gemm_tc_supported(const Gemm& g) {
     if (g.C2 && (uintptr_t)g.C2 % 16) return false;
     if (g.aux && (uintptr_t)g.aux % 16) return false;
     if (g.N % 8) return false;
+    if (g.epi == EPI_ROPE && (g.N % 128 || !g.rope || g.rope_T <= 0 || g.c_dtype != NC_BF16)) return false;
     return true;
 }
 
@@ -491,6 +527,7 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     p.C2 = g.C2; p.alpha = g.alpha; p.beta = g.beta; p.epi = g.epi;
     p.ws = p.splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
     p.flag = g_gemm_flag;
+    p.rope = g.rope; p.rope_T = g.rope_T; p.rope_cols = g.rope_cols;
 
     CUtensorMap ma, mb;
     if (!g.a_t) NC_TRY(make_map(&ma, g.A, g.K, g.M, g.batch, g.lda, g.sA, 64, BM));

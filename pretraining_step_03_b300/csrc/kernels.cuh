@@ -14,6 +14,7 @@ enum EpiKind {
     EPI_STORE = 0,      // C = alpha*acc + beta*aux            (aux may alias C)
     EPI_RELU2 = 1,      // C = alpha*acc (pre-activation h), C2 = relu(h)^2
     EPI_RELU2_BWD = 2,  // C = alpha*acc * 2*relu(aux)          (aux = h)
+    EPI_ROPE = 3,       // C = alpha*acc with columns < rope_cols rotated by RoPE (head dim 128)
 };
 
 struct Gemm {
@@ -26,6 +27,8 @@ struct Gemm {
     void* C2 = nullptr;
     float alpha = 1.f, beta = 0.f;
     int epi = EPI_STORE;
+    const float2* rope = nullptr;  // EPI_ROPE: [rope_T, 64] (cos, sin); row position = row % rope_T
+    int rope_T = 0, rope_cols = 0;
 };
 
 int gemm_simt(const Gemm& g, cudaStream_t s);
@@ -75,10 +78,13 @@ int embed_backward(const int32_t* tok, const float* g, float* dwte, int M, int d
 template <typename T>
 int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ldo, float* lse,
                       int B, int T_, int H, int D, cudaStream_t s);
+// rope: optional RoPE table; when the kernel can rotate dq, dk back itself it
+// does so and sets *rope_done = 1 (else the caller applies the inverse RoPE).
 template <typename T>
 int attention_backward(const T* q, const T* k, const T* v, long ld, const T* o, const T* dout,
                        long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
-                       int B, int T_, int H, int D, cudaStream_t s);
+                       int B, int T_, int H, int D, cudaStream_t s, const float2* rope = nullptr,
+                       int* rope_done = nullptr);
 
 // ------------------------------------------------------------ optimizers
 // Muon, phase 1: buf = mu*buf + g; g <- g + mu*buf (nesterov) or buf; per-CTA

@@ -175,6 +175,73 @@ __global__ void __launch_bounds__(CE_THREADS) ce_kernel(T* z, const int32_t* tgt
     }
 }
 
+// Same computation for bf16 logits with V a multiple of 8 * 512: the row is
+// read from HBM once (16-byte loads) into this thread's own slice of shared
+// memory, the three passes run from there, and the result is written once.
+constexpr float CE_LOG2E = 1.4426950408889634f;
+
+__global__ void __launch_bounds__(CE_THREADS) ce_rows_kernel(bf16* z, const int32_t* tgt, float* nll,
+                                                             int V, float scale, uint32_t* flag) {
+    extern __shared__ uint4 row_s[];
+    __shared__ float sh[32];
+    __shared__ float zt_s;
+    const long row = blockIdx.x;
+    uint4* zr = reinterpret_cast<uint4*>(z + row * V);
+    const int nv = V / (8 * CE_THREADS);
+    const int t = tgt[row];
+    const bool ok = t >= 0 && t < V;
+    if (threadIdx.x == 0) {
+        if (!ok) flag_set(flag, NC_FLAG_TOKEN_RANGE);
+        zt_s = ok ? __bfloat162float(z[row * V + t]) : 0.f;
+    }
+    float mx = -INFINITY;
+#pragma unroll 4
+    for (int k = 0; k < nv; ++k) {
+        const uint4 u = zr[threadIdx.x + k * CE_THREADS];
+        row_s[threadIdx.x + k * CE_THREADS] = u;
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            mx = fmaxf(mx, fmaxf(f.x, f.y));
+        }
+    }
+    mx = block_reduce(mx, sh, true);
+    const float mxl = mx * CE_LOG2E;
+    float se = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < nv; ++k) {
+        const uint4 u = row_s[threadIdx.x + k * CE_THREADS];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            se += exp2f(f.x * CE_LOG2E - mxl) + exp2f(f.y * CE_LOG2E - mxl);
+        }
+    }
+    se = block_reduce(se, sh, false);
+    const float lse = mx + logf(se);
+    const float lsel = lse * CE_LOG2E;
+    __syncthreads();  // zt_s was read before any thread overwrites z
+    if (threadIdx.x == 0) nll[row] = ok ? lse - zt_s : 0.f;
+#pragma unroll 4
+    for (int k = 0; k < nv; ++k) {
+        const int base = (threadIdx.x + k * CE_THREADS) * 8;
+        const uint4 u = row_s[threadIdx.x + k * CE_THREADS];
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            float p0 = exp2f(f.x * CE_LOG2E - lsel), p1 = exp2f(f.y * CE_LOG2E - lsel);
+            if (base + 2 * e == t) p0 -= 1.f;
+            if (base + 2 * e + 1 == t) p1 -= 1.f;
+            __nv_bfloat162 h = __floats2bfloat162_rn(p0 * scale, p1 * scale);
+            w[e] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        zr[threadIdx.x + k * CE_THREADS] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // Single CTA, fixed summation order: loss = mean nll; bpb = sum(nll | bytes>0) / (ln2 * sum bytes).
 __global__ void loss_reduce_kernel(const float* nll, const int32_t* tgt, const int32_t* tb, int M,
                                    int V, float* out, uint32_t* flag) {
@@ -381,6 +448,21 @@ template <typename T>
 int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float scale,
                   uint32_t* flag, cudaStream_t s) {
     if (M <= 0) return NC_OK;
+    if constexpr (sizeof(T) == 2) {
+        const int smem = V * 2;
+        if (V % (8 * CE_THREADS) == 0 && smem <= 200 * 1024 && (uintptr_t)logits % 16 == 0) {
+            static int attr_set = 0;
+            if (attr_set < smem) {
+                NC_TRY(cuda_check(cudaFuncSetAttribute(ce_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       smem), "ce smem attribute"));
+                attr_set = smem;
+            }
+            ce_rows_kernel<<<M, CE_THREADS, smem, s>>>(logits, tgt, nll, V, scale, flag);
+            note_launch();
+            NC_LAUNCH_CHECK("cross_entropy");
+            return NC_OK;
+        }
+    }
     ce_kernel<T><<<M, CE_THREADS, 0, s>>>(logits, tgt, nll, V, scale, flag);
     note_launch();
     NC_LAUNCH_CHECK("cross_entropy");

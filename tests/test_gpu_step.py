@@ -229,3 +229,27 @@ def test_checkpoint_roundtrip_is_bitwise(inputs):
     torch.cuda.synchronize()
     for i in range(a.n_params):
         assert np.array_equal(a.get_param(i), b.get_param(i)), i
+
+
+def test_vocab65536_head128_small_model():
+    """vocab 65536 and head dim 128: the row-resident cross-entropy, the
+    tensor-core attention with its fused inverse RoPE, and the GEMM epilogue
+    that applies RoPE to q and k."""
+    import torch
+    from pretraining_step_03_b300.model import Model
+    depth, d, h, v, b, t = 2, 256, 2, 65536, 2, 200
+    cfg = Config(depth, d, h, v)
+    params = synth.init_params(depth, d, h, v, seed=3)
+    tok, tgt = synth.zipf_rows(b, t, v, seed=4)
+    tb = synth.token_bytes_binomial(v, seed=2)
+    m = Model(depth, d, h, v, b, t, dtype="bf16")
+    m.set_params(params)
+    out = m.forward_backward(m.device_i32(tok), m.device_i32(tgt), m.device_i32(tb), b, t)
+    torch.cuda.synchronize()
+    loss, bpb = out.cpu().numpy().astype(np.float64)
+    assert m.check_flag() == 0
+    ref_loss, ref_bpb, ref_g = oracle.loss_and_grads([bf16_round(p) for p in params], cfg, tok, tgt, tb)
+    assert abs(loss - ref_loss) / ref_loss <= 1e-3, (loss, ref_loss)
+    assert abs(bpb - ref_bpb) / ref_bpb <= 1e-3, (bpb, ref_bpb)
+    for i in range(m.n_params):
+        assert_close(m.get_grad(i), ref_g[i], 0.999, 2e-2, f"grad {i}")
