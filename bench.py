@@ -17,6 +17,8 @@ Kernel-level workloads (profiling harnesses, not the headline):
                      T=2048, H=10, D=128, bf16 Q/K/V/dO ~ N(0, 1)
   --workload optim   Muon on the 120 d20 block matrices (N(0,1) gradients) and
                      AdamW on the 65536x1280 embedding and unembedding
+  --workload gemm    the d20 MLP up-projection GEMM alone: [B*2048, 1280] x
+                     [5120, 1280]^T -> bf16, B = --batch
 """
 
 import argparse
@@ -35,6 +37,7 @@ from pretraining_step_03_b300 import shapes, synth  # noqa: E402
 METRIC = "training tokens/sec and MFU (% of bf16 peak) for d20 step on 1 B300"
 WORKLOADS = {
     "attn": dict(B=32, T=2048, H=10, D=128),
+    "gemm": dict(B=32, T=2048, d=1280, F=5120),
     "optim": dict(depth=20, d_model=1280, n_head=10, vocab=65536),
     "d20": dict(depth=20, d_model=1280, n_head=10, vocab=65536, B=32, T=2048, n_micro=1),
     "d30": dict(depth=30, d_model=1920, n_head=15, vocab=65536, B=16, T=2048, n_micro=2),
@@ -159,6 +162,35 @@ def kernel_workload(args):
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
     pk = peaks()
+    if args.workload == "gemm":
+        M, K, N = args.batch * 2048, 1280, 5120
+        g = torch.Generator(device=dev).manual_seed(0)
+        A = torch.randn(M, K, device=dev, generator=g).to(torch.bfloat16)
+        W = torch.randn(N, K, device=dev, generator=g).to(torch.bfloat16)
+        C = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+
+        def run():
+            L.nc_gemm_bf16(M, N, K, 1, A.data_ptr(), K, 0, 0, W.data_ptr(), K, 0, 0, C.data_ptr(), N, 0,
+                           L.NC_BF16, 1.0, 0.0, 0, 0, s)
+
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        tf = 2.0 * M * N * K / ms / 1e9
+        line = {"metric": "bf16 GEMM TFLOP/s (d20 MLP up-projection shape)", "value": tf, "unit": "TFLOP/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "gemm", "M": M, "N": N, "K": K},
+                "frac_burst": tf / pk["tensor_burst"], "bytes_min": 2.0 * (M * K + N * K + M * N)}
+        print(json.dumps(line), flush=True)
+        return
     if args.workload == "attn":
         B, T, H, D = args.batch, 2048, 10, 128
         g = torch.Generator(device=dev).manual_seed(0)
@@ -249,7 +281,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=32, help="batch of the attn workload")
     args = ap.parse_args()
-    if args.workload in ("attn", "optim"):
+    if args.workload in ("attn", "optim", "gemm"):
         return kernel_workload(args)
     w = WORKLOADS[args.workload]
     rank = int(os.environ.get("RANK", "0"))
