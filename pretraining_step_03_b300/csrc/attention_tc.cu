@@ -198,7 +198,9 @@ __device__ __forceinline__ bool exchange(Smem& sm, uint64_t* xbar, int it, int g
 
 // ===================================================================== forward
 // smem tiles: 0 Q | 1,2 K/V stage 0 | 3,4 K/V stage 1 | 5,6 P buffers
-// barriers: 0 q_full, 1-2 kv_full, 3-4 kv_empty, 5-6 s_full, 7-8 p_full, 9-10 o_done, 11-12 xbar
+// barriers: 0 q_full, 1-2 k_full, 3-4 k_empty, 5-6 s_full, 7-8 p_full, 9-10 o_done, 11-12 xbar,
+//           13-14 v_empty, 15-16 v_full  (a K tile is released when its S MMA completes,
+//           a V tile after PV)
 // TMEM: S buffers at columns 0 and 128, O at 256.
 constexpr int FWD_TILES = 7;
 
@@ -208,18 +210,21 @@ __global__ void __launch_bounds__(NT, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, FWD_TILES);
-    const int qb = p.nblk - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // the heaviest (latest) query blocks first; (b, h) vary fastest
+    const int qb = p.nblk - 1 - blockIdx.y, h = blockIdx.x % p.H, b = blockIdx.x / p.H;
     const int nkb = qb + 1;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* q_full = &sm.bar[0];
-    uint64_t* kv_full = &sm.bar[1];
-    uint64_t* kv_empty = &sm.bar[3];
+    uint64_t* k_full = &sm.bar[1];
+    uint64_t* k_empty = &sm.bar[3];
     uint64_t* s_full = &sm.bar[5];
     uint64_t* p_full = &sm.bar[7];
     uint64_t* o_done = &sm.bar[9];
     uint64_t* xbar = &sm.bar[11];
-    const uint32_t counts[13] = {1, 1, 1, 1, 1, 1, 1, NSM, NSM, 1, 1, NSM, NSM};
-    setup(sm, 13, counts);
+    uint64_t* v_empty = &sm.bar[13];
+    uint64_t* v_full = &sm.bar[15];
+    const uint32_t counts[17] = {1, 1, 1, 1, 1, 1, 1, NSM, NSM, 1, 1, NSM, NSM, 1, 1, 1, 1};
+    setup(sm, 17, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* Q = sm.base;
     auto Kt = [&](int st) { return sm.base + (1 + 2 * st) * TILE; };
@@ -233,36 +238,40 @@ __global__ void __launch_bounds__(NT, 1)
         load_tile(Q, &mq, q_full, col, rowq);
         for (int j = 0; j < nkb; ++j) {
             const int st = j & 1;
-            if (!tc::mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
-            tc::mbar_expect_tx(&kv_full[st], 2 * TILE);
-            load_tile(Kt(st), &mk, &kv_full[st], col, b * p.T + j * BR);
-            load_tile(Vt(st), &mv, &kv_full[st], col, b * p.T + j * BR);
+            if (!tc::mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
+            tc::mbar_expect_tx(&k_full[st], TILE);
+            load_tile(Kt(st), &mk, &k_full[st], col, b * p.T + j * BR);
+            if (!tc::mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
+            tc::mbar_expect_tx(&v_full[st], TILE);
+            load_tile(Vt(st), &mv, &v_full[st], col, b * p.T + j * BR);
         }
     } else if (warp == 1 && lane == 0) {
         const uint32_t q0 = tc::smem_u32(Q);
         bool ok = tc::mbar_wait(q_full, 0, sm.abort);
         auto issue_s = [&](int j) -> bool {
             const int st = j & 1;
-            if (!tc::mbar_wait(&kv_full[st], (j >> 1) & 1, sm.abort)) return false;
+            if (!tc::mbar_wait(&k_full[st], (j >> 1) & 1, sm.abort)) return false;
             tc::fence_after();
             const uint32_t k0 = tc::smem_u32(Kt(st));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc::mma_bf16(tmem + (j & 1) * 128, dk_(q0, kk), dk_(k0, kk), IDESC_KK, kk > 0);
             tc::mma_commit(&s_full[j & 1]);
+            tc::mma_commit(&k_empty[st]);
             return true;
         };
         if (ok) ok = issue_s(0);
         for (int j = 0; ok && j < nkb; ++j) {
             if (j + 1 < nkb && !issue_s(j + 1)) break;
             if (!tc::mbar_wait(&p_full[j & 1], (j >> 1) & 1, sm.abort)) break;
+            if (!tc::mbar_wait(&v_full[j & 1], (j >> 1) & 1, sm.abort)) break;
             tc::fence_after();
             const uint32_t p0 = tc::smem_u32(Pt(j & 1)), v0 = tc::smem_u32(Vt(j & 1));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc::mma_bf16(tmem + 256, dk_(p0, kk), dm_(v0, kk), IDESC_KM, (j > 0 || kk > 0));
             tc::mma_commit(&o_done[j & 1]);
-            tc::mma_commit(&kv_empty[j & 1]);
+            tc::mma_commit(&v_empty[j & 1]);
         }
     } else if (warp >= 2) {
         const int g = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;
@@ -343,7 +352,8 @@ __global__ void __launch_bounds__(NT, 1)
 
 // ===================================================================== dQ
 // smem tiles: 0 Q | 1 dO | 2,3 K/V stage 0 | 4,5 K/V stage 1 | 6 dS
-// barriers: 0 qd_full, 1-2 kv_full, 3-4 kv_empty, 5 s_full, 6 s_free, 7 ds_full, 8 dq_done
+// barriers: 0 qd_full, 1-2 kv_full, 3-4 k_empty, 5 s_full, 6 s_free, 7 ds_full, 8 dq_done,
+//           9-10 v_empty  (a V tile is released after dP, a K tile after dQ)
 // TMEM: S at 0, dP at 128, dQ at 256.
 constexpr int DQ_TILES = 7;
 
@@ -354,18 +364,19 @@ __global__ void __launch_bounds__(NT, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DQ_TILES);
-    const int qb = p.nblk - 1 - blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int qb = p.nblk - 1 - blockIdx.y, h = blockIdx.x % p.H, b = blockIdx.x / p.H;
     const int nkb = qb + 1;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* qd_full = &sm.bar[0];
     uint64_t* kv_full = &sm.bar[1];
-    uint64_t* kv_empty = &sm.bar[3];
+    uint64_t* k_empty = &sm.bar[3];
     uint64_t* s_full = &sm.bar[5];
     uint64_t* s_free = &sm.bar[6];
     uint64_t* ds_full = &sm.bar[7];
     uint64_t* dq_done = &sm.bar[8];
-    const uint32_t counts[9] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1};
-    setup(sm, 9, counts);
+    uint64_t* v_empty = &sm.bar[9];
+    const uint32_t counts[11] = {1, 2, 2, 1, 1, 1, NSM, NSM, 1, 1, 1};
+    setup(sm, 11, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* Q = sm.base;
     uint8_t* dO = sm.base + TILE;
@@ -381,10 +392,12 @@ __global__ void __launch_bounds__(NT, 1)
         load_tile(dO, &mdo, qd_full, col, rowq);
         for (int j = 0; j < nkb; ++j) {
             const int st = j & 1;
-            if (!tc::mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
-            tc::mbar_expect_tx(&kv_full[st], 2 * TILE);
-            load_tile(Kt(st), &mk, &kv_full[st], col, b * p.T + j * BR);
+            if (!tc::mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
+            tc::mbar_expect_tx(&kv_full[st], TILE);
             load_tile(Vt(st), &mv, &kv_full[st], col, b * p.T + j * BR);
+            if (!tc::mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
+            tc::mbar_expect_tx(&kv_full[st], TILE);
+            load_tile(Kt(st), &mk, &kv_full[st], col, b * p.T + j * BR);
         }
     } else if (warp == 1 && lane == 0) {
         const uint32_t q0 = tc::smem_u32(Q), do0 = tc::smem_u32(dO), ds0 = tc::smem_u32(dS);
@@ -401,13 +414,14 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128, dk_(do0, kk), dk_(v0, kk), IDESC_KK, kk > 0);
             tc::mma_commit(s_full);
+            tc::mma_commit(&v_empty[st]);
             if (!(ok = tc::mbar_wait(ds_full, j & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc::mma_bf16(tmem + 256, dk_(ds0, kk), dm_(k0, kk), IDESC_KM, (j > 0 || kk > 0));
             tc::mma_commit(dq_done);
-            tc::mma_commit(&kv_empty[st]);
+            tc::mma_commit(&k_empty[st]);
         }
     } else if (warp >= 2) {
         const int g = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;
@@ -468,7 +482,7 @@ __global__ void __launch_bounds__(NT, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DKV_TILES);
-    const int kb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int kb = blockIdx.y, h = blockIdx.x % p.H, b = blockIdx.x / p.H;  // early keys (most work) first
     const int nq = p.nblk - kb;        // query blocks kb .. nblk-1
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* kv_full = &sm.bar[0];
@@ -642,7 +656,7 @@ int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, b
     AttnParams p{};
     p.T = T; p.H = H; p.nblk = ceil_div(T, BR); p.ldo = ldo; p.o = o; p.lse = lse;
     p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
-    attn_fwd_kernel<<<dim3(p.nblk, H, B), NT, smem_bytes(FWD_TILES), s>>>(mq, mk, mv, p);
+    attn_fwd_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(FWD_TILES), s>>>(mq, mk, mv, p);
     note_launch();
     NC_LAUNCH_CHECK("attn_fwd_kernel");
     return NC_OK;
@@ -667,8 +681,8 @@ int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, 
     p.T = T; p.H = H; p.nblk = ceil_div(T, BR); p.ldo = ldo; p.ldd = ldd;
     p.lse = const_cast<float*>(lse); p.delta = delta; p.dq = dq; p.dk = dk; p.dv = dv; p.rope = rope;
     p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
-    attn_dkdv_kernel<<<dim3(p.nblk, H, B), NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);
-    attn_dq_kernel<<<dim3(p.nblk, H, B), NT, smem_bytes(DQ_TILES), s>>>(mq, mk, mv, mdo, p);
+    attn_dkdv_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);
+    attn_dq_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(DQ_TILES), s>>>(mq, mk, mv, mdo, p);
     note_launch(2);
     NC_LAUNCH_CHECK("attn backward kernels");
     return NC_OK;
