@@ -70,7 +70,7 @@ struct nc_model {
     float* nll;
     float* g;          // residual gradient fp32 [M, d]
     void* gT;          // its act-type copy (bf16 mode)
-    float* dy;         // fp32 [M, d]
+    void* dy;          // gradient at a norm output [M, d] (act type)
     void* dqkv;
     void* dO;
     void* dh;
@@ -163,7 +163,7 @@ void layout(nc_model* m, char* base, size_t* total) {
         m->nll = (float*)c.take(M * 4);
         m->g = (float*)c.take(M * d * 4);
         m->gT = m->dtype == NC_BF16 ? c.take(M * d * act) : nullptr;
-        m->dy = (float*)c.take(M * d * 4);
+        m->dy = c.take(M * d * act);
         m->dqkv = c.take(M * 3 * d * act);
         m->dO = c.take(M * d * act);
         m->dh = c.take(M * 4 * d * act);
@@ -266,8 +266,8 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         return rmsnorm_forward<T>(x, (T*)y, r, M, d, s);
     };
     auto norm_b = [&](void* y, float* r, const float* gin) {
-        Prof pr(m, NC_PROF_NORM, 0, Md * (4 + ab + (gin ? 4 : 0) + 4 + (gT ? ab : 0)) + M * 4.0);
-        return rmsnorm_backward<T>(m->dy, (T*)y, r, gin, m->g, gT, M, d, s);
+        Prof pr(m, NC_PROF_NORM, 0, Md * (ab + ab + (gin ? 4 : 0) + 4 + (gT ? ab : 0)) + M * 4.0);
+        return rmsnorm_backward<T>((const T*)m->dy, (T*)y, r, gin, m->g, gT, M, d, s);
     };
     auto rope = [&](void* qkv, float sign) {
         Prof pr(m, NC_PROF_ROPE, 0, 4.0 * Md * ab);
@@ -324,7 +324,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
     // ------------------------------------------------ backward
     float* G = m->grads;
     NC_TRY(weight_grad(m, G + m->poff[iu], V, d, m->logits, V, m->yf, d, M, accumulate));
-    NC_TRY(run_gemm(m, mk(m, M, d, V, m->logits, V, false, W<T>(m, iu), d, true, m->dy, d, NC_FP32)));
+    NC_TRY(run_gemm(m, mk(m, M, d, V, m->logits, V, false, W<T>(m, iu), d, true, m->dy, d, act)));
     NC_TRY(norm_b(m->yf, m->rf, nullptr));
     for (int l = m->depth - 1; l >= 0; --l) {
         auto& Ly = m->L[l];
@@ -337,7 +337,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
             NC_TRY(run_gemm(m, g));
         }
         NC_TRY(weight_grad(m, G + m->poff[b0 + 4], F, d, m->dh, F, Ly.y2, d, M, accumulate));
-        NC_TRY(run_gemm(m, mk(m, M, d, F, m->dh, F, false, W<T>(m, b0 + 4), d, true, m->dy, d, NC_FP32)));
+        NC_TRY(run_gemm(m, mk(m, M, d, F, m->dh, F, false, W<T>(m, b0 + 4), d, true, m->dy, d, act)));
         NC_TRY(norm_b(Ly.y2, Ly.r2, m->g));
         // attention block
         NC_TRY(weight_grad(m, G + m->poff[b0 + 3], d, d, gop, d, Ly.o, d, M, accumulate));
@@ -353,7 +353,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         }
         if (!unroped) NC_TRY(rope(m->dqkv, -1.f));
         NC_TRY(weight_grad(m, G + m->poff[b0], 3 * d, d, m->dqkv, 3 * d, Ly.y1, d, M, accumulate));
-        NC_TRY(run_gemm(m, mk(m, M, d, 3 * d, m->dqkv, 3 * d, false, W<T>(m, b0), d, true, m->dy, d, NC_FP32)));
+        NC_TRY(run_gemm(m, mk(m, M, d, 3 * d, m->dqkv, 3 * d, false, W<T>(m, b0), d, true, m->dy, d, act)));
         NC_TRY(norm_b(Ly.y1, Ly.r1, m->g));
     }
     {

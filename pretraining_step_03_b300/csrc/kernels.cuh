@@ -49,7 +49,7 @@ template <typename T>
 int rmsnorm_forward(const float* x, T* y, float* r, int M, int d, cudaStream_t s);
 // g_out = g_in + r*(dy - y*mean(dy*y)); g_out may alias g_in; gT optional copy
 template <typename T>
-int rmsnorm_backward(const float* dy, const T* y, const float* r, const float* g_in,
+int rmsnorm_backward(const T* dy, const T* y, const float* r, const float* g_in,
                      float* g_out, T* gT, int M, int d, cudaStream_t s);
 // in place on the q and k thirds of qkv rows (row stride ld): sign +1 fwd, -1 bwd
 template <typename T>

@@ -82,20 +82,20 @@ __global__ void rmsnorm_fwd_kernel(const float* x, T* y, float* r, int M, int d)
 
 // g_out = g_in + r * (dy - y * mean(dy * y)) (g_in null = 0); optional low-precision copy gT.
 template <typename T>
-__global__ void rmsnorm_bwd_kernel(const float* dy, const T* y, const float* r, const float* g_in,
+__global__ void rmsnorm_bwd_kernel(const T* dy, const T* y, const float* r, const float* g_in,
                                    float* g_out, T* gT, int M, int d) {
     const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, lane = threadIdx.x % 32;
     if (row >= M) return;
     const long o = (long)row * d;
     float dot = 0.f;
     for (int i = lane * 4; i < d; i += 128) {
-        float4 a = load4<float>(dy + o + i), b = load4<T>(y + o + i);
+        float4 a = load4<T>(dy + o + i), b = load4<T>(y + o + i);
         dot += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
     }
     dot = warp_sum(dot) / (float)d;
     const float rr = r[row];
     for (int i = lane * 4; i < d; i += 128) {
-        float4 a = load4<float>(dy + o + i), b = load4<T>(y + o + i);
+        float4 a = load4<T>(dy + o + i), b = load4<T>(y + o + i);
         float4 g = g_in ? load4<float>(g_in + o + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         float4 out = make_float4(g.x + rr * (a.x - b.x * dot), g.y + rr * (a.y - b.y * dot),
                                  g.z + rr * (a.z - b.z * dot), g.w + rr * (a.w - b.w * dot));
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(CE_THREADS) ce_rows_kernel(bf16* z, const int3
         zt_s = ok ? __bfloat162float(z[row * V + t]) : 0.f;
     }
     float mx = -INFINITY;
-#pragma unroll 4
+#pragma unroll 16
     for (int k = 0; k < nv; ++k) {
         const uint4 u = zr[threadIdx.x + k * CE_THREADS];
         row_s[threadIdx.x + k * CE_THREADS] = u;
@@ -424,7 +424,7 @@ int rmsnorm_forward(const float* x, T* y, float* r, int M, int d, cudaStream_t s
 }
 
 template <typename T>
-int rmsnorm_backward(const float* dy, const T* y, const float* r, const float* g_in, float* g_out,
+int rmsnorm_backward(const T* dy, const T* y, const float* r, const float* g_in, float* g_out,
                      T* gT, int M, int d, cudaStream_t s) {
     if (M <= 0) return NC_OK;
     rmsnorm_bwd_kernel<T><<<ceil_div(M, 8), 256, 0, s>>>(dy, y, r, g_in, g_out, gT, M, d);
@@ -528,7 +528,7 @@ int cast_f32_bf16(const float* x, bf16* y, long n, cudaStream_t s) {
     template int embed_forward<T>(const int32_t*, const T*, float*, int, int, int, uint32_t*,   \
                                   cudaStream_t);                                                \
     template int rmsnorm_forward<T>(const float*, T*, float*, int, int, cudaStream_t);          \
-    template int rmsnorm_backward<T>(const float*, const T*, const float*, const float*, float*, \
+    template int rmsnorm_backward<T>(const T*, const T*, const float*, const float*, float*, \
                                      T*, int, int, cudaStream_t);                               \
     template int rope_apply<T>(T*, long, int, int, int, int, const float2*, float, cudaStream_t); \
     template int cross_entropy<T>(T*, const int32_t*, float*, int, int, float, uint32_t*,       \
