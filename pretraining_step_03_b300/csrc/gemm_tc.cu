@@ -202,6 +202,58 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
     }
 }
 
+// The epilogue of one accumulator tile for one row (this thread's TMEM lane).
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int split, int row, int tn,
+                                              uint32_t tbase) {
+    if (p.epi == EPI_ROPE) {
+        // chunk pairs (a, a+2) hold head-dim pairs (j, j+64) of one 128-wide head
+#pragma unroll 1
+        for (int pr = 0; pr < BN / 64; ++pr) {
+            const int a = (pr >> 1) * 4 + (pr & 1);
+            uint32_t ra[32], rb[32];
+            tc::tmem_ld32(tbase + a * 32, ra);
+            tc::tmem_ld32(tbase + (a + 2) * 32, rb);
+            tc::tmem_wait_ld();
+            const int na = tn * BN + a * 32;
+            if (row < p.M && na < p.N) {
+                float va[32], vb[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    va[j] = __uint_as_float(ra[j]) * p.alpha;
+                    vb[j] = __uint_as_float(rb[j]) * p.alpha;
+                }
+                if (na < p.rope_cols) {
+                    const float2* cs = p.rope + (long)(row % p.rope_T) * 64 + (pr & 1) * 32;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float2 c = __ldg(cs + j);
+                        const float x1 = va[j], x2 = vb[j];
+                        va[j] = x1 * c.x - x2 * c.y;
+                        vb[j] = x2 * c.x + x1 * c.y;
+                    }
+                }
+                const long ci = (long)b * p.sC + (long)row * p.ldc + na;
+                st32(p.C, ci, p.c_dtype, va);
+                st32(p.C, ci + 64, p.c_dtype, vb);
+            }
+        }
+    } else
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(tbase + c * 32, r);
+        tc::tmem_wait_ld();
+        const int n0 = tn * BN + c * 32;
+        if (row < p.M && n0 < p.N) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            epilogue32(p, b, split, row, n0, v);
+        }
+    }
+}
+
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -336,52 +388,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_after();
             const int row = tm * BM + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            if (p.epi == EPI_ROPE) {
-                // chunk pairs (a, a+2) hold head-dim pairs (j, j+64) of one 128-wide head
-#pragma unroll 1
-                for (int pr = 0; pr < BN / 64; ++pr) {
-                    const int a = (pr >> 1) * 4 + (pr & 1);
-                    uint32_t ra[32], rb[32];
-                    tc::tmem_ld32(tbase + a * 32, ra);
-                    tc::tmem_ld32(tbase + (a + 2) * 32, rb);
-                    tc::tmem_wait_ld();
-                    const int na = tn * BN + a * 32;
-                    if (row < p.M && na < p.N) {
-                        float va[32], vb[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            va[j] = __uint_as_float(ra[j]) * p.alpha;
-                            vb[j] = __uint_as_float(rb[j]) * p.alpha;
-                        }
-                        if (na < p.rope_cols) {
-                            const float2* cs = p.rope + (long)(row % p.rope_T) * 64 + (pr & 1) * 32;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const float2 c = __ldg(cs + j);
-                                const float x1 = va[j], x2 = vb[j];
-                                va[j] = x1 * c.x - x2 * c.y;
-                                vb[j] = x2 * c.x + x1 * c.y;
-                            }
-                        }
-                        const long ci = (long)b * p.sC + (long)row * p.ldc + na;
-                        st32(p.C, ci, p.c_dtype, va);
-                        st32(p.C, ci + 64, p.c_dtype, vb);
-                    }
-                }
-            } else
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tc::tmem_ld32(tbase + c * 32, r);
-                tc::tmem_wait_ld();
-                const int n0 = tn * BN + c * 32;
-                if (row < p.M && n0 < p.N) {
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    epilogue32(p, b, split, row, n0, v);
-                }
-            }
+            epilogue_tile<BN>(p, b, split, row, tn, tbase);
             tc::fence_before();
             tc::mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -395,6 +402,166 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 1) {
         tc::fence_after();
         tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- CTA-pair kernel
+// Two CTAs of a cluster share one 256 x 256 output tile: CTA rank r owns rows
+// [128 r, 128 r + 128) of A and of B (the N rows), and its TMEM holds its 128
+// output rows.  The leader (rank 0) issues tcgen05.mma.cta_group::2 (M=256,
+// N=256, K=16), which reads A and B halves from both CTAs' shared memory, so
+// each SM streams half the operand bytes per FLOP of the 1-CTA tile.  Both
+// CTAs' TMA loads complete on the leader's full barrier; the leader's commits
+// multicast to both CTAs' empty / accumulator-full barriers; both CTAs'
+// epilogue warps release an accumulator on the leader's barrier.
+constexpr int P_BN = 256, P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2, P_B_BYTES = 128 * BK * 2;
+constexpr int P_STAGE = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM = P_STAGES * P_STAGE + 1024 + 256;
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const TcParams p) {
+    constexpr int S = P_STAGES;
+    constexpr uint32_t IDESC = tc::idesc_bf16(256, P_BN, A_MN, B_MN);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * P_STAGE);
+    uint64_t* empty = full + S;
+    uint64_t* tfull = empty + S;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = tc::cluster_ctarank();
+    const long cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&tfull[a], 1);
+            tc::mbar_init(&tempty[a], 8);   // 4 epilogue warps x 2 CTAs
+        }
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch(&tmA);
+        tc::tma_prefetch(&tmB);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc2(tmem_slot, 512);
+        tc::tmem_relinquish2();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::cluster_sync();   // barriers of both CTAs initialised before any cross-CTA signal
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- TMA producer (both CTAs)
+        int stage = 0;
+        uint32_t ph = 0;
+        for (long u = cluster; u < p.units; u += nclusters) {
+            int b, split, tm, tn, kb0, kb1;
+            decode(p, u, b, split, tm, tn);
+            kb_range(p, split, kb0, kb1);
+            const int row_a = tm * 256 + (int)rank * 128, row_b = tn * P_BN + (int)rank * 128;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!tc::mbar_wait(&empty[stage], ph ^ 1, abort_flag)) { ok = false; break; }
+                uint8_t* sa = smem + stage * P_STAGE;
+                uint8_t* sb = sa + P_A_BYTES;
+                const uint32_t fb = tc::mapa(tc::smem_u32(&full[stage]), 0);
+                if (rank == 0) tc::mbar_expect_tx(&full[stage], 2 * P_STAGE);
+                if (!A_MN) {
+                    tc::tma_load_3d_pair(sa, &tmA, fb, kb * BK, row_a, b);
+                } else {
+                    tc::tma_load_3d_pair(sa, &tmA, fb, row_a, kb * BK, b);
+                    tc::tma_load_3d_pair(sa + 8192, &tmA, fb, row_a + 64, kb * BK, b);
+                }
+                if (!B_MN) {
+                    tc::tma_load_3d_pair(sb, &tmB, fb, kb * BK, row_b, b);
+                } else {
+                    tc::tma_load_3d_pair(sb, &tmB, fb, row_b, kb * BK, b);
+                    tc::tma_load_3d_pair(sb + 8192, &tmB, fb, row_b + 64, kb * BK, b);
+                }
+                if (++stage == S) { stage = 0; ph ^= 1; }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---------------------------------------------------- MMA issuer (leader only)
+        int stage = 0, acc = 0;
+        uint32_t ph = 0, aph = 0;
+        for (long u = cluster; u < p.units; u += nclusters) {
+            int b, split, tm, tn, kb0, kb1;
+            decode(p, u, b, split, tm, tn);
+            kb_range(p, split, kb0, kb1);
+            if (!tc::mbar_wait(&tempty[acc], aph ^ 1, abort_flag)) break;
+            tc::fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * P_BN);
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!tc::mbar_wait(&full[stage], ph, abort_flag)) { ok = false; break; }
+                tc::fence_after();
+                const uint32_t a0 = tc::smem_u32(smem + stage * P_STAGE);
+                const uint32_t b0 = a0 + P_A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t ad = A_MN ? tc::sdesc(a0 + kk * 2048, 8192, 1024)
+                                             : tc::sdesc(a0 + kk * 32, 16, 1024);
+                    const uint64_t bd = B_MN ? tc::sdesc(b0 + kk * 2048, 8192, 1024)
+                                             : tc::sdesc(b0 + kk * 32, 16, 1024);
+                    tc::mma2_bf16(d, ad, bd, IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma2_commit_mc(&empty[stage], 0x3);
+                if (++stage == S) { stage = 0; ph ^= 1; }
+            }
+            if (!ok) break;
+            tc::mma2_commit_mc(&tfull[acc], 0x3);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1;
+        }
+        if (*abort_flag) {
+            tc::mma2_commit_mc(drain, 0x1);
+            tc::mbar_wait_drain(drain, 0);
+        }
+    } else if (warp >= 2) {
+        // ---------------------------------------------------- epilogue (both CTAs)
+        const int q = warp & 3;
+        const uint32_t tempty_leader = tc::mapa(tc::smem_u32(&tempty[0]), 0);
+        int acc = 0;
+        uint32_t aph = 0;
+        for (long u = cluster; u < p.units; u += nclusters) {
+            int b, split, tm, tn;
+            decode(p, u, b, split, tm, tn);
+            if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
+            tc::fence_after();
+            const int row = tm * 256 + (int)rank * 128 + q * 32 + lane;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_BN);
+            epilogue_tile<P_BN>(p, b, split, row, tn, tbase);
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(tempty_leader + acc * 8);
+            acc ^= 1;
+            if (acc == 0) aph ^= 1;
+        }
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    tc::cluster_sync();   // no CTA leaves while its peer may still signal it
+    if (threadIdx.x == 0 && *abort_flag && p.flag) atomicOr(p.flag, NC_FLAG_TIMEOUT);
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc2(tmem, 512);
     }
 }
 
@@ -430,9 +597,37 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cuda
     return NC_OK;
 }
 
-int pick_splits(const Gemm& g, int tiles, int num_kb) {
+template <bool A_MN, bool B_MN>
+int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM),
+                          "gemm_tc2 smem attribute"));
+        attr = true;
+    }
+    long clusters = p.units < num_sms() / 2 ? p.units : num_sms() / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = P_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    NC_TRY(cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN>, ma, mb, p), "gemm_tc2 launch"));
+    note_launch();
+    NC_LAUNCH_CHECK("gemm_tc2");
+    return NC_OK;
+}
+
+int pick_splits(const Gemm& g, int tiles, int num_kb, int slots) {
     const long work = (long)tiles * g.batch;
-    const int sms = num_sms();
+    const int sms = slots;
     if (work >= sms || num_kb < 8 || g.epi != EPI_STORE) return 1;
     int s = (int)((2L * sms + work - 1) / work);
     s = s < num_kb / 4 ? s : num_kb / 4;
@@ -503,22 +698,28 @@ bool gemm_tc_supported(const Gemm& g) {
     return true;
 }
 
+// CTA pairs (256 x 256 tiles) for every GEMM big enough to fill them.
+static bool use_pairs(const Gemm& g) { return g.M >= 256 && g.N >= 256; }
+
 size_t gemm_tc_splitk_bytes(const Gemm& g) {
-    const int bn = g.N > 128 ? 256 : 128;
-    const int tiles = ceil_div(g.M, BM) * ceil_div(g.N, bn);
-    const int s = pick_splits(g, tiles, ceil_div(g.K, BK));
+    const bool pair = use_pairs(g);
+    const int bm = pair ? 256 : BM, bn = pair ? P_BN : (g.N > 128 ? 256 : 128);
+    const int tiles = ceil_div(g.M, bm) * ceil_div(g.N, bn);
+    const int s = pick_splits(g, tiles, ceil_div(g.K, BK), pair ? num_sms() / 2 : num_sms());
     return s > 1 ? (size_t)s * g.batch * g.M * g.N * 4 : 0;
 }
 
 int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     if (!gemm_tc_supported(g)) return set_error(NC_ERR_UNSUPPORTED, "gemm_tc: unsupported operands");
-    const int bn = g.N > 128 ? 256 : 128;
+    const bool pair = use_pairs(g);
+    const int bm = pair ? 256 : BM;
+    const int bn = pair ? P_BN : (g.N > 128 ? 256 : 128);
     TcParams p{};
     p.M = g.M; p.N = g.N; p.K = g.K; p.batch = g.batch;
-    p.tiles_m = ceil_div(g.M, BM);
+    p.tiles_m = ceil_div(g.M, bm);
     p.tiles_n = ceil_div(g.N, bn);
     p.num_kb = ceil_div(g.K, BK);
-    p.splits = pick_splits(g, p.tiles_m * p.tiles_n, p.num_kb);
+    p.splits = pick_splits(g, p.tiles_m * p.tiles_n, p.num_kb, pair ? num_sms() / 2 : num_sms());
     size_t need = p.splits > 1 ? (size_t)p.splits * g.batch * g.M * g.N * 4 : 0;
     if (need > ws_bytes || ws == nullptr) p.splits = 1;
     p.units = (long)p.tiles_m * p.tiles_n * p.splits * g.batch;
@@ -532,11 +733,16 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     CUtensorMap ma, mb;
     if (!g.a_t) NC_TRY(make_map(&ma, g.A, g.K, g.M, g.batch, g.lda, g.sA, 64, BM));
     else        NC_TRY(make_map(&ma, g.A, g.M, g.K, g.batch, g.lda, g.sA, 64, 64));
-    if (!g.b_t) NC_TRY(make_map(&mb, g.B, g.K, g.N, g.batch, g.ldb, g.sB, 64, bn));
+    if (!g.b_t) NC_TRY(make_map(&mb, g.B, g.K, g.N, g.batch, g.ldb, g.sB, 64, pair ? 128 : bn));
     else        NC_TRY(make_map(&mb, g.B, g.N, g.K, g.batch, g.ldb, g.sB, 64, 64));
 
     int rc;
-    if (bn == 256) {
+    if (pair) {
+        if (!g.a_t && !g.b_t) rc = launch2<false, false>(ma, mb, p, s);
+        else if (!g.a_t && g.b_t) rc = launch2<false, true>(ma, mb, p, s);
+        else if (g.a_t && !g.b_t) rc = launch2<true, false>(ma, mb, p, s);
+        else rc = launch2<true, true>(ma, mb, p, s);
+    } else if (bn == 256) {
         if (!g.a_t && !g.b_t) rc = launch<256, false, false>(ma, mb, p, s);
         else if (!g.a_t && g.b_t) rc = launch<256, false, true>(ma, mb, p, s);
         else if (g.a_t && !g.b_t) rc = launch<256, true, false>(ma, mb, p, s);

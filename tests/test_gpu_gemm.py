@@ -63,3 +63,16 @@ def test_split_k_weight_gradient_shape():
 def test_d20_projection_shape():
     got, ref = _run(1024, 3840, 1280, 0, 0, c_dtype="bf16")
     assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= 8e-3
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_cta_pair_tiles_ragged(ta, tb):
+    # M, N >= 256 run on CTA pairs (256 x 256 tiles); ragged in M, N and K
+    got, ref = _run(520, 776, 200, ta, tb)
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= 1e-4
+
+
+def test_cta_pair_batched_square():
+    # the Newton-Schulz shape class: batched square products, B stored [K, N]
+    got, ref = _run(384, 384, 384, 0, 1, batch=3, c_dtype="bf16", beta=1.0)
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= 8e-3
