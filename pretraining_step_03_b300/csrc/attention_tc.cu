@@ -13,9 +13,13 @@
 // same bytes serve as a K-major operand (K = the 128 columns) and as an
 // MN-major operand (K = the 128 rows), so K, V, Q and dO are loaded once and
 // used in both orientations.  One CTA: warp 0 issues TMA loads, warp 1
-// issues tcgen05.mma from one thread, warps 2-5 (128 threads, one row each)
-// do the softmax arithmetic on rows read from TMEM and write bf16 operand
-// tiles back to shared memory.
+// issues tcgen05.mma from one thread, warps 2-9 do the softmax arithmetic on
+// rows read from TMEM.  The probabilities (P, P^T) and score gradients (dS,
+// dS^T) never touch shared memory: they are written back into TMEM as packed
+// bf16 over the scores they came from and used from there as the A operand
+// of the next product, which keeps shared-memory bandwidth for the operands
+// TMA brings in (an M=128, N=128 MMA from shared memory already reads at the
+// SM's shared-memory bandwidth).
 //
 // forward (one CTA per 128-query block, keys in 128-blocks up to the diagonal):
 //   S_j = Q K_j^T into one of two TMEM buffers (the next S overlaps the
@@ -196,13 +200,22 @@ __device__ __forceinline__ bool exchange(Smem& sm, uint64_t* xbar, int it, int g
     return true;
 }
 
+// write this thread's 64 probabilities, packed bf16 pairs, into row columns
+// [16g, 16g+16) and [32+16g, 32+16g+16) of a TMEM region (the A-operand layout:
+// word c holds keys 2c and 2c+1)
+__device__ __forceinline__ void st_half_bf16(uint32_t taddr, int g, const uint32_t* w) {
+    tc::tmem_st16(taddr + 16 * g, w);
+    tc::tmem_st16(taddr + 32 + 16 * g, w + 16);
+}
+
 // ===================================================================== forward
-// smem tiles: 0 Q | 1,2 K/V stage 0 | 3,4 K/V stage 1 | 5,6 P buffers
-// barriers: 0 q_full, 1-2 k_full, 3-4 k_empty, 5-6 s_full, 7-8 p_full, 9-10 o_done, 11-12 xbar,
-//           13-14 v_empty, 15-16 v_full  (a K tile is released when its S MMA completes,
-//           a V tile after PV)
-// TMEM: S buffers at columns 0 and 128, O at 256.
+// smem tiles: 0 Q | 1..3 K stages | 4..6 V stages
+// barriers: 0 q_full, 1-3 k_full, 4-6 k_empty, 7-9 v_full, 10-12 v_empty, 13-14 s_full,
+//           15-16 p_full, 17-18 o_done, 19-20 xbar
+// TMEM: S buffers at columns 0 and 128 (P_j overwrites the first 64 columns of its
+// S buffer as packed bf16 and is the A operand of O += P V), O at 256.
 constexpr int FWD_TILES = 7;
+constexpr int FWD_NST = 3;
 
 __global__ void __launch_bounds__(NT, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -216,20 +229,19 @@ __global__ void __launch_bounds__(NT, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* q_full = &sm.bar[0];
     uint64_t* k_full = &sm.bar[1];
-    uint64_t* k_empty = &sm.bar[3];
-    uint64_t* s_full = &sm.bar[5];
-    uint64_t* p_full = &sm.bar[7];
-    uint64_t* o_done = &sm.bar[9];
-    uint64_t* xbar = &sm.bar[11];
-    uint64_t* v_empty = &sm.bar[13];
-    uint64_t* v_full = &sm.bar[15];
-    const uint32_t counts[17] = {1, 1, 1, 1, 1, 1, 1, NSM, NSM, 1, 1, NSM, NSM, 1, 1, 1, 1};
-    setup(sm, 17, counts);
+    uint64_t* k_empty = &sm.bar[4];
+    uint64_t* v_full = &sm.bar[7];
+    uint64_t* v_empty = &sm.bar[10];
+    uint64_t* s_full = &sm.bar[13];
+    uint64_t* p_full = &sm.bar[15];
+    uint64_t* o_done = &sm.bar[17];
+    uint64_t* xbar = &sm.bar[19];
+    const uint32_t counts[21] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NSM, NSM, 1, 1, NSM, NSM};
+    setup(sm, 21, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* Q = sm.base;
-    auto Kt = [&](int st) { return sm.base + (1 + 2 * st) * TILE; };
-    auto Vt = [&](int st) { return sm.base + (2 + 2 * st) * TILE; };
-    auto Pt = [&](int i) { return sm.base + (5 + i) * TILE; };
+    auto Kt = [&](int st) { return sm.base + (1 + st) * TILE; };
+    auto Vt = [&](int st) { return sm.base + (1 + FWD_NST + st) * TILE; };
     const int col = h * HD;
     const int rowq = b * p.T + qb * BR;
 
@@ -237,11 +249,12 @@ __global__ void __launch_bounds__(NT, 1)
         tc::mbar_expect_tx(q_full, TILE);
         load_tile(Q, &mq, q_full, col, rowq);
         for (int j = 0; j < nkb; ++j) {
-            const int st = j & 1;
-            if (!tc::mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
+            const int st = j % FWD_NST;
+            const uint32_t ph = ((j / FWD_NST) & 1) ^ 1;
+            if (!tc::mbar_wait(&k_empty[st], ph, sm.abort)) break;
             tc::mbar_expect_tx(&k_full[st], TILE);
             load_tile(Kt(st), &mk, &k_full[st], col, b * p.T + j * BR);
-            if (!tc::mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
+            if (!tc::mbar_wait(&v_empty[st], ph, sm.abort)) break;
             tc::mbar_expect_tx(&v_full[st], TILE);
             load_tile(Vt(st), &mv, &v_full[st], col, b * p.T + j * BR);
         }
@@ -249,8 +262,8 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t q0 = tc::smem_u32(Q);
         bool ok = tc::mbar_wait(q_full, 0, sm.abort);
         auto issue_s = [&](int j) -> bool {
-            const int st = j & 1;
-            if (!tc::mbar_wait(&k_full[st], (j >> 1) & 1, sm.abort)) return false;
+            const int st = j % FWD_NST;
+            if (!tc::mbar_wait(&k_full[st], (j / FWD_NST) & 1, sm.abort)) return false;
             tc::fence_after();
             const uint32_t k0 = tc::smem_u32(Kt(st));
 #pragma unroll
@@ -262,16 +275,19 @@ __global__ void __launch_bounds__(NT, 1)
         };
         if (ok) ok = issue_s(0);
         for (int j = 0; ok && j < nkb; ++j) {
+            // S_{j+1} goes to the other buffer; it was last read as P_{j-1} by PV_{j-1}, issued before
             if (j + 1 < nkb && !issue_s(j + 1)) break;
+            const int st = j % FWD_NST;
             if (!tc::mbar_wait(&p_full[j & 1], (j >> 1) & 1, sm.abort)) break;
-            if (!tc::mbar_wait(&v_full[j & 1], (j >> 1) & 1, sm.abort)) break;
+            if (!tc::mbar_wait(&v_full[st], (j / FWD_NST) & 1, sm.abort)) break;
             tc::fence_after();
-            const uint32_t p0 = tc::smem_u32(Pt(j & 1)), v0 = tc::smem_u32(Vt(j & 1));
+            const uint32_t v0 = tc::smem_u32(Vt(st));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tmem + 256, dk_(p0, kk), dm_(v0, kk), IDESC_KM, (j > 0 || kk > 0));
+                tc::mma_bf16_ts(tmem + 256, tmem + (j & 1) * 128 + kk * 8, dm_(v0, kk), IDESC_KM,
+                                (j > 0 || kk > 0));
             tc::mma_commit(&o_done[j & 1]);
-            tc::mma_commit(&v_empty[j & 1]);
+            tc::mma_commit(&v_empty[st]);
         }
     } else if (warp >= 2) {
         const int g = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;
@@ -283,7 +299,8 @@ __global__ void __launch_bounds__(NT, 1)
         for (int j = 0; j < nkb; ++j) {
             if (!(ok = tc::mbar_wait_warp(&s_full[j & 1], (j >> 1) & 1, sm.abort))) break;
             tc::fence_after();
-            ld_half(tmem + lanes + (j & 1) * 128, g, s);
+            const uint32_t sb = tmem + lanes + (j & 1) * 128;
+            ld_half(sb, g, s);
             float mx = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
@@ -328,9 +345,8 @@ __global__ void __launch_bounds__(NT, 1)
                 w[i] = pack2(a, bb);
             }
             l += sum;
-            if (j >= 2 && !(ok = tc::mbar_wait_warp(&o_done[j & 1], ((j - 2) >> 1) & 1, sm.abort))) break;
-            store_half(Pt(j & 1), r, g, w);
-            tc::fence_async_smem();
+            st_half_bf16(sb, g, w);
+            tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(&p_full[j & 1]);
         }
@@ -351,11 +367,12 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ===================================================================== dQ
-// smem tiles: 0 Q | 1 dO | 2,3 K/V stage 0 | 4,5 K/V stage 1 | 6 dS
-// barriers: 0 qd_full, 1-2 kv_full, 3-4 k_empty, 5 s_full, 6 s_free, 7 ds_full, 8 dq_done,
-//           9-10 v_empty  (a V tile is released after dP, a K tile after dQ)
-// TMEM: S at 0, dP at 128, dQ at 256.
-constexpr int DQ_TILES = 7;
+// smem tiles: 0 Q | 1 dO | 2,3 K stages | 4,5 V stages
+// barriers: 0 qd_full, 1-2 k_full, 3-4 k_empty, 5-6 v_full, 7-8 v_empty, 9 s_full, 10 ds_full,
+//           11 dq_done
+// TMEM: S at 0 (dS overwrites its first 64 columns as packed bf16, the A operand of
+// dQ += dS K), dP at 128, dQ at 256.
+constexpr int DQ_TILES = 6;
 
 __global__ void __launch_bounds__(NT, 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -368,21 +385,20 @@ __global__ void __launch_bounds__(NT, 1)
     const int nkb = qb + 1;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* qd_full = &sm.bar[0];
-    uint64_t* kv_full = &sm.bar[1];
+    uint64_t* k_full = &sm.bar[1];
     uint64_t* k_empty = &sm.bar[3];
-    uint64_t* s_full = &sm.bar[5];
-    uint64_t* s_free = &sm.bar[6];
-    uint64_t* ds_full = &sm.bar[7];
-    uint64_t* dq_done = &sm.bar[8];
-    uint64_t* v_empty = &sm.bar[9];
-    const uint32_t counts[11] = {1, 2, 2, 1, 1, 1, NSM, NSM, 1, 1, 1};
-    setup(sm, 11, counts);
+    uint64_t* v_full = &sm.bar[5];
+    uint64_t* v_empty = &sm.bar[7];
+    uint64_t* s_full = &sm.bar[9];
+    uint64_t* ds_full = &sm.bar[10];
+    uint64_t* dq_done = &sm.bar[11];
+    const uint32_t counts[12] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NSM, 1};
+    setup(sm, 12, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* Q = sm.base;
     uint8_t* dO = sm.base + TILE;
-    auto Kt = [&](int st) { return sm.base + (2 + 2 * st) * TILE; };
-    auto Vt = [&](int st) { return sm.base + (3 + 2 * st) * TILE; };
-    uint8_t* dS = sm.base + 6 * TILE;
+    auto Kt = [&](int st) { return sm.base + (2 + st) * TILE; };
+    auto Vt = [&](int st) { return sm.base + (4 + st) * TILE; };
     const int col = h * HD;
     const int rowq = b * p.T + qb * BR;
 
@@ -392,25 +408,27 @@ __global__ void __launch_bounds__(NT, 1)
         load_tile(dO, &mdo, qd_full, col, rowq);
         for (int j = 0; j < nkb; ++j) {
             const int st = j & 1;
-            if (!tc::mbar_wait(&v_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
-            tc::mbar_expect_tx(&kv_full[st], TILE);
-            load_tile(Vt(st), &mv, &kv_full[st], col, b * p.T + j * BR);
-            if (!tc::mbar_wait(&k_empty[st], ((j >> 1) & 1) ^ 1, sm.abort)) break;
-            tc::mbar_expect_tx(&kv_full[st], TILE);
-            load_tile(Kt(st), &mk, &kv_full[st], col, b * p.T + j * BR);
+            const uint32_t ph = ((j >> 1) & 1) ^ 1;
+            if (!tc::mbar_wait(&k_empty[st], ph, sm.abort)) break;
+            tc::mbar_expect_tx(&k_full[st], TILE);
+            load_tile(Kt(st), &mk, &k_full[st], col, b * p.T + j * BR);
+            if (!tc::mbar_wait(&v_empty[st], ph, sm.abort)) break;
+            tc::mbar_expect_tx(&v_full[st], TILE);
+            load_tile(Vt(st), &mv, &v_full[st], col, b * p.T + j * BR);
         }
     } else if (warp == 1 && lane == 0) {
-        const uint32_t q0 = tc::smem_u32(Q), do0 = tc::smem_u32(dO), ds0 = tc::smem_u32(dS);
+        const uint32_t q0 = tc::smem_u32(Q), do0 = tc::smem_u32(dO);
         bool ok = tc::mbar_wait(qd_full, 0, sm.abort);
         for (int j = 0; ok && j < nkb; ++j) {
             const int st = j & 1;
-            if (!(ok = tc::mbar_wait(&kv_full[st], (j >> 1) & 1, sm.abort))) break;
-            // S and dP of the previous block must have been read out of TMEM
-            if (j > 0 && !(ok = tc::mbar_wait(s_free, (j - 1) & 1, sm.abort))) break;
+            // S_j overwrites the dS_{j-1} that dQ_{j-1} (issued before) reads
+            if (!(ok = tc::mbar_wait(&k_full[st], (j >> 1) & 1, sm.abort))) break;
             tc::fence_after();
             const uint32_t k0 = tc::smem_u32(Kt(st)), v0 = tc::smem_u32(Vt(st));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(q0, kk), dk_(k0, kk), IDESC_KK, kk > 0);
+            if (!(ok = tc::mbar_wait(&v_full[st], (j >> 1) & 1, sm.abort))) break;
+            tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128, dk_(do0, kk), dk_(v0, kk), IDESC_KK, kk > 0);
             tc::mma_commit(s_full);
@@ -419,7 +437,7 @@ __global__ void __launch_bounds__(NT, 1)
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tmem + 256, dk_(ds0, kk), dm_(k0, kk), IDESC_KM, (j > 0 || kk > 0));
+                tc::mma_bf16_ts(tmem + 256, tmem + kk * 8, dm_(k0, kk), IDESC_KM, (j > 0 || kk > 0));
             tc::mma_commit(dq_done);
             tc::mma_commit(&k_empty[st]);
         }
@@ -447,12 +465,8 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int i = 0; i < 32; ++i)
                     w[i] = pack2(s[2 * i] * (d[2 * i] - Dt), s[2 * i + 1] * (d[2 * i + 1] - Dt));
             }
-            tc::fence_before();
-            tc::mbar_arrive(s_free);
-            // the previous dQ MMA must be done reading the dS tile
-            if (j > 0 && !(ok = tc::mbar_wait_warp(dq_done, (j - 1) & 1, sm.abort))) break;
-            store_half(dS, r, g, w);
-            tc::fence_async_smem();
+            st_half_bf16(tmem + lanes, g, w);
+            tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(ds_full);
         }
@@ -469,11 +483,14 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ===================================================================== dK, dV
-// smem tiles: 0 K | 1 V | 2,3 Q/dO stage 0 | 4,5 Q/dO stage 1 | 6 P^T then dS^T
-// barriers: 0 kv_full, 1-2 qd_full, 3-4 qd_empty, 5 s_full, 6 s_free, 7 p_full, 8 dv_done,
-//           9 ds_full, 10 dk_done, 11-12 stat barriers
-// TMEM: S^T at 0, dP^T at 128, dV at 256, dK at 384.
-constexpr int DKV_TILES = 7;
+// smem tiles: 0 K | 1 V | 2,3 Q/dO stage 0 | 4,5 Q/dO stage 1
+// barriers: 0 kv_full, 1-2 qd_full, 3-4 qd_empty, 5 s_full, 6 p_full, 7 ds_full, 8 dk_done,
+//           9-10 stat barriers
+// TMEM: S^T at 0 (P^T overwrites its first 64 columns, packed bf16, the A operand of
+// dV += P^T dO), dP^T at 128 (dS^T likewise, the A operand of dK += dS^T Q), dV at 256,
+// dK at 384.  Issue order per block i: dV_i, S^T_{i+1}, dK_i, dP^T_{i+1}: each product
+// that overwrites a region comes after the product that reads it.
+constexpr int DKV_TILES = 6;
 
 __global__ void __launch_bounds__(NT, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -489,20 +506,17 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* qd_full = &sm.bar[1];
     uint64_t* qd_empty = &sm.bar[3];
     uint64_t* s_full = &sm.bar[5];
-    uint64_t* s_free = &sm.bar[6];
-    uint64_t* p_full = &sm.bar[7];
-    uint64_t* dv_done = &sm.bar[8];
-    uint64_t* ds_full = &sm.bar[9];
-    uint64_t* dk_done = &sm.bar[10];
-    uint64_t* sbar = &sm.bar[11];
-    const uint32_t counts[13] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1, NSM, 1, NSM, NSM};
-    setup(sm, 13, counts);
+    uint64_t* p_full = &sm.bar[6];
+    uint64_t* ds_full = &sm.bar[7];
+    uint64_t* dk_done = &sm.bar[8];
+    uint64_t* sbar = &sm.bar[9];
+    const uint32_t counts[11] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1, NSM, NSM};
+    setup(sm, 11, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* K = sm.base;
     uint8_t* V = sm.base + TILE;
     auto Qt = [&](int st) { return sm.base + (2 + 2 * st) * TILE; };
     auto dOt = [&](int st) { return sm.base + (3 + 2 * st) * TILE; };
-    uint8_t* PS = sm.base + 6 * TILE;
     const int col = h * HD;
     const int rowk = b * p.T + kb * BR;
 
@@ -518,39 +532,47 @@ __global__ void __launch_bounds__(NT, 1)
             load_tile(dOt(st), &mdo, &qd_full[st], col, b * p.T + j * BR);
         }
     } else if (warp == 1 && lane == 0) {
-        const uint32_t k0 = tc::smem_u32(K), v0 = tc::smem_u32(V), ps0 = tc::smem_u32(PS);
-        bool ok = tc::mbar_wait(kv_full, 0, sm.abort);
-        auto issue_s = [&](int i) -> bool {
-            const int st = i & 1;
-            if (!tc::mbar_wait(&qd_full[st], (i >> 1) & 1, sm.abort)) return false;
-            if (i > 0 && !tc::mbar_wait(s_free, (i - 1) & 1, sm.abort)) return false;
+        const uint32_t k0 = tc::smem_u32(K), v0 = tc::smem_u32(V);
+        bool ok = tc::mbar_wait(kv_full, 0, sm.abort) && tc::mbar_wait(&qd_full[0], 0, sm.abort);
+        if (ok) {
             tc::fence_after();
-            const uint32_t q0 = tc::smem_u32(Qt(st)), do0 = tc::smem_u32(dOt(st));
+            const uint32_t q0 = tc::smem_u32(Qt(0)), do0 = tc::smem_u32(dOt(0));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(k0, kk), dk_(q0, kk), IDESC_KK, kk > 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128, dk_(v0, kk), dk_(do0, kk), IDESC_KK, kk > 0);
             tc::mma_commit(s_full);
-            return true;
-        };
-        if (ok) ok = issue_s(0);
+        }
         for (int i = 0; ok && i < nq; ++i) {
-            const int st = i & 1;
+            const int st = i & 1, sn = (i + 1) & 1;
             const uint32_t q0 = tc::smem_u32(Qt(st)), do0 = tc::smem_u32(dOt(st));
+            const bool more = i + 1 < nq;
             if (!(ok = tc::mbar_wait(p_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tmem + 256, dk_(ps0, kk), dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
-            tc::mma_commit(dv_done);
-            if (i + 1 < nq && !(ok = issue_s(i + 1))) break;
+                tc::mma_bf16_ts(tmem + 256, tmem + kk * 8, dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
+            if (more) {
+                if (!(ok = tc::mbar_wait(&qd_full[sn], ((i + 1) >> 1) & 1, sm.abort))) break;
+                tc::fence_after();
+                const uint32_t qn = tc::smem_u32(Qt(sn));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(k0, kk), dk_(qn, kk), IDESC_KK, kk > 0);
+            }
             if (!(ok = tc::mbar_wait(ds_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tmem + 384, dk_(ps0, kk), dm_(q0, kk), IDESC_KM, (i > 0 || kk > 0));
+                tc::mma_bf16_ts(tmem + 384, tmem + 128 + kk * 8, dm_(q0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dk_done);
             tc::mma_commit(&qd_empty[st]);
+            if (more) {
+                const uint32_t don = tc::smem_u32(dOt(sn));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma_bf16(tmem + 128, dk_(v0, kk), dk_(don, kk), IDESC_KK, kk > 0);
+                tc::mma_commit(s_full);
+            }
         }
     } else if (warp >= 2) {
         const int g = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;   // r = key row of the block
@@ -581,9 +603,8 @@ __global__ void __launch_bounds__(NT, 1)
             uint32_t w[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) w[e] = pack2(s[2 * e], s[2 * e + 1]);
-            if (i > 0 && !(ok = tc::mbar_wait_warp(dk_done, (i - 1) & 1, sm.abort))) break;
-            store_half(PS, r, g, w);
-            tc::fence_async_smem();
+            st_half_bf16(tmem + lanes, g, w);
+            tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(p_full);
             {   // dS^T = P^T (dP^T - D[c])
@@ -594,11 +615,8 @@ __global__ void __launch_bounds__(NT, 1)
                     w[e] = pack2(s[2 * e] * (d[2 * e] - stat[128 + col_of(g, 2 * e)]),
                                  s[2 * e + 1] * (d[2 * e + 1] - stat[128 + col_of(g, 2 * e + 1)]));
             }
-            tc::fence_before();
-            tc::mbar_arrive(s_free);
-            if (!(ok = tc::mbar_wait_warp(dv_done, i & 1, sm.abort))) break;
-            store_half(PS, r, g, w);
-            tc::fence_async_smem();
+            st_half_bf16(tmem + lanes + 128, g, w);
+            tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(ds_full);
         }
