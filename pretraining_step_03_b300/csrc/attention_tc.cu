@@ -263,6 +263,10 @@ __global__ void __launch_bounds__(NT, 1)
         bool ok = tc::mbar_wait(q_full, 0, sm.abort);
         auto issue_s = [&](int j) -> bool {
             const int st = j % FWD_NST;
+            // P_{j-2} in this S buffer is the A operand of PV_{j-2}: an MMA's TMEM
+            // writes are not ordered after an earlier MMA's TMEM operand reads, so
+            // wait for PV_{j-2} to complete (PV_{j-1} keeps the pipe busy meanwhile)
+            if (j >= 2 && !tc::mbar_wait(&o_done[j & 1], ((j - 2) >> 1) & 1, sm.abort)) return false;
             if (!tc::mbar_wait(&k_full[st], (j / FWD_NST) & 1, sm.abort)) return false;
             tc::fence_after();
             const uint32_t k0 = tc::smem_u32(Kt(st));
@@ -275,7 +279,6 @@ __global__ void __launch_bounds__(NT, 1)
         };
         if (ok) ok = issue_s(0);
         for (int j = 0; ok && j < nkb; ++j) {
-            // S_{j+1} goes to the other buffer; it was last read as P_{j-1} by PV_{j-1}, issued before
             if (j + 1 < nkb && !issue_s(j + 1)) break;
             const int st = j % FWD_NST;
             if (!tc::mbar_wait(&p_full[j & 1], (j >> 1) & 1, sm.abort)) break;
@@ -421,8 +424,9 @@ __global__ void __launch_bounds__(NT, 1)
         bool ok = tc::mbar_wait(qd_full, 0, sm.abort);
         for (int j = 0; ok && j < nkb; ++j) {
             const int st = j & 1;
-            // S_j overwrites the dS_{j-1} that dQ_{j-1} (issued before) reads
             if (!(ok = tc::mbar_wait(&k_full[st], (j >> 1) & 1, sm.abort))) break;
+            // S_j overwrites dS_{j-1}, the TMEM A operand of dQ_{j-1}: wait for it
+            if (j > 0 && !(ok = tc::mbar_wait(dq_done, (j - 1) & 1, sm.abort))) break;
             tc::fence_after();
             const uint32_t k0 = tc::smem_u32(Kt(st)), v0 = tc::smem_u32(Vt(st));
 #pragma unroll
@@ -485,11 +489,11 @@ __global__ void __launch_bounds__(NT, 1)
 // ===================================================================== dK, dV
 // smem tiles: 0 K | 1 V | 2,3 Q/dO stage 0 | 4,5 Q/dO stage 1
 // barriers: 0 kv_full, 1-2 qd_full, 3-4 qd_empty, 5 s_full, 6 p_full, 7 ds_full, 8 dk_done,
-//           9-10 stat barriers
+//           9-10 stat barriers, 11 dv_done
 // TMEM: S^T at 0 (P^T overwrites its first 64 columns, packed bf16, the A operand of
 // dV += P^T dO), dP^T at 128 (dS^T likewise, the A operand of dK += dS^T Q), dV at 256,
-// dK at 384.  Issue order per block i: dV_i, S^T_{i+1}, dK_i, dP^T_{i+1}: each product
-// that overwrites a region comes after the product that reads it.
+// dK at 384.  Issue order per block i: dV_i, dK_i, then S^T_{i+1} once dV_i has
+// completed and dP^T_{i+1} once dK_i has (they overwrite those products' A operands).
 constexpr int DKV_TILES = 6;
 
 __global__ void __launch_bounds__(NT, 1)
@@ -510,8 +514,9 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* ds_full = &sm.bar[7];
     uint64_t* dk_done = &sm.bar[8];
     uint64_t* sbar = &sm.bar[9];
-    const uint32_t counts[11] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1, NSM, NSM};
-    setup(sm, 11, counts);
+    uint64_t* dv_done = &sm.bar[11];
+    const uint32_t counts[12] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1, NSM, NSM, 1};
+    setup(sm, 12, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* K = sm.base;
     uint8_t* V = sm.base + TILE;
@@ -546,19 +551,12 @@ __global__ void __launch_bounds__(NT, 1)
         for (int i = 0; ok && i < nq; ++i) {
             const int st = i & 1, sn = (i + 1) & 1;
             const uint32_t q0 = tc::smem_u32(Qt(st)), do0 = tc::smem_u32(dOt(st));
-            const bool more = i + 1 < nq;
             if (!(ok = tc::mbar_wait(p_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc::mma_bf16_ts(tmem + 256, tmem + kk * 8, dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
-            if (more) {
-                if (!(ok = tc::mbar_wait(&qd_full[sn], ((i + 1) >> 1) & 1, sm.abort))) break;
-                tc::fence_after();
-                const uint32_t qn = tc::smem_u32(Qt(sn));
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(k0, kk), dk_(qn, kk), IDESC_KK, kk > 0);
-            }
+            tc::mma_commit(dv_done);
             if (!(ok = tc::mbar_wait(ds_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
@@ -566,8 +564,17 @@ __global__ void __launch_bounds__(NT, 1)
                 tc::mma_bf16_ts(tmem + 384, tmem + 128 + kk * 8, dm_(q0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dk_done);
             tc::mma_commit(&qd_empty[st]);
-            if (more) {
-                const uint32_t don = tc::smem_u32(dOt(sn));
+            if (i + 1 < nq) {
+                // S^T_{i+1} / dP^T_{i+1} overwrite P^T_i / dS^T_i, the TMEM A operands of
+                // dV_i / dK_i: wait for each to complete (the other keeps the pipe busy)
+                if (!(ok = tc::mbar_wait(&qd_full[sn], ((i + 1) >> 1) & 1, sm.abort))) break;
+                if (!(ok = tc::mbar_wait(dv_done, i & 1, sm.abort))) break;
+                tc::fence_after();
+                const uint32_t qn = tc::smem_u32(Qt(sn)), don = tc::smem_u32(dOt(sn));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(k0, kk), dk_(qn, kk), IDESC_KK, kk > 0);
+                if (!(ok = tc::mbar_wait(dk_done, i & 1, sm.abort))) break;
+                tc::fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc::mma_bf16(tmem + 128, dk_(v0, kk), dk_(don, kk), IDESC_KK, kk > 0);
