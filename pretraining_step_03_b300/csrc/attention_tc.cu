@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(NT, 1)
 // smem tiles: 0 Q | 1 dO | 2,3 K stages | 4,5 V stages
 // barriers: 0 qd_full, 1-2 k_full, 3-4 k_empty, 5-6 v_full, 7-8 v_empty, 9 s_full, 10 ds_full,
 //           11 dq_done
-// TMEM: S at 0 (dS overwrites its first 64 columns as packed bf16, the A operand of
-// dQ += dS K), dP at 128, dQ at 256.
+// TMEM: S at 0, dP at 128, dQ at 256, dS at 384 (packed bf16, the A operand of
+// dQ += dS K).
 constexpr int DQ_TILES = 6;
 
 __global__ void __launch_bounds__(NT, 1)
@@ -425,8 +425,6 @@ __global__ void __launch_bounds__(NT, 1)
         for (int j = 0; ok && j < nkb; ++j) {
             const int st = j & 1;
             if (!(ok = tc::mbar_wait(&k_full[st], (j >> 1) & 1, sm.abort))) break;
-            // S_j overwrites dS_{j-1}, the TMEM A operand of dQ_{j-1}: wait for it
-            if (j > 0 && !(ok = tc::mbar_wait(dq_done, (j - 1) & 1, sm.abort))) break;
             tc::fence_after();
             const uint32_t k0 = tc::smem_u32(Kt(st)), v0 = tc::smem_u32(Vt(st));
 #pragma unroll
@@ -441,7 +439,7 @@ __global__ void __launch_bounds__(NT, 1)
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16_ts(tmem + 256, tmem + kk * 8, dm_(k0, kk), IDESC_KM, (j > 0 || kk > 0));
+                tc::mma_bf16_ts(tmem + 256, tmem + 384 + kk * 8, dm_(k0, kk), IDESC_KM, (j > 0 || kk > 0));
             tc::mma_commit(dq_done);
             tc::mma_commit(&k_empty[st]);
         }
@@ -469,7 +467,10 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int i = 0; i < 32; ++i)
                     w[i] = pack2(s[2 * i] * (d[2 * i] - Dt), s[2 * i + 1] * (d[2 * i + 1] - Dt));
             }
-            st_half_bf16(tmem + lanes, g, w);
+            // dS_{j-1} here was read by dQ_{j-1}; S_j was issued after ds_full_{j-1}
+            // and dQ_{j-1} follows it, so wait for dQ_{j-1} before overwriting
+            if (j > 0 && !(ok = tc::mbar_wait_warp(dq_done, (j - 1) & 1, sm.abort))) break;
+            st_half_bf16(tmem + lanes + 384, g, w);
             tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(ds_full);
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(NT, 1)
 // ===================================================================== dK, dV
 // smem tiles: 0 K | 1 V | 2,3 Q/dO stage 0 | 4,5 Q/dO stage 1
 // barriers: 0 kv_full, 1-2 qd_full, 3-4 qd_empty, 5 s_full, 6 p_full, 7 ds_full, 8 dk_done,
-//           9-10 stat barriers, 11 dv_done
+//           9-10 stat barriers, 11 dv_done, 12-13 read barriers
 // TMEM: S^T at 0 (P^T overwrites its first 64 columns, packed bf16, the A operand of
 // dV += P^T dO), dP^T at 128 (dS^T likewise, the A operand of dK += dS^T Q), dV at 256,
 // dK at 384.  Issue order per block i: dV_i, dK_i, then S^T_{i+1} once dV_i has
@@ -515,8 +516,9 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* dk_done = &sm.bar[8];
     uint64_t* sbar = &sm.bar[9];
     uint64_t* dv_done = &sm.bar[11];
-    const uint32_t counts[12] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1, NSM, NSM, 1};
-    setup(sm, 12, counts);
+    uint64_t* rbar = &sm.bar[12];
+    const uint32_t counts[14] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1, NSM, NSM, 1, NSM, NSM};
+    setup(sm, 14, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* K = sm.base;
     uint8_t* V = sm.base + TILE;
@@ -607,22 +609,32 @@ __global__ void __launch_bounds__(NT, 1)
                 const int c = col_of(g, e);
                 s[e] = (i == 0 && r > c) ? 0.f : exp2f(s[e] * c2 - stat[c]);
             }
-            uint32_t w[32];
+            uint32_t wp[32], wd[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) w[e] = pack2(s[2 * e], s[2 * e + 1]);
-            st_half_bf16(tmem + lanes, g, w);
+            for (int e = 0; e < 32; ++e) wp[e] = pack2(s[2 * e], s[2 * e + 1]);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {   // dS^T = P^T (dP^T - D[c]), one 32-column chunk at a time
+                uint32_t d[32];
+                tc::tmem_ld32(tmem + lanes + 128 + (g + 2 * h2) * 32, d);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int i0 = 32 * h2 + 2 * e;
+                    wd[16 * h2 + e] = pack2(s[i0] * (__uint_as_float(d[2 * e]) - stat[128 + col_of(g, i0)]),
+                                            s[i0 + 1] * (__uint_as_float(d[2 * e + 1]) - stat[128 + col_of(g, i0 + 1)]));
+                }
+            }
+            // the packed operands land in columns the other group reads: both groups
+            // finish reading S^T and dP^T first
+            tc::fence_before();
+            tc::mbar_arrive(&rbar[i & 1]);
+            if (!(ok = tc::mbar_wait_warp(&rbar[i & 1], (i >> 1) & 1, sm.abort))) break;
+            tc::fence_after();
+            st_half_bf16(tmem + lanes, g, wp);
             tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(p_full);
-            {   // dS^T = P^T (dP^T - D[c])
-                float d[64];
-                ld_half(tmem + lanes + 128, g, d);
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    w[e] = pack2(s[2 * e] * (d[2 * e] - stat[128 + col_of(g, 2 * e)]),
-                                 s[2 * e + 1] * (d[2 * e + 1] - stat[128 + col_of(g, 2 * e + 1)]));
-            }
-            st_half_bf16(tmem + lanes + 128, g, w);
+            st_half_bf16(tmem + lanes + 128, g, wd);
             tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(ds_full);
