@@ -304,12 +304,15 @@ __global__ void __launch_bounds__(NT, 1)
             tc::fence_after();
             const uint32_t sb = tmem + lanes + (j & 1) * 128;
             ld_half(sb, g, s);
-            float mx = -INFINITY;
+            if (j == qb) {   // diagonal block: keys after the query are masked
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                s[i] = (j == qb && col_of(g, i) > r) ? -INFINITY : s[i] * c2;
-                mx = fmaxf(mx, s[i]);
+                for (int i = 0; i < 64; ++i)
+                    if (col_of(g, i) > r) s[i] = -INFINITY;
             }
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], s[i]);
+            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;   // in log2 units
             float mo;
             if (!(ok = exchange(sm, xbar, j, g, r, mx, &mo))) break;
             mx = fmaxf(mx, mo);
@@ -340,14 +343,14 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             uint32_t w[32];
-            float sum = 0.f;
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float a = exp2f(s[2 * i] - m2), bb = exp2f(s[2 * i + 1] - m2);
-                sum += a + bb;
+                const float a = exp2f(fmaf(s[2 * i], c2, -m2)), bb = exp2f(fmaf(s[2 * i + 1], c2, -m2));
+                sum4[i & 3] += a + bb;
                 w[i] = pack2(a, bb);
             }
-            l += sum;
+            l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             st_half_bf16(sb, g, w);
             tc::tmem_wait_st();
             tc::fence_before();
@@ -458,7 +461,12 @@ __global__ void __launch_bounds__(NT, 1)
             tc::fence_after();
             ld_half(tmem + lanes, g, s);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) s[i] = (j == qb && col_of(g, i) > r) ? 0.f : exp2f(s[i] * c2 - lse2);
+            for (int i = 0; i < 64; ++i) s[i] = exp2f(fmaf(s[i], c2, -lse2));
+            if (j == qb) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (col_of(g, i) > r) s[i] = 0.f;
+            }
             uint32_t w[32];
             {
                 float d[64];
@@ -603,11 +611,25 @@ __global__ void __launch_bounds__(NT, 1)
             if (!(ok = tc::mbar_wait_warp(s_full, i & 1, sm.abort))) break;
             tc::fence_after();
             ld_half(tmem + lanes, g, s);
-            // P^T[r][c] = exp2(S^T*c2 - lse2[c]), zero where key r > query c
+            // P^T[r][c] = exp2(S^T*c2 - lse2[c]), zero where key r > query c; this
+            // thread's columns are two contiguous runs of 32 (statistics as float4)
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                const int c = col_of(g, e);
-                s[e] = (i == 0 && r > c) ? 0.f : exp2f(s[e] * c2 - stat[c]);
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const float4* l4 = reinterpret_cast<const float4*>(stat + 64 * h2 + 32 * g);
+#pragma unroll
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 lv = l4[k4];
+                    float* x = s + 32 * h2 + 4 * k4;
+                    x[0] = exp2f(fmaf(x[0], c2, -lv.x));
+                    x[1] = exp2f(fmaf(x[1], c2, -lv.y));
+                    x[2] = exp2f(fmaf(x[2], c2, -lv.z));
+                    x[3] = exp2f(fmaf(x[3], c2, -lv.w));
+                }
+            }
+            if (i == 0) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e)
+                    if (r > col_of(g, e)) s[e] = 0.f;
             }
             uint32_t wp[32], wd[32];
 #pragma unroll
@@ -617,11 +639,15 @@ __global__ void __launch_bounds__(NT, 1)
                 uint32_t d[32];
                 tc::tmem_ld32(tmem + lanes + 128 + (g + 2 * h2) * 32, d);
                 tc::tmem_wait_ld();
+                const float4* d4 = reinterpret_cast<const float4*>(stat + 128 + 64 * h2 + 32 * g);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int i0 = 32 * h2 + 2 * e;
-                    wd[16 * h2 + e] = pack2(s[i0] * (__uint_as_float(d[2 * e]) - stat[128 + col_of(g, i0)]),
-                                            s[i0 + 1] * (__uint_as_float(d[2 * e + 1]) - stat[128 + col_of(g, i0 + 1)]));
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 dv4 = d4[k4];
+                    const float* x = s + 32 * h2 + 4 * k4;
+                    wd[16 * h2 + 2 * k4] = pack2(x[0] * (__uint_as_float(d[4 * k4]) - dv4.x),
+                                                 x[1] * (__uint_as_float(d[4 * k4 + 1]) - dv4.y));
+                    wd[16 * h2 + 2 * k4 + 1] = pack2(x[2] * (__uint_as_float(d[4 * k4 + 2]) - dv4.z),
+                                                     x[3] * (__uint_as_float(d[4 * k4 + 3]) - dv4.w));
                 }
             }
             // the packed operands land in columns the other group reads: both groups
