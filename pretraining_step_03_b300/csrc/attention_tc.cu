@@ -424,22 +424,31 @@ __global__ void __launch_bounds__(NT, 1)
         }
     } else if (warp == 1 && lane == 0) {
         const uint32_t q0 = tc::smem_u32(Q), do0 = tc::smem_u32(dO);
-        bool ok = tc::mbar_wait(qd_full, 0, sm.abort);
-        for (int j = 0; ok && j < nkb; ++j) {
+        // S and dP of block j (TMEM 0, 128) are read only by the softmax, so the next
+        // block's S and dP go in as soon as the softmax is done with them (ds_full),
+        // ahead of dQ_j: the softmax of block j+1 overlaps dQ_j
+        auto issue_sdp = [&](int j) -> bool {
             const int st = j & 1;
-            if (!(ok = tc::mbar_wait(&k_full[st], (j >> 1) & 1, sm.abort))) break;
+            if (!tc::mbar_wait(&k_full[st], (j >> 1) & 1, sm.abort)) return false;
             tc::fence_after();
             const uint32_t k0 = tc::smem_u32(Kt(st)), v0 = tc::smem_u32(Vt(st));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(q0, kk), dk_(k0, kk), IDESC_KK, kk > 0);
-            if (!(ok = tc::mbar_wait(&v_full[st], (j >> 1) & 1, sm.abort))) break;
+            if (!tc::mbar_wait(&v_full[st], (j >> 1) & 1, sm.abort)) return false;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128, dk_(do0, kk), dk_(v0, kk), IDESC_KK, kk > 0);
             tc::mma_commit(s_full);
             tc::mma_commit(&v_empty[st]);
+            return true;
+        };
+        bool ok = tc::mbar_wait(qd_full, 0, sm.abort) && issue_sdp(0);
+        for (int j = 0; ok && j < nkb; ++j) {
+            const int st = j & 1;
             if (!(ok = tc::mbar_wait(ds_full, j & 1, sm.abort))) break;
+            if (j + 1 < nkb && !(ok = issue_sdp(j + 1))) break;
             tc::fence_after();
+            const uint32_t k0 = tc::smem_u32(Kt(st));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc::mma_bf16_ts(tmem + 256, tmem + 384 + kk * 8, dm_(k0, kk), IDESC_KM, (j > 0 || kk > 0));
@@ -497,12 +506,13 @@ __global__ void __launch_bounds__(NT, 1)
 
 // ===================================================================== dK, dV
 // smem tiles: 0 K | 1 V | 2,3 Q/dO stage 0 | 4,5 Q/dO stage 1
-// barriers: 0 kv_full, 1-2 qd_full, 3-4 qd_empty, 5 s_full, 6 p_full, 7 ds_full, 8 dk_done,
-//           9-10 stat barriers, 11 dv_done, 12-13 read barriers
-// TMEM: S^T at 0 (P^T overwrites its first 64 columns, packed bf16, the A operand of
-// dV += P^T dO), dP^T at 128 (dS^T likewise, the A operand of dK += dS^T Q), dV at 256,
-// dK at 384.  Issue order per block i: dV_i, dK_i, then S^T_{i+1} once dV_i has
-// completed and dP^T_{i+1} once dK_i has (they overwrite those products' A operands).
+// barriers: 0 kv_full, 1-2 qd_full, 3-4 qd_empty, 5 s_full, 6 dp_full, 7 s_free, 8 p_full,
+//           9 ds_full, 10 dv_done, 11 dk_done, 12-13 stat barriers, 14-15 read barriers
+// TMEM: S^T at 0, dP^T at 128, dV at 256, dK at 384.  The packed bf16 operands go into
+// the dP^T region once it has been read: dS^T at 128 (A of dK += dS^T Q), P^T at 192
+// (A of dV += P^T dO).  So S^T of the next block can run as soon as the softmax has
+// read S^T of this one, overlapping this block's dV and dK; dP^T of the next block
+// waits for dV and dK, whose A operands it overwrites.
 constexpr int DKV_TILES = 6;
 
 __global__ void __launch_bounds__(NT, 1)
@@ -519,14 +529,16 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* qd_full = &sm.bar[1];
     uint64_t* qd_empty = &sm.bar[3];
     uint64_t* s_full = &sm.bar[5];
-    uint64_t* p_full = &sm.bar[6];
-    uint64_t* ds_full = &sm.bar[7];
-    uint64_t* dk_done = &sm.bar[8];
-    uint64_t* sbar = &sm.bar[9];
-    uint64_t* dv_done = &sm.bar[11];
-    uint64_t* rbar = &sm.bar[12];
-    const uint32_t counts[14] = {1, 1, 1, 1, 1, 1, NSM, NSM, 1, NSM, NSM, 1, NSM, NSM};
-    setup(sm, 14, counts);
+    uint64_t* dp_full = &sm.bar[6];
+    uint64_t* s_free = &sm.bar[7];
+    uint64_t* p_full = &sm.bar[8];
+    uint64_t* ds_full = &sm.bar[9];
+    uint64_t* dv_done = &sm.bar[10];
+    uint64_t* dk_done = &sm.bar[11];
+    uint64_t* sbar = &sm.bar[12];
+    uint64_t* rbar = &sm.bar[14];
+    const uint32_t counts[16] = {1, 1, 1, 1, 1, 1, 1, NSM, NSM, NSM, 1, 1, NSM, NSM, NSM, NSM};
+    setup(sm, 16, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* K = sm.base;
     uint8_t* V = sm.base + TILE;
@@ -548,24 +560,39 @@ __global__ void __launch_bounds__(NT, 1)
         }
     } else if (warp == 1 && lane == 0) {
         const uint32_t k0 = tc::smem_u32(K), v0 = tc::smem_u32(V);
+        auto issue_st = [&](int i) {   // S^T_i = K Q_i^T
+            const uint32_t qn = tc::smem_u32(Qt(i & 1));
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(k0, kk), dk_(qn, kk), IDESC_KK, kk > 0);
+            tc::mma_commit(s_full);
+        };
+        auto issue_dpt = [&](int i) {  // dP^T_i = V dO_i^T
+            const uint32_t don = tc::smem_u32(dOt(i & 1));
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128, dk_(v0, kk), dk_(don, kk), IDESC_KK, kk > 0);
+            tc::mma_commit(dp_full);
+        };
         bool ok = tc::mbar_wait(kv_full, 0, sm.abort) && tc::mbar_wait(&qd_full[0], 0, sm.abort);
         if (ok) {
             tc::fence_after();
-            const uint32_t q0 = tc::smem_u32(Qt(0)), do0 = tc::smem_u32(dOt(0));
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(k0, kk), dk_(q0, kk), IDESC_KK, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128, dk_(v0, kk), dk_(do0, kk), IDESC_KK, kk > 0);
-            tc::mma_commit(s_full);
+            issue_st(0);
+            issue_dpt(0);
         }
         for (int i = 0; ok && i < nq; ++i) {
-            const int st = i & 1, sn = (i + 1) & 1;
+            const int st = i & 1;
+            const bool more = i + 1 < nq;
             const uint32_t q0 = tc::smem_u32(Qt(st)), do0 = tc::smem_u32(dOt(st));
+            if (!(ok = tc::mbar_wait(s_free, i & 1, sm.abort))) break;
+            if (more) {
+                if (!(ok = tc::mbar_wait(&qd_full[(i + 1) & 1], ((i + 1) >> 1) & 1, sm.abort))) break;
+                tc::fence_after();
+                issue_st(i + 1);
+            }
             if (!(ok = tc::mbar_wait(p_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16_ts(tmem + 256, tmem + kk * 8, dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
+                tc::mma_bf16_ts(tmem + 256, tmem + 192 + kk * 8, dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dv_done);
             if (!(ok = tc::mbar_wait(ds_full, i & 1, sm.abort))) break;
             tc::fence_after();
@@ -574,21 +601,11 @@ __global__ void __launch_bounds__(NT, 1)
                 tc::mma_bf16_ts(tmem + 384, tmem + 128 + kk * 8, dm_(q0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dk_done);
             tc::mma_commit(&qd_empty[st]);
-            if (i + 1 < nq) {
-                // S^T_{i+1} / dP^T_{i+1} overwrite P^T_i / dS^T_i, the TMEM A operands of
-                // dV_i / dK_i: wait for each to complete (the other keeps the pipe busy)
-                if (!(ok = tc::mbar_wait(&qd_full[sn], ((i + 1) >> 1) & 1, sm.abort))) break;
+            if (more) {
                 if (!(ok = tc::mbar_wait(dv_done, i & 1, sm.abort))) break;
-                tc::fence_after();
-                const uint32_t qn = tc::smem_u32(Qt(sn)), don = tc::smem_u32(dOt(sn));
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(k0, kk), dk_(qn, kk), IDESC_KK, kk > 0);
                 if (!(ok = tc::mbar_wait(dk_done, i & 1, sm.abort))) break;
                 tc::fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_bf16(tmem + 128, dk_(v0, kk), dk_(don, kk), IDESC_KK, kk > 0);
-                tc::mma_commit(s_full);
+                issue_dpt(i + 1);
             }
         }
     } else if (warp >= 2) {
@@ -611,6 +628,8 @@ __global__ void __launch_bounds__(NT, 1)
             if (!(ok = tc::mbar_wait_warp(s_full, i & 1, sm.abort))) break;
             tc::fence_after();
             ld_half(tmem + lanes, g, s);
+            tc::fence_before();
+            tc::mbar_arrive(s_free);
             // P^T[r][c] = exp2(S^T*c2 - lse2[c]), zero where key r > query c; this
             // thread's columns are two contiguous runs of 32 (statistics as float4)
 #pragma unroll
@@ -634,6 +653,8 @@ __global__ void __launch_bounds__(NT, 1)
             uint32_t wp[32], wd[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) wp[e] = pack2(s[2 * e], s[2 * e + 1]);
+            if (!(ok = tc::mbar_wait_warp(dp_full, i & 1, sm.abort))) break;
+            tc::fence_after();
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {   // dS^T = P^T (dP^T - D[c]), one 32-column chunk at a time
                 uint32_t d[32];
@@ -650,13 +671,13 @@ __global__ void __launch_bounds__(NT, 1)
                                                      x[3] * (__uint_as_float(d[4 * k4 + 3]) - dv4.w));
                 }
             }
-            // the packed operands land in columns the other group reads: both groups
-            // finish reading S^T and dP^T first
+            // the packed operands land in dP^T columns the other group reads: both
+            // groups finish reading dP^T first
             tc::fence_before();
             tc::mbar_arrive(&rbar[i & 1]);
             if (!(ok = tc::mbar_wait_warp(&rbar[i & 1], (i >> 1) & 1, sm.abort))) break;
             tc::fence_after();
-            st_half_bf16(tmem + lanes, g, wp);
+            st_half_bf16(tmem + lanes + 192, g, wp);
             tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(p_full);
@@ -665,7 +686,8 @@ __global__ void __launch_bounds__(NT, 1)
             tc::fence_before();
             tc::mbar_arrive(ds_full);
         }
-        if (ok && tc::mbar_wait_warp(dk_done, (nq - 1) & 1, sm.abort)) {
+        if (ok && tc::mbar_wait_warp(dk_done, (nq - 1) & 1, sm.abort) &&
+            tc::mbar_wait_warp(dv_done, (nq - 1) & 1, sm.abort)) {
             tc::fence_after();
             const int key = kb * BR + r;
             ld_half(tmem + lanes + 256, g, s);
