@@ -190,6 +190,25 @@ NC_API int nc_attention_backward(const void* q, const void* k, const void* v, in
                           int B, int T, int H, int D, int dtype, void* stream);
 
 /*
+ * The attention backward above, for callers that cannot allocate device
+ * memory (no counterpart on the pages: it only changes where the scratch
+ * lives).  Same arguments and results as nc_attention_backward minus the
+ * workspace: the B*H*T row statistics go to a fixed array compiled into the
+ * library, which every GPU that loads it holds until the process exits.
+ * B*H*T must not exceed NC_ATTN_NOALLOC_MAX_ROWS (NC_ERR_ARG otherwise).
+ * Allocates nothing.  The first call on a device looks up the array's device
+ * address (with that device current), so make it before any stream capture.
+ * All calls share the array: calls that overlap on the GPU (different
+ * streams) race; calls on one stream are safe.  Nothing needs clearing: each
+ * call overwrites every element it reads.
+ */
+#define NC_ATTN_NOALLOC_MAX_ROWS (1L << 20)
+NC_API int nc_attention_backward_noalloc(const void* q, const void* k, const void* v, int ld_qkv,
+                                         const void* o, const void* dout, int ld_o, const float* lse,
+                                         void* dq, void* dk, void* dv, int ld_dqkv, int B, int T, int H,
+                                         int D, int dtype, void* stream);
+
+/*
  * Dense GEMM on the tensor cores (bf16 in, fp32 accumulate):
  * C[b] = alpha * op(A[b]) op(B[b])^T + beta * C_in[b] for b < batch, where
  * op(A) is [M, K] and op(B) is [N, K].  trans_a = 0: A row-major [M, K] with

@@ -55,6 +55,8 @@ SIGNATURES = {
     "nc_attention_workspace_bytes": (_SZ, [_I, _I, _I]),
     "nc_attention_backward": (_I, [_V, _V, _V, _I, _V, _V, _I, _V, _V, _V, _V, _I, _V, _I, _I, _I,
                                    _I, _I, _V]),
+    "nc_attention_backward_noalloc": (_I, [_V, _V, _V, _I, _V, _V, _I, _V, _V, _V, _V, _I, _I, _I, _I,
+                                           _I, _I, _V]),
     "nc_profile": (_I, [_V, _I]),
     "nc_profile_read": (_I, [_V, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_L),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]),
@@ -197,6 +199,12 @@ def nc_attention_backward(q, k, v, ld_qkv, o, dout, ld_o, lse, dq, dk, dv, ld_dq
                           D, dtype, stream):
     _check(lib().nc_attention_backward(q, k, v, ld_qkv, o, dout, ld_o, lse, dq, dk, dv, ld_dqkv,
                                        workspace, B, T, H, D, dtype, stream))
+
+
+def nc_attention_backward_noalloc(q, k, v, ld_qkv, o, dout, ld_o, lse, dq, dk, dv, ld_dqkv, B, T, H, D,
+                                  dtype, stream):
+    _check(lib().nc_attention_backward_noalloc(q, k, v, ld_qkv, o, dout, ld_o, lse, dq, dk, dv, ld_dqkv,
+                                               B, T, H, D, dtype, stream))
 
 
 def nc_gemm_bf16(M, N, K, batch, A, lda, stride_a, trans_a, B, ldb, stride_b, trans_b, C, ldc, stride_c,
