@@ -36,12 +36,13 @@ int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ld
 template <typename T>
 int attention_backward(const T* q, const T* k, const T* v, long ld, const T* o, const T* dout,
                        long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
-                       int B, int T_, int H, int D, cudaStream_t s, const float2* rope, int* rope_done) {
+                       int B, int T_, int H, int D, cudaStream_t s, const float2* rope, int* rope_done,
+                       bool delta_ready) {
     if (rope_done) *rope_done = 0;
     if (B <= 0 || T_ <= 0) return NC_OK;
     if constexpr (sizeof(T) == 2) {
         if (attention_tc_supported(ld, ldo, ldd, q, k, v, D)) {
-            NC_TRY(attention_delta_simt_bf16(o, dout, ldo, delta, B, T_, H, D, s));
+            if (!delta_ready) NC_TRY(attention_delta_simt_bf16(o, dout, ldo, delta, B, T_, H, D, s));
             if (rope_done) *rope_done = rope != nullptr;
             return attention_backward_tc(q, k, v, ld, dout, ldo, lse, delta, dq, dk, dv, ldd, B, T_, H,
                                          rope, s);
@@ -58,9 +59,10 @@ template int attention_forward<bf16>(const bf16*, const bf16*, const bf16*, long
 template int attention_backward<float>(const float*, const float*, const float*, long, const float*,
                                        const float*, long, const float*, float*, float*, float*,
                                        long, float*, int, int, int, int, cudaStream_t, const float2*,
-                                       int*);
+                                       int*, bool);
 template int attention_backward<bf16>(const bf16*, const bf16*, const bf16*, long, const bf16*,
                                       const bf16*, long, const float*, bf16*, bf16*, bf16*, long,
-                                      float*, int, int, int, int, cudaStream_t, const float2*, int*);
+                                      float*, int, int, int, int, cudaStream_t, const float2*, int*,
+                                      bool);
 
 }  // namespace nc

@@ -341,7 +341,14 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         NC_TRY(norm_b(Ly.y2, Ly.r2, m->g));
         // attention block
         NC_TRY(weight_grad(m, G + m->poff[b0 + 3], d, d, gop, d, Ly.o, d, M, accumulate));
-        NC_TRY(run_gemm(m, mk(m, M, d, d, gop, d, false, W<T>(m, b0 + 3), d, true, m->dO, d, act)));
+        {   // dO = g Wo; with head dim 128 the epilogue also leaves D_t = dO_t . O_t per head
+            Gemm g = mk(m, M, d, d, gop, d, false, W<T>(m, b0 + 3), d, true, m->dO, d, act);
+            if (fuse_rope) {
+                g.epi = EPI_DELTA; g.aux = Ly.o; g.ldaux = d; g.aux_dtype = act; g.delta = m->delta;
+                g.rope_T = T_;
+            }
+            NC_TRY(run_gemm(m, g));
+        }
         T* q = (T*)Ly.qkv;
         T* dq = (T*)m->dqkv;
         int unroped = 0;
@@ -349,7 +356,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
             Prof pr(m, NC_PROF_ATTN_BWD, 2.5 * attn_fl, 0);
             NC_TRY(attention_backward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, (T*)m->dO, d, Ly.lse, dq,
                                          dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s, m->rope,
-                                         &unroped));
+                                         &unroped, fuse_rope));
         }
         if (!unroped) NC_TRY(rope(m->dqkv, -1.f));
         NC_TRY(weight_grad(m, G + m->poff[b0], 3 * d, d, m->dqkv, 3 * d, Ly.y1, d, M, accumulate));

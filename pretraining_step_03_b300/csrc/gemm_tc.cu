@@ -45,6 +45,7 @@ struct TcParams {
     uint32_t* flag;   // device flag word for timeouts (may be null)
     const float2* rope;
     int rope_T, rope_cols;
+    float* delta;
 };
 
 template <int BN> struct Cfg {
@@ -236,6 +237,33 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
                 const long ci = (long)b * p.sC + (long)row * p.ldc + na;
                 st32(p.C, ci, p.c_dtype, va);
                 st32(p.C, ci + 64, p.c_dtype, vb);
+            }
+        }
+    } else if (p.epi == EPI_DELTA) {
+        // dO (bf16) out; per 128-column head the dot product with O (aux) of the
+        // rounded values, i.e. exactly what the attention backward will consume
+        float dot = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tc::tmem_ld32(tbase + c * 32, r);
+            tc::tmem_wait_ld();
+            const int n0 = tn * BN + c * 32;
+            if (row < p.M && n0 < p.N) {
+                float v[32], o[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[j]) * p.alpha));
+                const long ci = (long)b * p.sC + (long)row * p.ldc + n0;
+                st32(p.C, ci, NC_BF16, v);
+                ld32(p.aux, (long)b * p.sAux + (long)row * p.ldaux + n0, NC_BF16, o);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) dot = fmaf(v[j], o[j], dot);
+                if ((c & 3) == 3) {
+                    const int hh = n0 / 128, t = row % p.rope_T, bb = row / p.rope_T;
+                    p.delta[((long)bb * (p.N / 128) + hh) * p.rope_T + t] = dot;
+                    dot = 0.f;
+                }
             }
         }
     } else
@@ -695,6 +723,9 @@ bool gemm_tc_supported(const Gemm& g) {
     if (g.aux && (uintptr_t)g.aux % 16) return false;
     if (g.N % 8) return false;
     if (g.epi == EPI_ROPE && (g.N % 128 || !g.rope || g.rope_T <= 0 || g.c_dtype != NC_BF16)) return false;
+    if (g.epi == EPI_DELTA && (g.N % 128 || !g.delta || !g.aux || g.rope_T <= 0 || g.c_dtype != NC_BF16 ||
+                               g.aux_dtype != NC_BF16 || g.batch != 1))
+        return false;
     return true;
 }
 
@@ -728,7 +759,7 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     p.C2 = g.C2; p.alpha = g.alpha; p.beta = g.beta; p.epi = g.epi;
     p.ws = p.splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
     p.flag = g_gemm_flag;
-    p.rope = g.rope; p.rope_T = g.rope_T; p.rope_cols = g.rope_cols;
+    p.rope = g.rope; p.rope_T = g.rope_T; p.rope_cols = g.rope_cols; p.delta = g.delta;
 
     CUtensorMap ma, mb;
     if (!g.a_t) NC_TRY(make_map(&ma, g.A, g.K, g.M, g.batch, g.lda, g.sA, 64, BM));

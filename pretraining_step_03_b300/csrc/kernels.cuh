@@ -15,6 +15,7 @@ enum EpiKind {
     EPI_RELU2 = 1,      // C = alpha*acc (pre-activation h), C2 = relu(h)^2
     EPI_RELU2_BWD = 2,  // C = alpha*acc * 2*relu(aux)          (aux = h)
     EPI_ROPE = 3,       // C = alpha*acc with columns < rope_cols rotated by RoPE (head dim 128)
+    EPI_DELTA = 4,      // C = alpha*acc (bf16) and delta[b, h, t] = sum over head h of bf16(C) * aux
 };
 
 struct Gemm {
@@ -29,6 +30,7 @@ struct Gemm {
     int epi = EPI_STORE;
     const float2* rope = nullptr;  // EPI_ROPE: [rope_T, 64] (cos, sin); row position = row % rope_T
     int rope_T = 0, rope_cols = 0;
+    float* delta = nullptr;        // EPI_DELTA: [B, N/128, rope_T] row statistics (row = b*rope_T + t)
 };
 
 int gemm_simt(const Gemm& g, cudaStream_t s);
@@ -80,11 +82,12 @@ int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ld
                       int B, int T_, int H, int D, cudaStream_t s);
 // rope: optional RoPE table; when the kernel can rotate dq, dk back itself it
 // does so and sets *rope_done = 1 (else the caller applies the inverse RoPE).
+// delta_ready: delta already holds dO.O per row (computed by the producer of dO)
 template <typename T>
 int attention_backward(const T* q, const T* k, const T* v, long ld, const T* o, const T* dout,
                        long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
                        int B, int T_, int H, int D, cudaStream_t s, const float2* rope = nullptr,
-                       int* rope_done = nullptr);
+                       int* rope_done = nullptr, bool delta_ready = false);
 
 // ------------------------------------------------------------ optimizers
 // Muon, phase 1: buf = mu*buf + g; g <- g + mu*buf (nesterov) or buf; per-CTA

@@ -175,70 +175,96 @@ __global__ void __launch_bounds__(CE_THREADS) ce_kernel(T* z, const int32_t* tgt
     }
 }
 
-// Same computation for bf16 logits with V a multiple of 8 * 512: the row is
-// read from HBM once (16-byte loads) into this thread's own slice of shared
-// memory, the three passes run from there, and the result is written once.
+// Same computation for bf16 logits with V a multiple of 8 * 256, in two passes
+// over the row with an online max / sum-exp: the first pass reads the row from
+// HBM, the second re-reads it (from L2: a row is 2V bytes and only the rows in
+// flight need to stay resident) and writes the gradient in place.  No shared
+// row buffer, so several rows per SM overlap their loads.
 constexpr float CE_LOG2E = 1.4426950408889634f;
+constexpr int CE2_THREADS = 256;
 
-__global__ void __launch_bounds__(CE_THREADS) ce_rows_kernel(bf16* z, const int32_t* tgt, float* nll,
-                                                             int V, float scale, uint32_t* flag) {
-    extern __shared__ uint4 row_s[];
-    __shared__ float sh[32];
-    __shared__ float zt_s;
+__device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2) {
+    const float mm = fmaxf(m, m2);
+    s = (m == -INFINITY ? 0.f : s * exp2f((m - mm) * CE_LOG2E)) +
+        (m2 == -INFINITY ? 0.f : s2 * exp2f((m2 - mm) * CE_LOG2E));
+    m = mm;
+}
+
+__global__ void __launch_bounds__(CE2_THREADS) ce_online_kernel(bf16* z, const int32_t* tgt, float* nll,
+                                                                int V, float scale, uint32_t* flag) {
+    __shared__ float shm[32], shs[32];
+    __shared__ float zt_s, lse_s;
     const long row = blockIdx.x;
     uint4* zr = reinterpret_cast<uint4*>(z + row * V);
-    const int nv = V / (8 * CE_THREADS);
+    const int nv = V / (8 * CE2_THREADS);
     const int t = tgt[row];
     const bool ok = t >= 0 && t < V;
     if (threadIdx.x == 0) {
         if (!ok) flag_set(flag, NC_FLAG_TOKEN_RANGE);
         zt_s = ok ? __bfloat162float(z[row * V + t]) : 0.f;
     }
-    float mx = -INFINITY;
-#pragma unroll 16
-    for (int k = 0; k < nv; ++k) {
-        const uint4 u = zr[threadIdx.x + k * CE_THREADS];
-        row_s[threadIdx.x + k * CE_THREADS] = u;
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-            mx = fmaxf(mx, fmaxf(f.x, f.y));
-        }
-    }
-    mx = block_reduce(mx, sh, true);
-    const float mxl = mx * CE_LOG2E;
-    float se = 0.f;
+    float m = -INFINITY, se = 0.f;
 #pragma unroll 4
     for (int k = 0; k < nv; ++k) {
-        const uint4 u = row_s[threadIdx.x + k * CE_THREADS];
+        const uint4 u = zr[threadIdx.x + k * CE2_THREADS];
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float f[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-            se += exp2f(f.x * CE_LOG2E - mxl) + exp2f(f.y * CE_LOG2E - mxl);
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            f[2 * e] = x.x;
+            f[2 * e + 1] = x.y;
+        }
+        float cm = f[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) cm = fmaxf(cm, f[e]);
+        if (cm > m) {
+            se = m == -INFINITY ? 0.f : se * exp2f((m - cm) * CE_LOG2E);
+            m = cm;
+        }
+        const float ml = m * CE_LOG2E;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) se += exp2f(fmaf(f[e], CE_LOG2E, -ml));
+    }
+    // (max, sum) across the block: warps by shuffles, then warp leaders
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, se, o);
+        ms_combine(m, se, m2, s2);
+    }
+    const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
+    if (lane == 0) { shm[wid] = m; shs[wid] = se; }
+    __syncthreads();
+    if (wid == 0) {
+        float m1 = lane < CE2_THREADS / 32 ? shm[lane] : -INFINITY;
+        float s1 = lane < CE2_THREADS / 32 ? shs[lane] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m1, o), s2 = __shfl_xor_sync(0xffffffffu, s1, o);
+            ms_combine(m1, s1, m2, s2);
+        }
+        if (lane == 0) {
+            lse_s = m1 + logf(s1);
+            nll[row] = ok ? lse_s - zt_s : 0.f;
         }
     }
-    se = block_reduce(se, sh, false);
-    const float lse = mx + logf(se);
-    const float lsel = lse * CE_LOG2E;
-    __syncthreads();  // zt_s was read before any thread overwrites z
-    if (threadIdx.x == 0) nll[row] = ok ? lse - zt_s : 0.f;
+    __syncthreads();   // zt_s was read before any thread overwrites z
+    const float lsel = lse_s * CE_LOG2E;
 #pragma unroll 4
     for (int k = 0; k < nv; ++k) {
-        const int base = (threadIdx.x + k * CE_THREADS) * 8;
-        const uint4 u = row_s[threadIdx.x + k * CE_THREADS];
+        const int base = (threadIdx.x + k * CE2_THREADS) * 8;
+        const uint4 u = zr[threadIdx.x + k * CE2_THREADS];
         uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-            float p0 = exp2f(f.x * CE_LOG2E - lsel), p1 = exp2f(f.y * CE_LOG2E - lsel);
+            float p0 = exp2f(fmaf(f.x, CE_LOG2E, -lsel)), p1 = exp2f(fmaf(f.y, CE_LOG2E, -lsel));
             if (base + 2 * e == t) p0 -= 1.f;
             if (base + 2 * e + 1 == t) p1 -= 1.f;
             __nv_bfloat162 h = __floats2bfloat162_rn(p0 * scale, p1 * scale);
             w[e] = *reinterpret_cast<uint32_t*>(&h);
         }
-        zr[threadIdx.x + k * CE_THREADS] = make_uint4(w[0], w[1], w[2], w[3]);
+        zr[threadIdx.x + k * CE2_THREADS] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -449,15 +475,8 @@ int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float
                   uint32_t* flag, cudaStream_t s) {
     if (M <= 0) return NC_OK;
     if constexpr (sizeof(T) == 2) {
-        const int smem = V * 2;
-        if (V % (8 * CE_THREADS) == 0 && smem <= 200 * 1024 && (uintptr_t)logits % 16 == 0) {
-            static int attr_set = 0;
-            if (attr_set < smem) {
-                NC_TRY(cuda_check(cudaFuncSetAttribute(ce_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       smem), "ce smem attribute"));
-                attr_set = smem;
-            }
-            ce_rows_kernel<<<M, CE_THREADS, smem, s>>>(logits, tgt, nll, V, scale, flag);
+        if (V % (8 * CE2_THREADS) == 0 && (uintptr_t)logits % 16 == 0) {
+            ce_online_kernel<<<M, CE2_THREADS, 0, s>>>(logits, tgt, nll, V, scale, flag);
             note_launch();
             NC_LAUNCH_CHECK("cross_entropy");
             return NC_OK;
