@@ -30,7 +30,8 @@
 namespace nc {
 namespace {
 
-constexpr int BM = 128, BK = 64, NTHREADS = 192, GROUP_M = 8;
+constexpr int BM = 128, BK = 64, NTHREADS = 320, GROUP_M = 8;
+constexpr int EPI_WARPS = 8;   // two groups of four, each owns half the tile columns
 
 struct TcParams {
     int M, N, K, batch;
@@ -203,14 +204,15 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
     }
 }
 
-// The epilogue of one accumulator tile for one row (this thread's TMEM lane).
+// The epilogue of one accumulator tile for one row (this thread's TMEM lane),
+// columns of group g (the first or second half of the tile).
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int split, int row, int tn,
-                                              uint32_t tbase) {
+                                              uint32_t tbase, int g) {
     if (p.epi == EPI_ROPE) {
         // chunk pairs (a, a+2) hold head-dim pairs (j, j+64) of one 128-wide head
 #pragma unroll 1
-        for (int pr = 0; pr < BN / 64; ++pr) {
+        for (int pr = g * (BN / 128); pr < (g + 1) * (BN / 128); ++pr) {
             const int a = (pr >> 1) * 4 + (pr & 1);
             uint32_t ra[32], rb[32];
             tc::tmem_ld32(tbase + a * 32, ra);
@@ -244,7 +246,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
         // rounded values, i.e. exactly what the attention backward will consume
         float dot = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = g * (BN / 64); c < (g + 1) * (BN / 64); ++c) {
             uint32_t r[32];
             tc::tmem_ld32(tbase + c * 32, r);
             tc::tmem_wait_ld();
@@ -268,7 +270,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
         }
     } else
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = g * (BN / 64); c < (g + 1) * (BN / 64); ++c) {
         uint32_t r[32];
         tc::tmem_ld32(tbase + c * 32, r);
         tc::tmem_wait_ld();
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&tfull[a], 1);
-            tc::mbar_init(&tempty[a], 128);
+            tc::mbar_init(&tempty[a], EPI_WARPS * 32);
         }
         tc::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue
-        const int q = warp & 3;
+        const int q = warp & 3, g = (warp - 2) >> 2;
         int acc = 0;
         uint32_t aph = 0;
         for (long u = blockIdx.x; u < p.units; u += gridDim.x) {
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_after();
             const int row = tm * BM + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            epilogue_tile<BN>(p, b, split, row, tn, tbase);
+            epilogue_tile<BN>(p, b, split, row, tn, tbase, g);
             tc::fence_before();
             tc::mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -474,7 +476,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&tfull[a], 1);
-            tc::mbar_init(&tempty[a], 8);   // 4 epilogue warps x 2 CTAs
+            tc::mbar_init(&tempty[a], 2 * EPI_WARPS);   // every epilogue warp of both CTAs
         }
         tc::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -563,7 +565,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue (both CTAs)
-        const int q = warp & 3;
+        const int q = warp & 3, g = (warp - 2) >> 2;
         const uint32_t tempty_leader = tc::mapa(tc::smem_u32(&tempty[0]), 0);
         int acc = 0;
         uint32_t aph = 0;
@@ -574,7 +576,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_after();
             const int row = tm * 256 + (int)rank * 128 + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_BN);
-            epilogue_tile<P_BN>(p, b, split, row, tn, tbase);
+            epilogue_tile<P_BN>(p, b, split, row, tn, tbase, g);
             tc::fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(tempty_leader + acc * 8);
@@ -653,14 +655,27 @@ int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cud
     return NC_OK;
 }
 
+// Fraction of the slots busy when `units` work items run in waves of `slots`.
+double wave_eff(long units, int slots) {
+    const long waves = (units + slots - 1) / slots;
+    return (double)units / ((double)waves * slots);
+}
+
+// Split K over CTAs when that fills the GPU's waves better (long-K, small-output
+// products such as the weight gradients); each extra split costs an fp32 partial.
 int pick_splits(const Gemm& g, int tiles, int num_kb, int slots) {
+    if (g.epi != EPI_STORE || num_kb < 16) return 1;
     const long work = (long)tiles * g.batch;
-    const int sms = slots;
-    if (work >= sms || num_kb < 8 || g.epi != EPI_STORE) return 1;
-    int s = (int)((2L * sms + work - 1) / work);
-    s = s < num_kb / 4 ? s : num_kb / 4;
-    s = s < 32 ? s : 32;
-    return s < 1 ? 1 : s;
+    double best = wave_eff(work, slots);
+    int bs = 1;
+    for (int s = 2; s <= 16 && num_kb / s >= 8; ++s) {
+        const double e = wave_eff(work * s, slots) - 0.005 * s;
+        if (e > best + 0.02) {
+            best = e;
+            bs = s;
+        }
+    }
+    return bs;
 }
 
 }  // namespace
@@ -723,7 +738,7 @@ bool gemm_tc_supported(const Gemm& g) {
     if (g.aux && (uintptr_t)g.aux % 16) return false;
     if (g.N % 8) return false;
     if (g.epi == EPI_ROPE && (g.N % 128 || !g.rope || g.rope_T <= 0 || g.c_dtype != NC_BF16)) return false;
-    if (g.epi == EPI_DELTA && (g.N % 128 || !g.delta || !g.aux || g.rope_T <= 0 || g.c_dtype != NC_BF16 ||
+    if (g.epi == EPI_DELTA && (g.N % 128 || g.N < 256 || !g.delta || !g.aux || g.rope_T <= 0 || g.c_dtype != NC_BF16 ||
                                g.aux_dtype != NC_BF16 || g.batch != 1))
         return false;
     return true;
