@@ -661,17 +661,24 @@ double wave_eff(long units, int slots) {
     return (double)units / ((double)waves * slots);
 }
 
-// Split K over CTAs when that fills the GPU's waves better (long-K, small-output
-// products such as the weight gradients); each extra split costs an fp32 partial.
+// Split K over CTAs when that fills the GPU's waves better.  Modelled time:
+// the MMA work at ~1.4 PFLOP/s divided by the wave efficiency, plus, for
+// s > 1, writing and re-reading s fp32 partials of the output at ~6 TB/s.
+// In practice this splits the long-K, small-output weight gradients only.
 int pick_splits(const Gemm& g, int tiles, int num_kb, int slots) {
     if (g.epi != EPI_STORE || num_kb < 16) return 1;
     const long work = (long)tiles * g.batch;
-    double best = wave_eff(work, slots);
+    const double flops = 2.0 * g.M * g.N * (double)g.K * g.batch;
+    const double out_bytes = (double)g.M * g.N * g.batch * 4.0;
+    auto cost = [&](int s) {
+        return flops / 1.4e15 / wave_eff(work * s, slots) + (s > 1 ? 2.0 * s * out_bytes / 6.0e12 : 0.0);
+    };
     int bs = 1;
+    double best = cost(1);
     for (int s = 2; s <= 16 && num_kb / s >= 8; ++s) {
-        const double e = wave_eff(work * s, slots) - 0.005 * s;
-        if (e > best + 0.02) {
-            best = e;
+        const double c = cost(s);
+        if (c < 0.97 * best) {
+            best = c;
             bs = s;
         }
     }
