@@ -505,15 +505,19 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 // ===================================================================== dK, dV
-// smem tiles: 0 K | 1 V | 2,3 Q/dO stage 0 | 4,5 Q/dO stage 1
-// barriers: 0 kv_full, 1-2 qd_full, 3-4 qd_empty, 5 s_full, 6 dp_full, 7 s_free, 8 p_full,
-//           9 ds_full, 10 dv_done, 11 dk_done, 12-13 stat barriers, 14-15 read barriers
+// smem tiles: 0 K | 1 V | 2..4 Q stages | 5,6 dO stages
+// barriers: 0 kv_full, 1-3 q_full, 4-6 q_empty, 7-8 do_full, 9-10 do_empty, 11 s_full,
+//           12 dp_full, 13 s_free, 14 p_full, 15 ds_full, 16 dv_done, 17 dk_done,
+//           18-19 stat barriers, 20-21 read barriers
 // TMEM: S^T at 0, dP^T at 128, dV at 256, dK at 384.  The packed bf16 operands go into
 // the dP^T region once it has been read: dS^T at 128 (A of dK += dS^T Q), P^T at 192
-// (A of dV += P^T dO).  So S^T of the next block can run as soon as the softmax has
-// read S^T of this one, overlapping this block's dV and dK; dP^T of the next block
-// waits for dV and dK, whose A operands it overwrites.
-constexpr int DKV_TILES = 6;
+// (A of dV += P^T dO).  Tensor-pipe order in steady state: dV_i, dK_i, dP^T_{i+1}
+// (once dV_i and dK_i, whose A operands it overwrites, have completed), S^T_{i+2}
+// (once the softmax has read S^T_{i+1}); the softmax's exp phase for block i+1 runs
+// under dV_i / dK_i and its dS phase under S^T_{i+2}.  Three Q stages let Q_{i+2}
+// arrive while Q_i (for dK_i) is still in use.
+constexpr int DKV_TILES = 7;
+constexpr int DKV_QST = 3, DKV_DST = 2;
 
 __global__ void __launch_bounds__(NT, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -526,24 +530,26 @@ __global__ void __launch_bounds__(NT, 1)
     const int nq = p.nblk - kb;        // query blocks kb .. nblk-1
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* kv_full = &sm.bar[0];
-    uint64_t* qd_full = &sm.bar[1];
-    uint64_t* qd_empty = &sm.bar[3];
-    uint64_t* s_full = &sm.bar[5];
-    uint64_t* dp_full = &sm.bar[6];
-    uint64_t* s_free = &sm.bar[7];
-    uint64_t* p_full = &sm.bar[8];
-    uint64_t* ds_full = &sm.bar[9];
-    uint64_t* dv_done = &sm.bar[10];
-    uint64_t* dk_done = &sm.bar[11];
-    uint64_t* sbar = &sm.bar[12];
-    uint64_t* rbar = &sm.bar[14];
-    const uint32_t counts[16] = {1, 1, 1, 1, 1, 1, 1, NSM, NSM, NSM, 1, 1, NSM, NSM, NSM, NSM};
-    setup(sm, 16, counts);
+    uint64_t* q_full = &sm.bar[1];
+    uint64_t* q_empty = &sm.bar[4];
+    uint64_t* do_full = &sm.bar[7];
+    uint64_t* do_empty = &sm.bar[9];
+    uint64_t* s_full = &sm.bar[11];
+    uint64_t* dp_full = &sm.bar[12];
+    uint64_t* s_free = &sm.bar[13];
+    uint64_t* p_full = &sm.bar[14];
+    uint64_t* ds_full = &sm.bar[15];
+    uint64_t* dv_done = &sm.bar[16];
+    uint64_t* dk_done = &sm.bar[17];
+    uint64_t* sbar = &sm.bar[18];
+    uint64_t* rbar = &sm.bar[20];
+    const uint32_t counts[22] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NSM, NSM, NSM, 1, 1, NSM, NSM, NSM, NSM};
+    setup(sm, 22, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* K = sm.base;
     uint8_t* V = sm.base + TILE;
-    auto Qt = [&](int st) { return sm.base + (2 + 2 * st) * TILE; };
-    auto dOt = [&](int st) { return sm.base + (3 + 2 * st) * TILE; };
+    auto Qt = [&](int i) { return sm.base + (2 + i % DKV_QST) * TILE; };
+    auto dOt = [&](int i) { return sm.base + (2 + DKV_QST + i % DKV_DST) * TILE; };
     const int col = h * HD;
     const int rowk = b * p.T + kb * BR;
 
@@ -551,61 +557,71 @@ __global__ void __launch_bounds__(NT, 1)
         tc::mbar_expect_tx(kv_full, 2 * TILE);
         load_tile(K, &mk, kv_full, col, rowk);
         load_tile(V, &mv, kv_full, col, rowk);
-        for (int i = 0; i < nq; ++i) {
-            const int st = i & 1, j = kb + i;
-            if (!tc::mbar_wait(&qd_empty[st], ((i >> 1) & 1) ^ 1, sm.abort)) break;
-            tc::mbar_expect_tx(&qd_full[st], 2 * TILE);
-            load_tile(Qt(st), &mq, &qd_full[st], col, b * p.T + j * BR);
-            load_tile(dOt(st), &mdo, &qd_full[st], col, b * p.T + j * BR);
+        // Q runs up to three blocks ahead, dO two; interleave so neither starves the other
+        int iq = 0, id = 0;
+        bool ok = true;
+        while (ok && (iq < nq || id < nq)) {
+            if (iq < nq && iq <= id + 1) {
+                const int st = iq % DKV_QST;
+                if (!(ok = tc::mbar_wait(&q_empty[st], ((iq / DKV_QST) & 1) ^ 1, sm.abort))) break;
+                tc::mbar_expect_tx(&q_full[st], TILE);
+                load_tile(Qt(iq), &mq, &q_full[st], col, b * p.T + (kb + iq) * BR);
+                ++iq;
+            } else {
+                const int st = id % DKV_DST;
+                if (!(ok = tc::mbar_wait(&do_empty[st], ((id / DKV_DST) & 1) ^ 1, sm.abort))) break;
+                tc::mbar_expect_tx(&do_full[st], TILE);
+                load_tile(dOt(id), &mdo, &do_full[st], col, b * p.T + (kb + id) * BR);
+                ++id;
+            }
         }
     } else if (warp == 1 && lane == 0) {
         const uint32_t k0 = tc::smem_u32(K), v0 = tc::smem_u32(V);
-        auto issue_st = [&](int i) {   // S^T_i = K Q_i^T
-            const uint32_t qn = tc::smem_u32(Qt(i & 1));
+        auto issue_st = [&](int i) -> bool {   // S^T_i = K Q_i^T
+            if (!tc::mbar_wait(&q_full[i % DKV_QST], (i / DKV_QST) & 1, sm.abort)) return false;
+            tc::fence_after();
+            const uint32_t qn = tc::smem_u32(Qt(i));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(k0, kk), dk_(qn, kk), IDESC_KK, kk > 0);
             tc::mma_commit(s_full);
+            return true;
         };
-        auto issue_dpt = [&](int i) {  // dP^T_i = V dO_i^T
-            const uint32_t don = tc::smem_u32(dOt(i & 1));
+        auto issue_dpt = [&](int i) -> bool {  // dP^T_i = V dO_i^T
+            if (!tc::mbar_wait(&do_full[i % DKV_DST], (i / DKV_DST) & 1, sm.abort)) return false;
+            tc::fence_after();
+            const uint32_t don = tc::smem_u32(dOt(i));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128, dk_(v0, kk), dk_(don, kk), IDESC_KK, kk > 0);
             tc::mma_commit(dp_full);
+            return true;
         };
-        bool ok = tc::mbar_wait(kv_full, 0, sm.abort) && tc::mbar_wait(&qd_full[0], 0, sm.abort);
-        if (ok) {
-            tc::fence_after();
-            issue_st(0);
-            issue_dpt(0);
-        }
+        bool ok = tc::mbar_wait(kv_full, 0, sm.abort) && issue_st(0) && issue_dpt(0);
+        // S^T_1 as soon as the softmax has read S^T_0
+        if (ok && nq > 1) ok = tc::mbar_wait(s_free, 0, sm.abort) && issue_st(1);
         for (int i = 0; ok && i < nq; ++i) {
-            const int st = i & 1;
-            const bool more = i + 1 < nq;
-            const uint32_t q0 = tc::smem_u32(Qt(st)), do0 = tc::smem_u32(dOt(st));
-            if (!(ok = tc::mbar_wait(s_free, i & 1, sm.abort))) break;
-            if (more) {
-                if (!(ok = tc::mbar_wait(&qd_full[(i + 1) & 1], ((i + 1) >> 1) & 1, sm.abort))) break;
-                tc::fence_after();
-                issue_st(i + 1);
-            }
+            const uint32_t q0 = tc::smem_u32(Qt(i)), do0 = tc::smem_u32(dOt(i));
             if (!(ok = tc::mbar_wait(p_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc::mma_bf16_ts(tmem + 256, tmem + 192 + kk * 8, dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dv_done);
+            tc::mma_commit(&do_empty[i % DKV_DST]);
             if (!(ok = tc::mbar_wait(ds_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc::mma_bf16_ts(tmem + 384, tmem + 128 + kk * 8, dm_(q0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dk_done);
-            tc::mma_commit(&qd_empty[st]);
-            if (more) {
+            tc::mma_commit(&q_empty[i % DKV_QST]);
+            if (i + 1 < nq) {
                 if (!(ok = tc::mbar_wait(dv_done, i & 1, sm.abort))) break;
                 if (!(ok = tc::mbar_wait(dk_done, i & 1, sm.abort))) break;
-                tc::fence_after();
-                issue_dpt(i + 1);
+                if (!(ok = issue_dpt(i + 1))) break;
+            }
+            if (i + 2 < nq) {
+                if (!(ok = tc::mbar_wait(s_free, (i + 1) & 1, sm.abort))) break;
+                if (!(ok = issue_st(i + 2))) break;
             }
         }
     } else if (warp >= 2) {
