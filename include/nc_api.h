@@ -181,7 +181,11 @@ NC_API int nc_attention_forward(const void* q, const void* k, const void* v, int
 /*
  * Gradients of the attention above given dO (layout of o, ld_o): dq, dk, dv
  * in the layout of q, k, v with ld_dqkv.  workspace: device scratch of
- * nc_attention_workspace_bytes() bytes (row statistics).  Deterministic.
+ * nc_attention_workspace_bytes() bytes, 16-byte aligned: the row statistics
+ * D_t = dO_t.O_t, then (bf16, head dim 128) a store for the score gradients
+ * dS of every causal 128x128 block (B*H*nb(nb+1)/2 tiles of 32 KB, nb =
+ * ceil(T/128)), which lets dq be formed without recomputing the scores.
+ * Deterministic.
  */
 NC_API size_t nc_attention_workspace_bytes(int B, int T, int H);
 NC_API int nc_attention_backward(const void* q, const void* k, const void* v, int ld_qkv,

@@ -34,10 +34,14 @@
 // dq and dk back to the unrotated q, k frame in its epilogue.
 // backward, deterministic, no atomics:
 //   dK/dV kernel, one CTA per 128-key block, query blocks from the diagonal on:
-//     S^T = K Q^T, dP^T = V dO^T, P^T and dS^T through one shared tile,
-//     dV += P^T dO, dK += dS^T Q accumulated in TMEM;
-//   dQ kernel, one CTA per 128-query block, key blocks up to the diagonal:
-//     S = Q K^T, dP = dO V^T, dS to shared memory, dQ += dS K in TMEM.
+//     S^T = K Q^T, dP^T = V dO^T, P^T and dS^T packed into TMEM,
+//     dV += P^T dO, dK += dS^T Q accumulated in TMEM; given a dS store it also
+//     writes each dS^T block (bf16) to global memory;
+//   dQ, with the dS store: one CTA per 128-query block streams the stored dS
+//     blocks and the K blocks up to the diagonal, dQ += dS K in TMEM (no
+//     score is recomputed; the sum runs in key order, so it is deterministic);
+//   dQ, without it: one CTA per 128-query block recomputes S = Q K^T and
+//     dP = dO V^T, forms dS in TMEM and accumulates dQ += dS K.
 #include "kernels.cuh"
 #include "tc_ptx.cuh"
 
@@ -134,9 +138,24 @@ struct AttnParams {
     const float* delta;    // [B, H, T] (backward)
     bf16 *dq, *dk, *dv;    // backward outputs
     const float2* rope;    // [T, 64] (cos, sin); non-null: dq, dk leave rotated back
+    bf16* ds;              // backward: dS tiles written by the dK/dV kernel (null: not kept)
+    long ds_bh;            // tiles per (batch, head): nblk (nblk + 1) / 2
     float scale;           // 1/sqrt(D)
     uint32_t* flag;
 };
+
+// The dS store.  Tile (bh, i, j) holds dS of query block i, key block j <= i of
+// batch-head bh; the tiles of one query block are consecutive (j = 0 .. i).  A
+// tile is 32 KB: two 64-key halves of 16 KB, each [query/8][key%64][query%8]
+// bf16, i.e. 16-byte chunks of 8 queries with the key fastest.  That order lets
+// a warp (32 consecutive keys) write 512 contiguous bytes, and a half is the
+// interleaved MN-major image of dS (M = queries, K = keys) that the dQ product
+// copies to shared memory unchanged.
+constexpr int DS_TILE = BR * HD * 2;
+constexpr int DS_HALF = DS_TILE / 2;
+__device__ __forceinline__ uint8_t* ds_tile(const AttnParams& p, int bh, int i, int j) {
+    return reinterpret_cast<uint8_t*>(p.ds) + ((long)bh * p.ds_bh + (long)i * (i + 1) / 2 + j) * DS_TILE;
+}
 
 struct Smem {
     uint8_t* base;
@@ -164,14 +183,14 @@ __device__ __forceinline__ bool misaligned(const uint8_t* raw, uint32_t* flag) {
     return true;
 }
 
-__device__ __forceinline__ void setup(Smem& s, int nbar, const uint32_t* counts) {
+__device__ __forceinline__ void setup(Smem& s, int nbar, const uint32_t* counts, uint32_t ncols = 512) {
     if (threadIdx.x == 0) {
         for (int i = 0; i < nbar; ++i) tc::mbar_init(&s.bar[i], counts[i]);
         *s.abort = 0;
         tc::fence_barrier_init();
     }
     if (threadIdx.x / 32 == 1) {
-        tc::tmem_alloc(s.tmem_slot, 512);
+        tc::tmem_alloc(s.tmem_slot, ncols);
         tc::tmem_relinquish();
     }
     tc::fence_before();
@@ -179,13 +198,13 @@ __device__ __forceinline__ void setup(Smem& s, int nbar, const uint32_t* counts)
     tc::fence_after();
 }
 
-__device__ __forceinline__ void teardown(Smem& s, uint32_t tmem, uint32_t* flag) {
+__device__ __forceinline__ void teardown(Smem& s, uint32_t tmem, uint32_t* flag, uint32_t ncols = 512) {
     tc::fence_before();
     __syncthreads();
     if (threadIdx.x == 0 && *s.abort && flag) atomicOr(flag, NC_FLAG_TIMEOUT);
     if (threadIdx.x / 32 == 1) {
         tc::fence_after();
-        tc::tmem_dealloc(tmem, 512);
+        tc::tmem_dealloc(tmem, ncols);
     }
 }
 
@@ -629,15 +648,22 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
         const float c2 = p.scale * LOG2E;
         const long srow = ((long)b * p.H + h) * p.T;
+        // this thread's statistic of query row kb*BR + 128 i + r (group 0: lse, 1: D),
+        // loaded one block ahead so its latency hides under the previous block
+        const float* src = (g == 0 ? p.lse : p.delta) + srow;
+        auto fetch = [&](int jb) { const int t = jb * BR + r; return t < p.T ? src[t] : NAN; };
+        float nxt = fetch(kb);
         float s[64];
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
             const int j = kb + i;
             float* stat = sm.xch + (i & 1) * 256;          // [lse2 | D] of this query block
             {
-                const int t = j * BR + r;
-                if (g == 0) stat[r] = t < p.T ? p.lse[srow + t] * LOG2E : INFINITY;
-                else stat[128 + r] = t < p.T ? p.delta[srow + t] : 0.f;
+                const float cur = nxt;
+                if (i + 1 < nq) nxt = fetch(j + 1);
+                const bool valid = j * BR + r < p.T;
+                if (g == 0) stat[r] = valid ? cur * LOG2E : INFINITY;
+                else stat[128 + r] = valid ? cur : 0.f;
             }
             tc::mbar_arrive(&sbar[i & 1]);
             if (!(ok = tc::mbar_wait_warp(&sbar[i & 1], (i >> 1) & 1, sm.abort))) break;
@@ -701,6 +727,17 @@ __global__ void __launch_bounds__(NT, 1)
             tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(ds_full);
+            if (p.ds) {   // keep key r's dS for the dQ product: query chunks 4g+k and 8+4g+k
+                uint8_t* base = ds_tile(p, blockIdx.x, j, kb) + (r >> 6) * DS_HALF + (r & 63) * 16;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t* x = wd + 16 * h2 + 4 * k;
+                        *reinterpret_cast<uint4*>(base + (8 * h2 + 4 * g + k) * 1024) =
+                            make_uint4(x[0], x[1], x[2], x[3]);
+                    }
+            }
         }
         if (ok && tc::mbar_wait_warp(dk_done, (nq - 1) & 1, sm.abort) &&
             tc::mbar_wait_warp(dv_done, (nq - 1) & 1, sm.abort)) {
@@ -716,6 +753,93 @@ __global__ void __launch_bounds__(NT, 1)
         }
     }
     teardown(sm, tmem, p.flag);
+}
+
+// ===================================================================== dQ from the dS^T store
+// dQ_i = scale * sum_{j<=i} dS_ij K_j as a streamed block-causal product: the dK/dV
+// kernel has already formed every dS_ij, so nothing is recomputed here.  Stages hold
+// 64 keys: the stored dS half (64 keys x 128 queries, the interleaved MN-major A
+// operand, one plain bulk copy) and the K half-tile (64 keys x 128 dims, the
+// 128-byte-swizzled MN-major B operand, by TMA).  Four warps read dQ out of
+// TMEM; two CTAs share an SM so one's epilogue overlaps the other's stream.
+// barriers: 0..2 full, 3..5 empty, 6 done, 7 drain
+constexpr int DQS_NT = 192;              // producer warp, MMA warp, 4 epilogue warps
+constexpr int HATOM = 64 * 128;          // 8 KB: 64 rows x 64 bf16, 128-byte swizzle
+constexpr int DQS_ST = 3;                // stages of 4 atoms (one TILE) each
+constexpr uint32_t IDESC_MM = tc::idesc_bf16(128, 128, true, true);
+
+// MN-major view of a 64-row half tile (MN = its 128 columns, two atoms), k-th 16-row slice
+__device__ __forceinline__ uint64_t dh_(uint32_t half, int kk) { return tc::sdesc(half + kk * 2048, HATOM, 1024); }
+// the stored dS half (interleaved MN-major: 8-key groups 128 B apart, 8-query chunks 1 KB apart)
+__device__ __forceinline__ uint64_t dsa_(uint32_t half, int kk) { return tc::sdesc_none(half + kk * 256, 128, 1024); }
+
+__global__ void __launch_bounds__(DQS_NT, 2)
+    attn_dq_ds_kernel(const __grid_constant__ CUtensorMap mk, const AttnParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (misaligned(smem_raw, p.flag)) return;
+    Smem sm = carve(smem_raw, DQS_ST);
+    const int qb = p.nblk - 1 - blockIdx.y, h = blockIdx.x % p.H, b = blockIdx.x / p.H;
+    const int nu = 2 * (qb + 1);           // 64-key units up to the diagonal
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    uint64_t* full = &sm.bar[0];
+    uint64_t* empty = &sm.bar[3];
+    uint64_t* done = &sm.bar[6];
+    uint64_t* drain = &sm.bar[7];
+    const uint32_t counts[8] = {1, 1, 1, 1, 1, 1, 1, 1};
+    setup(sm, 8, counts, 128);
+    const uint32_t tmem = *sm.tmem_slot;
+    const int col = h * HD;
+
+    if (warp == 0 && lane == 0) {
+        const uint8_t* ds0 = ds_tile(p, blockIdx.x, qb, 0);
+        int u = 0;
+        for (; u < nu; ++u) {
+            const int st = u % DQS_ST;
+            if (!tc::mbar_wait(&empty[st], ((u / DQS_ST) & 1) ^ 1, sm.abort)) break;
+            uint8_t* dst = sm.base + st * TILE;
+            tc::mbar_expect_tx(&full[st], TILE);
+            const int kr = b * p.T + 64 * u;
+            tc::bulk_load(dst, ds0 + (long)u * DS_HALF, DS_HALF, &full[st]);
+            tc::tma_load_3d(dst + 2 * HATOM, &mk, &full[st], col, kr, 0);
+            tc::tma_load_3d(dst + 3 * HATOM, &mk, &full[st], col + 64, kr, 0);
+        }
+        if (*sm.abort)   // let the copies still in flight land before the CTA exits
+            for (int w = u - 1; w >= 0 && w >= u - DQS_ST; --w)
+                tc::mbar_wait_drain(&full[w % DQS_ST], (w / DQS_ST) & 1);
+    } else if (warp == 1 && lane == 0) {
+        bool ok = true;
+        for (int u = 0; u < nu; ++u) {
+            const int st = u % DQS_ST;
+            if (!(ok = tc::mbar_wait(&full[st], (u / DQS_ST) & 1, sm.abort))) break;
+            tc::fence_after();
+            const uint32_t a0 = tc::smem_u32(sm.base + st * TILE), b0 = a0 + 2 * HATOM;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) tc::mma_bf16(tmem, dsa_(a0, kk), dh_(b0, kk), IDESC_MM, (u > 0 || kk > 0));
+            tc::mma_commit(&empty[st]);
+        }
+        if (ok) tc::mma_commit(done);
+        if (*sm.abort) {
+            tc::mma_commit(drain);
+            tc::mbar_wait_drain(drain, 0);
+        }
+    } else if (warp >= 2) {
+        const int q = warp & 3, r = q * 32 + lane;
+        const uint32_t lanes = (uint32_t)(q * 32) << 16;
+        const int t = qb * BR + r;
+        if (tc::mbar_wait_warp(done, 0, sm.abort)) {
+            tc::fence_after();
+            float v[64];
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {
+                ld_half(tmem + lanes, g, v);
+                if (t < p.T) {
+                    if (p.rope) unrope_half(v, p.rope, t, g);
+                    store_out_half(p.dq + (long)(b * p.T + t) * p.ldd + col, g, v, p.scale);
+                }
+            }
+        }
+    }
+    teardown(sm, tmem, p.flag, 128);
 }
 
 int smem_bytes(int tiles) { return tiles * TILE + 256 + XCH_BYTES; }
@@ -763,15 +887,23 @@ int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, b
     return NC_OK;
 }
 
+// dS store: B*H*nblk(nblk+1)/2 tiles of 128 x 128 bf16
+size_t attention_tc_ds_bytes(int B, int T, int H) {
+    const long nblk = ceil_div(T, BR);
+    return (size_t)B * H * (nblk * (nblk + 1) / 2) * DS_TILE;
+}
+
 int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, const bf16* dout,
                           long ldo, const float* lse, const float* delta, bf16* dq, bf16* dk, bf16* dv,
-                          long ldd, int B, int T, int H, const float2* rope, cudaStream_t s) {
+                          long ldd, int B, int T, int H, const float2* rope, bf16* ds, cudaStream_t s) {
     static bool init = false;
     if (!init) {
         NC_TRY(set_smem(attn_dq_kernel, smem_bytes(DQ_TILES)));
         NC_TRY(set_smem(attn_dkdv_kernel, smem_bytes(DKV_TILES)));
+        NC_TRY(set_smem(attn_dq_ds_kernel, smem_bytes(DQS_ST)));
         init = true;
     }
+    if ((uintptr_t)ds % 16) ds = nullptr;
     CUtensorMap mq, mk, mv, mdo;
     const long rows = (long)B * T;
     NC_TRY(maps(&mq, q, rows, ld, H));
@@ -782,8 +914,15 @@ int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, 
     p.T = T; p.H = H; p.nblk = ceil_div(T, BR); p.ldo = ldo; p.ldd = ldd;
     p.lse = const_cast<float*>(lse); p.delta = delta; p.dq = dq; p.dk = dk; p.dv = dv; p.rope = rope;
     p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
+    p.ds = ds; p.ds_bh = (long)p.nblk * (p.nblk + 1) / 2;
     attn_dkdv_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);
-    attn_dq_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(DQ_TILES), s>>>(mq, mk, mv, mdo, p);
+    if (ds) {
+        CUtensorMap mk64;
+        NC_TRY(make_map(&mk64, k, (long)H * HD, rows, 1, ld, 0, 64, 64));
+        attn_dq_ds_kernel<<<dim3(H * B, p.nblk), DQS_NT, smem_bytes(DQS_ST), s>>>(mk64, p);
+    } else {
+        attn_dq_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(DQ_TILES), s>>>(mq, mk, mv, mdo, p);
+    }
     note_launch(2);
     NC_LAUNCH_CHECK("attn backward kernels");
     return NC_OK;

@@ -75,6 +75,8 @@ struct nc_model {
     void* dO;
     void* dh;
     float* delta;      // attention row statistics [M * H]
+    void* ds;          // attention dS store for (maxB, maxT) (bf16, head dim 128)
+    size_t ds_bytes;
     void* ebws;
     size_t ebws_bytes;
     void* splitk;
@@ -168,6 +170,8 @@ void layout(nc_model* m, char* base, size_t* total) {
         m->dO = c.take(M * d * act);
         m->dh = c.take(M * 4 * d * act);
         m->delta = (float*)c.take(M * m->H * 4);
+        m->ds_bytes = m->dtype == NC_BF16 ? attention_ds_bytes(m->maxB, m->maxT, m->H, m->Dh) : 0;
+        m->ds = m->ds_bytes ? c.take(m->ds_bytes) : nullptr;
         m->ebws_bytes = embed_backward_ws_bytes((int)M, d, V);
         m->ebws = c.take(m->ebws_bytes);
     }
@@ -356,7 +360,8 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
             Prof pr(m, NC_PROF_ATTN_BWD, 2.5 * attn_fl, 0);
             NC_TRY(attention_backward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, (T*)m->dO, d, Ly.lse, dq,
                                          dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s, m->rope,
-                                         &unroped, fuse_rope));
+                                         &unroped, fuse_rope,
+                                         attention_ds_bytes(B, T_, H, Dh) <= m->ds_bytes ? m->ds : nullptr));
         }
         if (!unroped) NC_TRY(rope(m->dqkv, -1.f));
         NC_TRY(weight_grad(m, G + m->poff[b0], 3 * d, d, m->dqkv, 3 * d, Ly.y1, d, M, accumulate));
@@ -765,7 +770,11 @@ int nc_attention_forward(const void* q, const void* k, const void* v, int ld_qkv
     return set_error(NC_ERR_ARG, "dtype %d", dtype);
 }
 
-size_t nc_attention_workspace_bytes(int B, int T, int H) { return (size_t)B * T * H * 4; }
+// [row statistics: B*H*T floats | dS store of the bf16 head-dim-128 path]
+size_t nc_attention_workspace_bytes(int B, int T, int H) {
+    if (B <= 0 || T <= 0 || H <= 0) return 256;
+    return al((size_t)B * T * H * 4) + attention_ds_bytes(B, T, H, 128);
+}
 
 int nc_attention_backward(const void* q, const void* k, const void* v, int ld_qkv, const void* o,
                           const void* dout, int ld_o, const float* lse, void* dq, void* dk, void* dv,
@@ -780,7 +789,9 @@ int nc_attention_backward(const void* q, const void* k, const void* v, int ld_qk
     if (dtype == NC_BF16)
         return attention_backward<bf16>((const bf16*)q, (const bf16*)k, (const bf16*)v, ld_qkv,
                                         (const bf16*)o, (const bf16*)dout, ld_o, lse, (bf16*)dq,
-                                        (bf16*)dk, (bf16*)dv, ld_dqkv, (float*)workspace, B, T, H, D, s);
+                                        (bf16*)dk, (bf16*)dv, ld_dqkv, (float*)workspace, B, T, H, D, s,
+                                        nullptr, nullptr, false,
+                                        (char*)workspace + al((size_t)B * T * H * 4));
     if (dtype == NC_FP32)
         return attention_backward<float>((const float*)q, (const float*)k, (const float*)v, ld_qkv,
                                          (const float*)o, (const float*)dout, ld_o, lse, (float*)dq,

@@ -83,11 +83,16 @@ int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ld
 // rope: optional RoPE table; when the kernel can rotate dq, dk back itself it
 // does so and sets *rope_done = 1 (else the caller applies the inverse RoPE).
 // delta_ready: delta already holds dO.O per row (computed by the producer of dO)
+// ds: optional scratch of attention_ds_bytes(B, T_, H) bytes; with it the bf16
+// head-dim-128 path keeps dS from the dK/dV pass and forms dq as a plain product
+// instead of recomputing the scores.
 template <typename T>
 int attention_backward(const T* q, const T* k, const T* v, long ld, const T* o, const T* dout,
                        long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
                        int B, int T_, int H, int D, cudaStream_t s, const float2* rope = nullptr,
-                       int* rope_done = nullptr, bool delta_ready = false);
+                       int* rope_done = nullptr, bool delta_ready = false, void* ds = nullptr);
+// bytes of the dS scratch above (0 where it would not be used)
+size_t attention_ds_bytes(int B, int T_, int H, int D);
 
 // ------------------------------------------------------------ optimizers
 // Muon, phase 1: buf = mu*buf + g; g <- g + mu*buf (nesterov) or buf; per-CTA
