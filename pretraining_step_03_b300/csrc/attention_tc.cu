@@ -527,16 +527,26 @@ __global__ void __launch_bounds__(NT, 1)
 // smem tiles: 0 K | 1 V | 2..4 Q stages | 5,6 dO stages
 // barriers: 0 kv_full, 1-3 q_full, 4-6 q_empty, 7-8 do_full, 9-10 do_empty, 11 s_full,
 //           12 dp_full, 13 s_free, 14 p_full, 15 ds_full, 16 dv_done, 17 dk_done,
-//           18-19 stat barriers, 20-21 read barriers
+//           18-19 stat barriers
 // TMEM: S^T at 0, dP^T at 128, dV at 256, dK at 384.  The packed bf16 operands go into
-// the dP^T region once it has been read: dS^T at 128 (A of dK += dS^T Q), P^T at 192
-// (A of dV += P^T dO).  Tensor-pipe order in steady state: dV_i, dK_i, dP^T_{i+1}
-// (once dV_i and dK_i, whose A operands it overwrites, have completed), S^T_{i+2}
-// (once the softmax has read S^T_{i+1}); the softmax's exp phase for block i+1 runs
-// under dV_i / dK_i and its dS phase under S^T_{i+2}.  Three Q stages let Q_{i+2}
-// arrive while Q_i (for dK_i) is still in use.
+// the dP^T region once it has been read, each group only into the 64 columns it read
+// itself (so the two groups never wait for each other): group g puts its P^T slices
+// at 128 + 32g .. +31 and its dS^T slices at 192 + 32g .. +31, and the products take
+// each 16-query K slice from where its group left it (pk_col).  Tensor-pipe order in
+// steady state: dV_i, dK_i, dP^T_{i+1} (once dV_i and dK_i, whose A operands it
+// overwrites, have completed), S^T_{i+2} (once the softmax has read S^T_{i+1}); the
+// softmax's exp phase for block i+1 runs under dV_i / dK_i and its dS phase under
+// S^T_{i+2}.  P^T is released to dV before dS^T is computed.  Three Q stages let
+// Q_{i+2} arrive while Q_i (for dK_i) is still in use.
 constexpr int DKV_TILES = 7;
 constexpr int DKV_QST = 3, DKV_DST = 2;
+
+// TMEM column (relative to the packed region) of K slice kk (queries 16kk .. 16kk+15)
+// of a packed operand: queries [32g, 32g+32) and [64+32g, 64+32g+32) belong to group g,
+// which stores them as 32 consecutive columns at 32g.
+__host__ __device__ constexpr uint32_t pk_col(int kk) {
+    return 32u * ((kk >> 1) & 1) + 16u * (kk >> 2) + 8u * (kk & 1);
+}
 
 __global__ void __launch_bounds__(NT, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -561,9 +571,8 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* dv_done = &sm.bar[16];
     uint64_t* dk_done = &sm.bar[17];
     uint64_t* sbar = &sm.bar[18];
-    uint64_t* rbar = &sm.bar[20];
-    const uint32_t counts[22] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NSM, NSM, NSM, 1, 1, NSM, NSM, NSM, NSM};
-    setup(sm, 22, counts);
+    const uint32_t counts[20] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NSM, NSM, NSM, 1, 1, NSM, NSM};
+    setup(sm, 20, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* K = sm.base;
     uint8_t* V = sm.base + TILE;
@@ -623,14 +632,14 @@ __global__ void __launch_bounds__(NT, 1)
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16_ts(tmem + 256, tmem + 192 + kk * 8, dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
+                tc::mma_bf16_ts(tmem + 256, tmem + 128 + pk_col(kk), dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dv_done);
             tc::mma_commit(&do_empty[i % DKV_DST]);
             if (!(ok = tc::mbar_wait(ds_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16_ts(tmem + 384, tmem + 128 + kk * 8, dm_(q0, kk), IDESC_KM, (i > 0 || kk > 0));
+                tc::mma_bf16_ts(tmem + 384, tmem + 192 + pk_col(kk), dm_(q0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dk_done);
             tc::mma_commit(&q_empty[i % DKV_QST]);
             if (i + 1 < nq) {
@@ -692,38 +701,43 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int e = 0; e < 64; ++e)
                     if (r > col_of(g, e)) s[e] = 0.f;
             }
-            uint32_t wp[32], wd[32];
+            uint32_t wd[32];
+            {
+                uint32_t d[32];   // this thread's dP^T, one 32-query chunk at a time
+                {
+                    uint32_t wp[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) wp[e] = pack2(s[2 * e], s[2 * e + 1]);
-            if (!(ok = tc::mbar_wait_warp(dp_full, i & 1, sm.abort))) break;
-            tc::fence_after();
+                    for (int e = 0; e < 32; ++e) wp[e] = pack2(s[2 * e], s[2 * e + 1]);
+                    if (!(ok = tc::mbar_wait_warp(dp_full, i & 1, sm.abort))) break;
+                    tc::fence_after();
+                    tc::tmem_ld32(tmem + lanes + 128 + 32 * g, d);
+                    tc::tmem_wait_ld();
+                    // P^T into the columns just read; dV_i can start while dS^T is formed
+                    tc::tmem_st32(tmem + lanes + 128 + 32 * g, wp);
+                    tc::tmem_wait_st();
+                }
+                tc::fence_before();
+                tc::mbar_arrive(p_full);
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {   // dS^T = P^T (dP^T - D[c]), one 32-column chunk at a time
-                uint32_t d[32];
-                tc::tmem_ld32(tmem + lanes + 128 + (g + 2 * h2) * 32, d);
-                tc::tmem_wait_ld();
-                const float4* d4 = reinterpret_cast<const float4*>(stat + 128 + 64 * h2 + 32 * g);
+                for (int h2 = 0; h2 < 2; ++h2) {   // dS^T = P^T (dP^T - D[c])
+                    if (h2 == 1) {
+                        tc::tmem_ld32(tmem + lanes + 192 + 32 * g, d);
+                        tc::tmem_wait_ld();
+                    }
+                    const float4* d4 = reinterpret_cast<const float4*>(stat + 128 + 64 * h2 + 32 * g);
 #pragma unroll
-                for (int k4 = 0; k4 < 8; ++k4) {
-                    const float4 dv4 = d4[k4];
-                    const float* x = s + 32 * h2 + 4 * k4;
-                    wd[16 * h2 + 2 * k4] = pack2(x[0] * (__uint_as_float(d[4 * k4]) - dv4.x),
-                                                 x[1] * (__uint_as_float(d[4 * k4 + 1]) - dv4.y));
-                    wd[16 * h2 + 2 * k4 + 1] = pack2(x[2] * (__uint_as_float(d[4 * k4 + 2]) - dv4.z),
-                                                     x[3] * (__uint_as_float(d[4 * k4 + 3]) - dv4.w));
+                    for (int k4 = 0; k4 < 8; ++k4) {
+                        const float4 dv4 = d4[k4];
+                        const float* x = s + 32 * h2 + 4 * k4;
+                        const uint32_t* y = d + 4 * k4;
+                        wd[16 * h2 + 2 * k4] = pack2(x[0] * (__uint_as_float(y[0]) - dv4.x),
+                                                     x[1] * (__uint_as_float(y[1]) - dv4.y));
+                        wd[16 * h2 + 2 * k4 + 1] = pack2(x[2] * (__uint_as_float(y[2]) - dv4.z),
+                                                         x[3] * (__uint_as_float(y[3]) - dv4.w));
+                    }
                 }
             }
-            // the packed operands land in dP^T columns the other group reads: both
-            // groups finish reading dP^T first
-            tc::fence_before();
-            tc::mbar_arrive(&rbar[i & 1]);
-            if (!(ok = tc::mbar_wait_warp(&rbar[i & 1], (i >> 1) & 1, sm.abort))) break;
-            tc::fence_after();
-            st_half_bf16(tmem + lanes + 192, g, wp);
-            tc::tmem_wait_st();
-            tc::fence_before();
-            tc::mbar_arrive(p_full);
-            st_half_bf16(tmem + lanes + 128, g, wd);
+            tc::tmem_st32(tmem + lanes + 192 + 32 * g, wd);
             tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(ds_full);
