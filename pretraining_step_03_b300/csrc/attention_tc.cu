@@ -117,12 +117,14 @@ __device__ __forceinline__ void store_out_half(bf16* row, int g, const float* v,
     }
 }
 
-// inverse RoPE (rotation by -angle) of head-dim pairs (j, j+64), j in [32g, 32g+32)
-__device__ __forceinline__ void unrope_half(float* v, const float2* table, int t, int g) {
-    const float2* row = table + (long)t * 64 + 32 * g;
+// inverse RoPE (rotation by -angle) of head-dim pairs (j, j+64), j in [32g, 32g+32);
+// the table is pair-major (pair j of position t at table[j * ld + t]), so the 32
+// lanes of a warp (consecutive positions) read 256 contiguous bytes
+__device__ __forceinline__ void unrope_half(float* v, const float2* table, int ld, int t, int g) {
+    const float2* col = table + (long)(32 * g) * ld + t;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const float2 cs = __ldg(row + i);
+        const float2 cs = __ldg(col + (long)i * ld);
         const float x1 = v[i], x2 = v[32 + i];
         v[i] = x1 * cs.x + x2 * cs.y;
         v[32 + i] = x2 * cs.x - x1 * cs.y;
@@ -137,7 +139,8 @@ struct AttnParams {
     float* lse;            // [B, H, T]
     const float* delta;    // [B, H, T] (backward)
     bf16 *dq, *dk, *dv;    // backward outputs
-    const float2* rope;    // [T, 64] (cos, sin); non-null: dq, dk leave rotated back
+    const float2* rope;    // (cos, sin) of pair j, position t at rope[j * rope_ld + t]; non-null:
+    int rope_ld;           //   dq, dk leave rotated back
     bf16* ds;              // backward: dS tiles written by the dK/dV kernel (null: not kept)
     long ds_bh;            // tiles per (batch, head): nblk (nblk + 1) / 2
     float scale;           // 1/sqrt(D)
@@ -515,7 +518,7 @@ __global__ void __launch_bounds__(NT, 1)
             tc::fence_after();
             ld_half(tmem + lanes + 256, g, s);
             if (t < p.T) {
-                if (p.rope) unrope_half(s, p.rope, t, g);
+                if (p.rope) unrope_half(s, p.rope, p.rope_ld, t, g);
                 store_out_half(p.dq + (long)(b * p.T + t) * p.ldd + col, g, s, p.scale);
             }
         }
@@ -761,7 +764,7 @@ __global__ void __launch_bounds__(NT, 1)
             if (key < p.T) store_out_half(p.dv + (long)(b * p.T + key) * p.ldd + col, g, s, 1.f);
             ld_half(tmem + lanes + 384, g, s);
             if (key < p.T) {
-                if (p.rope) unrope_half(s, p.rope, key, g);
+                if (p.rope) unrope_half(s, p.rope, p.rope_ld, key, g);
                 store_out_half(p.dk + (long)(b * p.T + key) * p.ldd + col, g, s, p.scale);
             }
         }
@@ -847,7 +850,7 @@ __global__ void __launch_bounds__(DQS_NT, 2)
             for (int g = 0; g < 2; ++g) {
                 ld_half(tmem + lanes, g, v);
                 if (t < p.T) {
-                    if (p.rope) unrope_half(v, p.rope, t, g);
+                    if (p.rope) unrope_half(v, p.rope, p.rope_ld, t, g);
                     store_out_half(p.dq + (long)(b * p.T + t) * p.ldd + col, g, v, p.scale);
                 }
             }
@@ -909,7 +912,8 @@ size_t attention_tc_ds_bytes(int B, int T, int H) {
 
 int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, const bf16* dout,
                           long ldo, const float* lse, const float* delta, bf16* dq, bf16* dk, bf16* dv,
-                          long ldd, int B, int T, int H, const float2* rope, bf16* ds, cudaStream_t s) {
+                          long ldd, int B, int T, int H, const float2* rope, int rope_ld, bf16* ds,
+                          cudaStream_t s) {
     static bool init = false;
     if (!init) {
         NC_TRY(set_smem(attn_dq_kernel, smem_bytes(DQ_TILES)));
@@ -927,6 +931,7 @@ int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, 
     AttnParams p{};
     p.T = T; p.H = H; p.nblk = ceil_div(T, BR); p.ldo = ldo; p.ldd = ldd;
     p.lse = const_cast<float*>(lse); p.delta = delta; p.dq = dq; p.dk = dk; p.dv = dv; p.rope = rope;
+    p.rope_ld = rope_ld;
     p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
     p.ds = ds; p.ds_bh = (long)p.nblk * (p.nblk + 1) / 2;
     attn_dkdv_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);

@@ -53,13 +53,13 @@ struct nc_model {
     void* nsA;         // [6L, d, d]
     void* nsB;
     // misc
-    float2* rope;      // [maxT, Dh/2]
+    float2* rope;      // [Dh/2, maxT]: (cos, sin) of pair j at position t at j * maxT + t
     float* loss;       // [2 * 64] micro-step {loss, bpb}
     uint32_t* flag;
     int32_t* tok_stage;  // [2, maxM] tokens, targets (nc_train_step)
     // activations (act type unless noted)
     struct Layer {
-        void *y1, *qkv, *o, *y2, *h, *a;
+        void *y1, *qkv, *o, *y2, *a;
         float *r1, *r2, *lse;
     };
     std::vector<Layer> L;
@@ -155,7 +155,6 @@ void layout(nc_model* m, char* base, size_t* total) {
             y.lse = (float*)c.take(M * m->H * 4);
             y.y2 = c.take(M * d * act);
             y.r2 = (float*)c.take(M * 4);
-            y.h = c.take(M * 4 * d * act);
             y.a = c.take(M * 4 * d * act);
         }
         m->x = (float*)c.take(M * d * 4);
@@ -265,6 +264,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
     T* gop = m->dtype == NC_BF16 ? (T*)m->gT : (T*)m->g;  // residual gradient as GEMM operand
     T* gT = m->dtype == NC_BF16 ? (T*)m->gT : nullptr;
     const bool fuse_rope = m->dtype == NC_BF16 && Dh == 128;
+    const int rope_ld = m->maxT > 0 ? m->maxT : 1;   // stride of the pair-major RoPE table
     auto norm_f = [&](const float* x, void* y, float* r) {
         Prof pr(m, NC_PROF_NORM, 0, Md * (4 + ab) + M * 4.0);
         return rmsnorm_forward<T>(x, (T*)y, r, M, d, s);
@@ -275,7 +275,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
     };
     auto rope = [&](void* qkv, float sign) {
         Prof pr(m, NC_PROF_ROPE, 0, 4.0 * Md * ab);
-        return rope_apply<T>((T*)qkv, 3 * d, M, T_, H, Dh, m->rope, sign, s);
+        return rope_apply<T>((T*)qkv, 3 * d, M, T_, H, Dh, m->rope, rope_ld, sign, s);
     };
 
     // ------------------------------------------------ forward
@@ -291,6 +291,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
             Gemm g = mk(m, M, 3 * d, d, Ly.y1, d, false, W<T>(m, b0), d, false, Ly.qkv, 3 * d, act);
             if (fuse_rope) {
                 g.epi = EPI_ROPE; g.rope = m->rope; g.rope_T = T_; g.rope_cols = 2 * d;
+                g.rope_ld = rope_ld;
             }
             NC_TRY(run_gemm(m, g));
             if (!fuse_rope) NC_TRY(rope(Ly.qkv, 1.f));
@@ -307,8 +308,8 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         }
         NC_TRY(norm_f(m->x, Ly.y2, Ly.r2));
         {   // h = y2 W1^T, a = relu(h)^2
-            Gemm g = mk(m, M, F, d, Ly.y2, d, false, W<T>(m, b0 + 4), d, false, Ly.h, F, act);
-            g.epi = EPI_RELU2; g.C2 = Ly.a;
+            Gemm g = mk(m, M, F, d, Ly.y2, d, false, W<T>(m, b0 + 4), d, false, Ly.a, F, act);
+            g.epi = EPI_RELU2;
             NC_TRY(run_gemm(m, g));
         }
         {   // x += a W2^T
@@ -337,7 +338,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         NC_TRY(weight_grad(m, G + m->poff[b0 + 5], d, F, gop, d, Ly.a, F, M, accumulate));
         {   // dh = (g W2) * 2 relu(h)
             Gemm g = mk(m, M, F, d, gop, d, false, W<T>(m, b0 + 5), F, true, m->dh, F, act);
-            g.epi = EPI_RELU2_BWD; g.aux = Ly.h; g.ldaux = F; g.aux_dtype = act;
+            g.epi = EPI_RELU2_BWD; g.aux = Ly.a; g.ldaux = F; g.aux_dtype = act;
             NC_TRY(run_gemm(m, g));
         }
         NC_TRY(weight_grad(m, G + m->poff[b0 + 4], F, d, m->dh, F, Ly.y2, d, M, accumulate));
@@ -360,7 +361,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
             Prof pr(m, NC_PROF_ATTN_BWD, 2.5 * attn_fl, 0);
             NC_TRY(attention_backward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, (T*)m->dO, d, Ly.lse, dq,
                                          dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s, m->rope,
-                                         &unroped, fuse_rope,
+                                         rope_ld, &unroped, fuse_rope,
                                          attention_ds_bytes(B, T_, H, Dh) <= m->ds_bytes ? m->ds : nullptr));
         }
         if (!unroped) NC_TRY(rope(m->dqkv, -1.f));
@@ -550,13 +551,15 @@ int nc_init_model(int depth, int d_model, int n_head, int vocab, uint64_t seed, 
             }
         if ((rc = cuda_check(cudaMemcpyAsync(m->mats, mats.data(), mats.size() * sizeof(MuonMat),
                                              cudaMemcpyHostToDevice, s), "H2D mats"))) break;
-        // RoPE table: angle t * 10000^(-2j/Dh), computed in double
+        // RoPE table: angle t * 10000^(-2j/Dh), computed in double; pair-major
+        // ([j][t]) so that kernels whose lanes hold consecutive positions read it
+        // contiguously
         const int half = m->Dh / 2, Tt = m->maxT > 0 ? m->maxT : 1;
         std::vector<float2> rt((size_t)Tt * half);
         for (int t = 0; t < Tt; ++t)
             for (int j = 0; j < half; ++j) {
                 double ang = t * pow(10000.0, -2.0 * j / m->Dh);
-                rt[(size_t)t * half + j] = make_float2((float)cos(ang), (float)sin(ang));
+                rt[(size_t)j * Tt + t] = make_float2((float)cos(ang), (float)sin(ang));
             }
         if ((rc = cuda_check(cudaMemcpyAsync(m->rope, rt.data(), rt.size() * 8, cudaMemcpyHostToDevice, s),
                              "H2D rope"))) break;
@@ -790,7 +793,7 @@ int nc_attention_backward(const void* q, const void* k, const void* v, int ld_qk
         return attention_backward<bf16>((const bf16*)q, (const bf16*)k, (const bf16*)v, ld_qkv,
                                         (const bf16*)o, (const bf16*)dout, ld_o, lse, (bf16*)dq,
                                         (bf16*)dk, (bf16*)dv, ld_dqkv, (float*)workspace, B, T, H, D, s,
-                                        nullptr, nullptr, false,
+                                        nullptr, 0, nullptr, false,
                                         (char*)workspace + al((size_t)B * T * H * 4));
     if (dtype == NC_FP32)
         return attention_backward<float>((const float*)q, (const float*)k, (const float*)v, ld_qkv,

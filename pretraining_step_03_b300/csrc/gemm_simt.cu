@@ -79,12 +79,11 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(Gemm g) {
                 if (g.aux && g.beta != 0.f) v += g.beta * ld_any(g.aux, ai, g.aux_dtype);
                 st_any(g.C, ci, g.c_dtype, v);
             } else if (g.epi == EPI_RELU2) {
-                st_any(g.C, ci, g.c_dtype, v);
                 float r = fmaxf(v, 0.f);
-                st_any(g.C2, ci, g.c_dtype, r * r);
-            } else {  // EPI_RELU2_BWD
-                float h = ld_any(g.aux, ai, g.aux_dtype);
-                st_any(g.C, ci, g.c_dtype, v * 2.f * fmaxf(h, 0.f));
+                st_any(g.C, ci, g.c_dtype, r * r);
+            } else {  // EPI_RELU2_BWD: d/dh relu(h)^2 = 2 relu(h) = 2 sqrt(a)
+                float a = ld_any(g.aux, ai, g.aux_dtype);
+                st_any(g.C, ci, g.c_dtype, v * 2.f * sqrtf(fmaxf(a, 0.f)));
             }
         }
     }

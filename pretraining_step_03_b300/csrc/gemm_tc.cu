@@ -32,6 +32,8 @@ namespace {
 
 constexpr int BM = 128, BK = 64, NTHREADS = 320, GROUP_M = 8;
 constexpr int EPI_WARPS = 8;   // two groups of four, each owns half the tile columns
+constexpr int EPI_STG = 4096;  // per epilogue warp: 32 rows x 32 fp32 staging for coalesced stores
+constexpr int EPI_STG_BYTES = EPI_WARPS * EPI_STG;
 
 struct TcParams {
     int M, N, K, batch;
@@ -39,13 +41,12 @@ struct TcParams {
     long units;
     void* C; long ldc, sC; int c_dtype;
     const void* aux; long ldaux, sAux; int aux_dtype;
-    void* C2;
     float alpha, beta;
     int epi;
     float* ws;        // split-K partials [splits][batch][M][N], or null
     uint32_t* flag;   // device flag word for timeouts (may be null)
-    const float2* rope;
-    int rope_T, rope_cols;
+    const float2* rope;   // (cos, sin) of pair j at position t: rope[j * rope_ld + t]
+    int rope_T, rope_cols, rope_ld;
     float* delta;
 };
 
@@ -55,7 +56,7 @@ template <int BN> struct Cfg {
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int STAGES = BN == 256 ? 4 : 6;
     static constexpr uint32_t TMEM_COLS = 2 * BN;
-    static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+    static constexpr int SMEM = STAGES * STAGE + 1024 + 256 + EPI_STG_BYTES;
 };
 
 __device__ __forceinline__ void decode(const TcParams& p, long u, int& b, int& split, int& tm,
@@ -134,14 +135,104 @@ __device__ __forceinline__ void st_elem(void* base, long i, int dt, float v) {
     else reinterpret_cast<bf16*>(base)[i] = __float2bfloat16_rn(v);
 }
 
-// Epilogue of 32 consecutive columns n0.. of one row.
+// Warp-cooperative row I/O.  Lane i holds 32 consecutive columns of row r0 + i
+// (rows ld elements apart, lane 0's first element at off0).  Going through the
+// warp's staging buffer (swizzled by 16-byte chunk, conflict-free), every global
+// access instruction covers whole 128-byte (fp32) or 64-byte (bf16) row segments,
+// instead of 32 separate 16-byte pieces of 32 rows.
+__device__ __forceinline__ void wst32(uint8_t* stg, void* base, long off0, long ld, int dt, const float* v) {
+    const int lane = threadIdx.x & 31;
+    if (dt == NC_FP32) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        __syncwarp();
+        float* out = reinterpret_cast<float*>(base) + off0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3), c = lane & 7;
+            *reinterpret_cast<float4*>(out + (long)r * ld + 4 * c) =
+                *reinterpret_cast<const float4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * c + 2 * e], v[8 * c + 2 * e + 1]);
+                w[e] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        __syncwarp();
+        bf16* out = reinterpret_cast<bf16*>(base) + off0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 8 * i + (lane >> 2), c = lane & 3;
+            *reinterpret_cast<uint4*>(out + (long)r * ld + 8 * c) =
+                *reinterpret_cast<const uint4*>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+        }
+    }
+    __syncwarp();
+}
+
+// Pieces of wst32's bf16 path: stage_bf16x16 puts 16 values (columns 16h..16h+15)
+// of this lane's row into a 32 x 32 bf16 staging block; flush_bf16 writes the
+// block out (rows ld elements apart, lane 0's row at off0).
+__device__ __forceinline__ void stage_bf16x16(uint8_t* stg, int h, const float* v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {
+        const int c = 2 * h + c2;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 x = __floats2bfloat162_rn(v[8 * c2 + 2 * e], v[8 * c2 + 2 * e + 1]);
+            w[e] = *reinterpret_cast<uint32_t*>(&x);
+        }
+        *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+__device__ __forceinline__ void flush_bf16(const uint8_t* stg, void* base, long off0, long ld) {
+    const int lane = threadIdx.x & 31;
+    __syncwarp();
+    bf16* out = reinterpret_cast<bf16*>(base) + off0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 8 * i + (lane >> 2), c = lane & 3;
+        *reinterpret_cast<uint4*>(out + (long)r * ld + 8 * c) =
+            *reinterpret_cast<const uint4*>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+    }
+    __syncwarp();
+}
+__device__ __forceinline__ void st16_bf16(bf16* dst, const float* v) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 x = __floats2bfloat162_rn(v[8 * c + 2 * e], v[8 * c + 2 * e + 1]);
+            w[e] = *reinterpret_cast<uint32_t*>(&x);
+        }
+        reinterpret_cast<uint4*>(dst)[c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Epilogue of 32 consecutive columns n0.. of one row.  coop: every lane of the
+// warp holds a valid row (consecutive rows) and the 32 columns are in range, so
+// the warp-cooperative loads / stores apply (all lanes take this path together).
 __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, int row, int n0,
-                                           float* v) {
+                                           float* v, uint8_t* stg, bool coop) {
+    const int lane = threadIdx.x & 31;
     const bool full = n0 + 32 <= p.N;
     const int nv = full ? 32 : p.N - n0;
     if (p.ws) {
         const long i = ((long)(split * p.batch + b) * p.M + row) * p.N + n0;
-        if (full) st32(p.ws, i, NC_FP32, v);
+        if (coop) wst32(stg, p.ws, i - (long)lane * p.N, p.N, NC_FP32, v);
+        else if (full) st32(p.ws, i, NC_FP32, v);
         else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) if (j < nv) p.ws[i + j] = v[j];
@@ -153,7 +244,8 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
     const long ci = (long)b * p.sC + (long)row * p.ldc + n0;
     const long ai = (long)b * p.sAux + (long)row * p.ldaux + n0;
     if (p.epi == EPI_STORE) {
-        if (p.aux && p.beta != 0.f) {
+        const bool with_aux = p.aux && p.beta != 0.f;
+        if (with_aux) {
             float a[32];
             if (full) ld32(p.aux, ai, p.aux_dtype, a);
             else {
@@ -163,39 +255,36 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] += p.beta * a[j];
         }
-        if (full) st32(p.C, ci, p.c_dtype, v);
+        if (coop && !with_aux) wst32(stg, p.C, ci - (long)lane * p.ldc, p.ldc, p.c_dtype, v);
+        else if (full) st32(p.C, ci, p.c_dtype, v);
         else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) if (j < nv) st_elem(p.C, ci + j, p.c_dtype, v[j]);
         }
     } else if (p.epi == EPI_RELU2) {
-        float a[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const float r = fmaxf(v[j], 0.f);
-            a[j] = r * r;
+            v[j] = r * r;
         }
-        if (full) {
-            st32(p.C, ci, p.c_dtype, v);
-            st32(p.C2, ci, p.c_dtype, a);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (j < nv) {
-                    st_elem(p.C, ci + j, p.c_dtype, v[j]);
-                    st_elem(p.C2, ci + j, p.c_dtype, a[j]);
-                }
-            }
-        }
-    } else {  // EPI_RELU2_BWD: dh = da * 2 relu(h)
-        float h[32];
-        if (full) ld32(p.aux, ai, p.aux_dtype, h);
+        if (coop) wst32(stg, p.C, ci - (long)lane * p.ldc, p.ldc, p.c_dtype, v);
+        else if (full) st32(p.C, ci, p.c_dtype, v);
         else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) h[j] = j < nv ? ld_elem(p.aux, ai + j, p.aux_dtype) : 0.f;
+            for (int j = 0; j < 32; ++j) if (j < nv) st_elem(p.C, ci + j, p.c_dtype, v[j]);
         }
+    } else {  // EPI_RELU2_BWD: dh = da * 2 relu(h) = da * 2 sqrt(a)
+        {
+            float a[32];
+            if (full) ld32(p.aux, ai, p.aux_dtype, a);
+            else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= 2.f * fmaxf(h[j], 0.f);
+                for (int j = 0; j < 32; ++j) a[j] = j < nv ? ld_elem(p.aux, ai + j, p.aux_dtype) : 0.f;
+            }
+            // 2 relu(h) = 2 sqrt(a); a * rsqrt(a) (a > 0) is accurate far beyond bf16
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= a[j] > 0.f ? 2.f * a[j] * rsqrtf(a[j]) : 0.f;
+        }
         if (full) st32(p.C, ci, p.c_dtype, v);
         else {
 #pragma unroll
@@ -208,37 +297,53 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
 // columns of group g (the first or second half of the tile).
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int split, int row, int tn,
-                                              uint32_t tbase, int g) {
+                                              uint32_t tbase, int g, uint8_t* stg) {
+    const int lane = threadIdx.x & 31;
+    const bool rows_ok = __all_sync(0xffffffffu, row < p.M);
     if (p.epi == EPI_ROPE) {
-        // chunk pairs (a, a+2) hold head-dim pairs (j, j+64) of one 128-wide head
+        // chunk pairs (a, a+2) hold head-dim pairs (j, j+64) of one 128-wide head; each
+        // is done in two 16-column halves (bounded registers), staged for coalesced stores
+        uint8_t* stg_b = stg + 2048;
 #pragma unroll 1
         for (int pr = g * (BN / 128); pr < (g + 1) * (BN / 128); ++pr) {
             const int a = (pr >> 1) * 4 + (pr & 1);
-            uint32_t ra[32], rb[32];
-            tc::tmem_ld32(tbase + a * 32, ra);
-            tc::tmem_ld32(tbase + (a + 2) * 32, rb);
-            tc::tmem_wait_ld();
             const int na = tn * BN + a * 32;
-            if (row < p.M && na < p.N) {
-                float va[32], vb[32];
+            const bool live = row < p.M && na < p.N;
+            const long ci = (long)b * p.sC + (long)row * p.ldc + na;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    va[j] = __uint_as_float(ra[j]) * p.alpha;
-                    vb[j] = __uint_as_float(rb[j]) * p.alpha;
+            for (int hh = 0; hh < 2; ++hh) {
+                float va[16], vb[16];
+                tc::tmem_ld16(tbase + a * 32 + 16 * hh, reinterpret_cast<uint32_t*>(va));
+                tc::tmem_ld16(tbase + (a + 2) * 32 + 16 * hh, reinterpret_cast<uint32_t*>(vb));
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    va[j] *= p.alpha;
+                    vb[j] *= p.alpha;
                 }
-                if (na < p.rope_cols) {
-                    const float2* cs = p.rope + (long)(row % p.rope_T) * 64 + (pr & 1) * 32;
+                if (live && na < p.rope_cols) {
+                    // pair-major table: the warp's 32 rows (consecutive positions) read
+                    // 256 contiguous bytes per pair
+                    const float2* cs = p.rope + (long)((pr & 1) * 32 + 16 * hh) * p.rope_ld + (row % p.rope_T);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float2 c = __ldg(cs + j);
+                    for (int j = 0; j < 16; ++j) {
+                        const float2 c = __ldg(cs + (long)j * p.rope_ld);
                         const float x1 = va[j], x2 = vb[j];
                         va[j] = x1 * c.x - x2 * c.y;
                         vb[j] = x2 * c.x + x1 * c.y;
                     }
                 }
-                const long ci = (long)b * p.sC + (long)row * p.ldc + na;
-                st32(p.C, ci, p.c_dtype, va);
-                st32(p.C, ci + 64, p.c_dtype, vb);
+                if (rows_ok) {
+                    stage_bf16x16(stg, hh, va);
+                    stage_bf16x16(stg_b, hh, vb);
+                } else if (live) {
+                    st16_bf16(reinterpret_cast<bf16*>(p.C) + ci + 16 * hh, va);
+                    st16_bf16(reinterpret_cast<bf16*>(p.C) + ci + 64 + 16 * hh, vb);
+                }
+            }
+            if (rows_ok && na < p.N) {
+                flush_bf16(stg, p.C, ci - (long)lane * p.ldc, p.ldc);
+                flush_bf16(stg_b, p.C, ci + 64 - (long)lane * p.ldc, p.ldc);
             }
         }
     } else if (p.epi == EPI_DELTA) {
@@ -247,20 +352,22 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
         float dot = 0.f;
 #pragma unroll 1
         for (int c = g * (BN / 64); c < (g + 1) * (BN / 64); ++c) {
-            uint32_t r[32];
-            tc::tmem_ld32(tbase + c * 32, r);
+            float v[32];
+            tc::tmem_ld32(tbase + c * 32, reinterpret_cast<uint32_t*>(v));
             tc::tmem_wait_ld();
             const int n0 = tn * BN + c * 32;
             if (row < p.M && n0 < p.N) {
-                float v[32], o[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    v[j] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[j]) * p.alpha));
+                for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * p.alpha));
                 const long ci = (long)b * p.sC + (long)row * p.ldc + n0;
-                st32(p.C, ci, NC_BF16, v);
-                ld32(p.aux, (long)b * p.sAux + (long)row * p.ldaux + n0, NC_BF16, o);
+                const long ai = (long)b * p.sAux + (long)row * p.ldaux + n0;
+                {
+                    float o[32];
+                    st32(p.C, ci, NC_BF16, v);
+                    ld32(p.aux, ai, NC_BF16, o);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) dot = fmaf(v[j], o[j], dot);
+                    for (int j = 0; j < 32; ++j) dot = fmaf(v[j], o[j], dot);
+                }
                 if ((c & 3) == 3) {
                     const int hh = n0 / 128, t = row % p.rope_T, bb = row / p.rope_T;
                     p.delta[((long)bb * (p.N / 128) + hh) * p.rope_T + t] = dot;
@@ -271,15 +378,12 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
     } else
 #pragma unroll 1
     for (int c = g * (BN / 64); c < (g + 1) * (BN / 64); ++c) {
-        uint32_t r[32];
-        tc::tmem_ld32(tbase + c * 32, r);
+        float v[32];
+        tc::tmem_ld32(tbase + c * 32, reinterpret_cast<uint32_t*>(v));
         tc::tmem_wait_ld();
         const int n0 = tn * BN + c * 32;
         if (row < p.M && n0 < p.N) {
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-            epilogue32(p, b, split, row, n0, v);
+            epilogue32(p, b, split, row, n0, v, stg, rows_ok && n0 + 32 <= p.N);
         }
     }
 }
@@ -409,6 +513,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3, g = (warp - 2) >> 2;
+        uint8_t* stg = smem + S * C::STAGE + 256 + (warp - 2) * EPI_STG;
         int acc = 0;
         uint32_t aph = 0;
         for (long u = blockIdx.x; u < p.units; u += gridDim.x) {
@@ -418,7 +523,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_after();
             const int row = tm * BM + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            epilogue_tile<BN>(p, b, split, row, tn, tbase, g);
+            epilogue_tile<BN>(p, b, split, row, tn, tbase, g, stg);
             tc::fence_before();
             tc::mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -447,7 +552,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 constexpr int P_BN = 256, P_STAGES = 6;
 constexpr int P_A_BYTES = 128 * BK * 2, P_B_BYTES = 128 * BK * 2;
 constexpr int P_STAGE = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM = P_STAGES * P_STAGE + 1024 + 256;
+constexpr int P_SMEM = P_STAGES * P_STAGE + 1024 + 256 + EPI_STG_BYTES;
 
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -566,6 +671,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue (both CTAs)
         const int q = warp & 3, g = (warp - 2) >> 2;
+        uint8_t* stg = smem + S * P_STAGE + 256 + (warp - 2) * EPI_STG;
         const uint32_t tempty_leader = tc::mapa(tc::smem_u32(&tempty[0]), 0);
         int acc = 0;
         uint32_t aph = 0;
@@ -576,7 +682,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::fence_after();
             const int row = tm * 256 + (int)rank * 128 + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_BN);
-            epilogue_tile<P_BN>(p, b, split, row, tn, tbase, g);
+            epilogue_tile<P_BN>(p, b, split, row, tn, tbase, g, stg);
             tc::fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(tempty_leader + acc * 8);
@@ -741,10 +847,10 @@ bool gemm_tc_supported(const Gemm& g) {
     if (g.lda % 8 || g.ldb % 8 || g.ldc % 8 || (g.aux && g.ldaux % 8)) return false;
     if (g.batch > 1 && (g.sA % 8 || g.sB % 8)) return false;
     if ((uintptr_t)g.A % 16 || (uintptr_t)g.B % 16 || (uintptr_t)g.C % 16) return false;
-    if (g.C2 && (uintptr_t)g.C2 % 16) return false;
     if (g.aux && (uintptr_t)g.aux % 16) return false;
     if (g.N % 8) return false;
-    if (g.epi == EPI_ROPE && (g.N % 128 || !g.rope || g.rope_T <= 0 || g.c_dtype != NC_BF16)) return false;
+    if (g.epi == EPI_ROPE && (g.N % 128 || !g.rope || g.rope_T <= 0 || g.rope_ld < g.rope_T ||
+                              g.c_dtype != NC_BF16)) return false;
     if (g.epi == EPI_DELTA && (g.N % 128 || g.N < 256 || !g.delta || !g.aux || g.rope_T <= 0 || g.c_dtype != NC_BF16 ||
                                g.aux_dtype != NC_BF16 || g.batch != 1))
         return false;
@@ -778,10 +884,10 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     p.units = (long)p.tiles_m * p.tiles_n * p.splits * g.batch;
     p.C = g.C; p.ldc = g.ldc; p.sC = g.sC; p.c_dtype = g.c_dtype;
     p.aux = g.aux; p.ldaux = g.ldaux; p.sAux = g.sAux; p.aux_dtype = g.aux_dtype;
-    p.C2 = g.C2; p.alpha = g.alpha; p.beta = g.beta; p.epi = g.epi;
+    p.alpha = g.alpha; p.beta = g.beta; p.epi = g.epi;
     p.ws = p.splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
     p.flag = g_gemm_flag;
-    p.rope = g.rope; p.rope_T = g.rope_T; p.rope_cols = g.rope_cols; p.delta = g.delta;
+    p.rope = g.rope; p.rope_T = g.rope_T; p.rope_cols = g.rope_cols; p.rope_ld = g.rope_ld; p.delta = g.delta;
 
     CUtensorMap ma, mb;
     if (!g.a_t) NC_TRY(make_map(&ma, g.A, g.K, g.M, g.batch, g.lda, g.sA, 64, BM));

@@ -12,8 +12,8 @@ namespace nc {
 // C = alpha * op(A) op(B)^T (+ epilogue), op(A) [M, K], op(B) [N, K].
 enum EpiKind {
     EPI_STORE = 0,      // C = alpha*acc + beta*aux            (aux may alias C)
-    EPI_RELU2 = 1,      // C = alpha*acc (pre-activation h), C2 = relu(h)^2
-    EPI_RELU2_BWD = 2,  // C = alpha*acc * 2*relu(aux)          (aux = h)
+    EPI_RELU2 = 1,      // C = relu(alpha*acc)^2 (the activation a; h itself is not kept)
+    EPI_RELU2_BWD = 2,  // C = alpha*acc * 2*sqrt(aux)          (aux = a = relu(h)^2, so 2 sqrt(a) = 2 relu(h))
     EPI_ROPE = 3,       // C = alpha*acc with columns < rope_cols rotated by RoPE (head dim 128)
     EPI_DELTA = 4,      // C = alpha*acc (bf16) and delta[b, h, t] = sum over head h of bf16(C) * aux
 };
@@ -25,11 +25,11 @@ struct Gemm {
     int in_dtype = NC_BF16;
     void* C = nullptr; long ldc = 0, sC = 0; int c_dtype = NC_BF16;
     const void* aux = nullptr; long ldaux = 0, sAux = 0; int aux_dtype = NC_BF16;
-    void* C2 = nullptr;
     float alpha = 1.f, beta = 0.f;
     int epi = EPI_STORE;
-    const float2* rope = nullptr;  // EPI_ROPE: [rope_T, 64] (cos, sin); row position = row % rope_T
-    int rope_T = 0, rope_cols = 0;
+    const float2* rope = nullptr;  // EPI_ROPE: (cos, sin) of pair j at position t is rope[j * rope_ld + t];
+    int rope_T = 0, rope_cols = 0; //   row position = row % rope_T
+    int rope_ld = 0;
     float* delta = nullptr;        // EPI_DELTA: [B, N/128, rope_T] row statistics (row = b*rope_T + t)
 };
 
@@ -55,7 +55,7 @@ int rmsnorm_backward(const T* dy, const T* y, const float* r, const float* g_in,
                      float* g_out, T* gT, int M, int d, cudaStream_t s);
 // in place on the q and k thirds of qkv rows (row stride ld): sign +1 fwd, -1 bwd
 template <typename T>
-int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* table, float sign,
+int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* table, int table_ld, float sign,
                cudaStream_t s);
 // logits [M, V] -> dlogits in place; nll [M]
 template <typename T>
@@ -80,8 +80,9 @@ int embed_backward(const int32_t* tok, const float* g, float* dwte, int M, int d
 template <typename T>
 int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ldo, float* lse,
                       int B, int T_, int H, int D, cudaStream_t s);
-// rope: optional RoPE table; when the kernel can rotate dq, dk back itself it
-// does so and sets *rope_done = 1 (else the caller applies the inverse RoPE).
+// rope: optional RoPE table ((cos, sin) of pair j at position t at rope[j * rope_ld + t]);
+// when the kernel can rotate dq, dk back itself it does so and sets *rope_done = 1
+// (else the caller applies the inverse RoPE).
 // delta_ready: delta already holds dO.O per row (computed by the producer of dO)
 // ds: optional scratch of attention_ds_bytes(B, T_, H) bytes; with it the bf16
 // head-dim-128 path keeps dS from the dK/dV pass and forms dq as a plain product
@@ -90,7 +91,8 @@ template <typename T>
 int attention_backward(const T* q, const T* k, const T* v, long ld, const T* o, const T* dout,
                        long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
                        int B, int T_, int H, int D, cudaStream_t s, const float2* rope = nullptr,
-                       int* rope_done = nullptr, bool delta_ready = false, void* ds = nullptr);
+                       int rope_ld = 0, int* rope_done = nullptr, bool delta_ready = false,
+                       void* ds = nullptr);
 // bytes of the dS scratch above (0 where it would not be used)
 size_t attention_ds_bytes(int B, int T_, int H, int D);
 

@@ -108,7 +108,7 @@ __global__ void rmsnorm_bwd_kernel(const T* dy, const T* y, const float* r, cons
 // Rotates pairs (j, j + Dh/2) of every q and k head by sign * angle(t, j).
 template <typename T>
 __global__ void rope_kernel(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* table,
-                            float sign) {
+                            int table_ld, float sign) {
     const int half = Dh / 2;
     long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     long total = (long)M * H * half;
@@ -118,7 +118,7 @@ __global__ void rope_kernel(T* qkv, long ld, int M, int T_, int H, int Dh, const
     int h = rh % H;
     long row = rh / H;
     int t = row % T_;
-    float2 cs = table[(long)t * half + j];
+    float2 cs = table[(long)j * table_ld + t];
     float c = cs.x, sn = sign * cs.y;
     T* base = qkv + row * ld + (long)h * Dh;
 #pragma unroll
@@ -460,11 +460,11 @@ int rmsnorm_backward(const T* dy, const T* y, const float* r, const float* g_in,
 }
 
 template <typename T>
-int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* table, float sign,
+int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* table, int table_ld, float sign,
                cudaStream_t s) {
     long total = (long)M * H * (Dh / 2);
     if (total <= 0) return NC_OK;
-    rope_kernel<T><<<ceil_div(total, 256), 256, 0, s>>>(qkv, ld, M, T_, H, Dh, table, sign);
+    rope_kernel<T><<<ceil_div(total, 256), 256, 0, s>>>(qkv, ld, M, T_, H, Dh, table, table_ld, sign);
     note_launch();
     NC_LAUNCH_CHECK("rope_apply");
     return NC_OK;
@@ -549,7 +549,7 @@ int cast_f32_bf16(const float* x, bf16* y, long n, cudaStream_t s) {
     template int rmsnorm_forward<T>(const float*, T*, float*, int, int, cudaStream_t);          \
     template int rmsnorm_backward<T>(const T*, const T*, const float*, const float*, float*, \
                                      T*, int, int, cudaStream_t);                               \
-    template int rope_apply<T>(T*, long, int, int, int, int, const float2*, float, cudaStream_t); \
+    template int rope_apply<T>(T*, long, int, int, int, int, const float2*, int, float, cudaStream_t); \
     template int cross_entropy<T>(T*, const int32_t*, float*, int, int, float, uint32_t*,       \
                                   cudaStream_t);
 NC_INST(float)
