@@ -32,8 +32,13 @@ namespace {
 
 constexpr int BM = 128, BK = 64, NTHREADS = 320, GROUP_M = 8;
 constexpr int EPI_WARPS = 8;   // two groups of four, each owns half the tile columns
-constexpr int EPI_STG = 4096;  // per epilogue warp: 32 rows x 32 fp32 staging for coalesced stores
+// Per epilogue warp: two 4 KB buffers, each a 32 x 32 block (fp32 or bf16) laid out with
+// the 128-byte (fp32) / 64-byte (bf16) TMA swizzle.  They receive the auxiliary matrix by
+// TMA one chunk ahead and then serve as the staging of the coalesced store.
+constexpr int EPI_BUF = 4096;
+constexpr int EPI_STG = 2 * EPI_BUF;
 constexpr int EPI_STG_BYTES = EPI_WARPS * EPI_STG;
+constexpr int BAR_BYTES = 512;   // mbarriers, TMEM slot, abort flag (after the staging)
 
 struct TcParams {
     int M, N, K, batch;
@@ -48,15 +53,16 @@ struct TcParams {
     const float2* rope;   // (cos, sin) of pair j at position t: rope[j * rope_ld + t]
     int rope_T, rope_cols, rope_ld;
     float* delta;
+    int aux_tma;      // the auxiliary matrix comes through the per-warp TMA buffers
 };
 
 template <int BN> struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int STAGES = BN == 256 ? 3 : 4;
     static constexpr uint32_t TMEM_COLS = 2 * BN;
-    static constexpr int SMEM = STAGES * STAGE + 1024 + 256 + EPI_STG_BYTES;
+    static constexpr int SMEM = STAGES * STAGE + 1024 + BAR_BYTES + EPI_STG_BYTES;
 };
 
 __device__ __forceinline__ void decode(const TcParams& p, long u, int& b, int& split, int& tm,
@@ -221,11 +227,78 @@ __device__ __forceinline__ void st16_bf16(bf16* dst, const float* v) {
     }
 }
 
+// The auxiliary-matrix pipeline of one epilogue warp: 32 x 32 blocks come in by TMA
+// into its two buffers, one chunk ahead, in issue order.
+struct XPipe {
+    uint8_t* buf;       // 2 x EPI_BUF
+    uint64_t* bar;      // 2 mbarriers (arrival count 1)
+    uint32_t phase;     // bit k: parity of buffer k's next completion
+    int issue, head;    // buffer of the next issue / of the oldest outstanding block
+    int pending;        // bit k: buffer k holds an issued, unconsumed block
+};
+
+__device__ __forceinline__ void x_issue(XPipe& x, const CUtensorMap* m, int n0, int row0, int b,
+                                        uint32_t bytes) {
+    const int k = x.issue;
+    x.issue ^= 1;
+    x.pending |= 1 << k;
+    __syncwarp();   // every lane is done with buffer k (aux read or store staging)
+    if ((threadIdx.x & 31) == 0) {
+        tc::fence_async_smem();   // those generic-proxy accesses before the TMA write
+        tc::mbar_expect_tx(&x.bar[k], bytes);
+        tc::tma_load_3d(x.buf + k * EPI_BUF, m, &x.bar[k], n0, row0, b);
+    }
+}
+
+// The oldest outstanding block, once it has landed (null if the CTA aborted).
+__device__ __forceinline__ uint8_t* x_wait(XPipe& x, volatile int* abort) {
+    const int k = x.head;
+    if (!tc::mbar_wait_warp(&x.bar[k], (x.phase >> k) & 1, abort)) return nullptr;
+    x.head ^= 1;
+    x.phase ^= 1u << k;
+    x.pending &= ~(1 << k);
+    return x.buf + k * EPI_BUF;
+}
+
+// After an abort: let issued copies land before the CTA exits.
+__device__ __forceinline__ void x_drain(XPipe& x) {
+    if ((threadIdx.x & 31) != 0) return;
+    for (int k = 0; k < 2; ++k)
+        if (x.pending & (1 << k)) tc::mbar_wait_drain(&x.bar[k], (x.phase >> k) & 1);
+}
+
+// This lane's 32 values of a TMA-loaded block (the layout of wst32's staging).
+__device__ __forceinline__ void x_row(const uint8_t* xb, int dt, float* a) {
+    const int lane = threadIdx.x & 31;
+    if (dt == NC_FP32) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float4 f = *reinterpret_cast<const float4*>(xb + lane * 128 + ((c ^ (lane & 7)) << 4));
+            a[4 * c] = f.x; a[4 * c + 1] = f.y; a[4 * c + 2] = f.z; a[4 * c + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 u = *reinterpret_cast<const uint4*>(xb + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+                a[8 * c + 2 * e] = f.x;
+                a[8 * c + 2 * e + 1] = f.y;
+            }
+        }
+    }
+    __syncwarp();   // the block is read before the buffer is reused as store staging
+}
+
 // Epilogue of 32 consecutive columns n0.. of one row.  coop: every lane of the
 // warp holds a valid row (consecutive rows) and the 32 columns are in range, so
 // the warp-cooperative loads / stores apply (all lanes take this path together).
+// xa: this row's 32 aux values, already read from the chunk's TMA block (null: the
+// aux matrix is read per thread here).
 __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, int row, int n0,
-                                           float* v, uint8_t* stg, bool coop) {
+                                           float* v, uint8_t* stg, bool coop, const float* xa) {
     const int lane = threadIdx.x & 31;
     const bool full = n0 + 32 <= p.N;
     const int nv = full ? 32 : p.N - n0;
@@ -245,7 +318,10 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
     const long ai = (long)b * p.sAux + (long)row * p.ldaux + n0;
     if (p.epi == EPI_STORE) {
         const bool with_aux = p.aux && p.beta != 0.f;
-        if (with_aux) {
+        if (with_aux && xa) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += p.beta * xa[j];
+        } else if (with_aux) {
             float a[32];
             if (full) ld32(p.aux, ai, p.aux_dtype, a);
             else {
@@ -255,7 +331,7 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] += p.beta * a[j];
         }
-        if (coop && !with_aux) wst32(stg, p.C, ci - (long)lane * p.ldc, p.ldc, p.c_dtype, v);
+        if (coop && (!with_aux || xa)) wst32(stg, p.C, ci - (long)lane * p.ldc, p.ldc, p.c_dtype, v);
         else if (full) st32(p.C, ci, p.c_dtype, v);
         else {
 #pragma unroll
@@ -274,18 +350,22 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
             for (int j = 0; j < 32; ++j) if (j < nv) st_elem(p.C, ci + j, p.c_dtype, v[j]);
         }
     } else {  // EPI_RELU2_BWD: dh = da * 2 relu(h) = da * 2 sqrt(a)
-        {
+        // 2 relu(h) = 2 sqrt(a); a * rsqrt(a) (a > 0) is accurate far beyond bf16
+        if (xa) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= xa[j] > 0.f ? 2.f * xa[j] * rsqrtf(xa[j]) : 0.f;
+        } else {
             float a[32];
             if (full) ld32(p.aux, ai, p.aux_dtype, a);
             else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) a[j] = j < nv ? ld_elem(p.aux, ai + j, p.aux_dtype) : 0.f;
             }
-            // 2 relu(h) = 2 sqrt(a); a * rsqrt(a) (a > 0) is accurate far beyond bf16
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] *= a[j] > 0.f ? 2.f * a[j] * rsqrtf(a[j]) : 0.f;
         }
-        if (full) st32(p.C, ci, p.c_dtype, v);
+        if (coop && xa) wst32(stg, p.C, ci - (long)lane * p.ldc, p.ldc, p.c_dtype, v);
+        else if (full) st32(p.C, ci, p.c_dtype, v);
         else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) if (j < nv) st_elem(p.C, ci + j, p.c_dtype, v[j]);
@@ -295,11 +375,15 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
 
 // The epilogue of one accumulator tile for one row (this thread's TMEM lane),
 // columns of group g (the first or second half of the tile).
+// With p.aux_tma the block of the first chunk was issued by the caller; each chunk
+// issues the next one before waiting for its own.
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int split, int row, int tn,
-                                              uint32_t tbase, int g, uint8_t* stg) {
+                                              uint32_t tbase, int g, uint8_t* stg, XPipe& x,
+                                              const CUtensorMap* mx, volatile int* abort) {
     const int lane = threadIdx.x & 31;
     const bool rows_ok = __all_sync(0xffffffffu, row < p.M);
+    const uint32_t xbytes = p.aux_dtype == NC_FP32 ? 4096u : 2048u;
     if (p.epi == EPI_ROPE) {
         // chunk pairs (a, a+2) hold head-dim pairs (j, j+64) of one 128-wide head; each
         // is done in two 16-column halves (bounded registers), staged for coalesced stores
@@ -356,17 +440,24 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
             tc::tmem_ld32(tbase + c * 32, reinterpret_cast<uint32_t*>(v));
             tc::tmem_wait_ld();
             const int n0 = tn * BN + c * 32;
+            const uint8_t* xb = nullptr;
+            float o[32];
+            if (p.aux_tma) {
+                if (c + 1 < (g + 1) * (BN / 64)) x_issue(x, mx, n0 + 32, row - lane, b, xbytes);
+                if (!(xb = x_wait(x, abort))) break;
+                x_row(xb, NC_BF16, o);
+            }
             if (row < p.M && n0 < p.N) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * p.alpha));
                 const long ci = (long)b * p.sC + (long)row * p.ldc + n0;
                 const long ai = (long)b * p.sAux + (long)row * p.ldaux + n0;
                 {
-                    float o[32];
-                    st32(p.C, ci, NC_BF16, v);
-                    ld32(p.aux, ai, NC_BF16, o);
+                    if (!xb) ld32(p.aux, ai, NC_BF16, o);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dot = fmaf(v[j], o[j], dot);
+                    if (xb && rows_ok) wst32(const_cast<uint8_t*>(xb), p.C, ci - (long)lane * p.ldc, p.ldc, NC_BF16, v);
+                    else st32(p.C, ci, NC_BF16, v);
                 }
                 if ((c & 3) == 3) {
                     const int hh = n0 / 128, t = row % p.rope_T, bb = row / p.rope_T;
@@ -382,8 +473,16 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
         tc::tmem_ld32(tbase + c * 32, reinterpret_cast<uint32_t*>(v));
         tc::tmem_wait_ld();
         const int n0 = tn * BN + c * 32;
+        const uint8_t* xb = nullptr;
+        float a[32];
+        if (p.aux_tma) {
+            if (c + 1 < (g + 1) * (BN / 64)) x_issue(x, mx, n0 + 32, row - lane, b, xbytes);
+            if (!(xb = x_wait(x, abort))) break;
+            x_row(xb, p.aux_dtype, a);
+        }
         if (row < p.M && n0 < p.N) {
-            epilogue32(p, b, split, row, n0, v, stg, rows_ok && n0 + 32 <= p.N);
+            epilogue32(p, b, split, row, n0, v, xb ? const_cast<uint8_t*>(xb) : stg,
+                       rows_ok && n0 + 32 <= p.N, xb ? a : nullptr);
         }
     }
 }
@@ -391,19 +490,21 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmX, const TcParams p) {
     using C = Cfg<BN>;
     constexpr int S = C::STAGES;
     constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, A_MN, B_MN);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE);
+    uint8_t* epi_smem = smem + S * C::STAGE;   // 1024-aligned: the swizzled TMA blocks need it
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi_smem + EPI_STG_BYTES);
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* xbar = drain + 1;   // [EPI_WARPS][2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2 * EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -417,10 +518,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(&tempty[a], EPI_WARPS * 32);
         }
         tc::mbar_init(drain, 1);
+        for (int i = 0; i < 2 * EPI_WARPS; ++i) tc::mbar_init(&xbar[i], 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch(&tmA);
         tc::tma_prefetch(&tmB);
+        if (p.aux_tma) tc::tma_prefetch(&tmX);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -513,22 +616,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3, g = (warp - 2) >> 2;
-        uint8_t* stg = smem + S * C::STAGE + 256 + (warp - 2) * EPI_STG;
+        XPipe x{epi_smem + (warp - 2) * EPI_STG, xbar + 2 * (warp - 2), 0u, 0, 0, 0};
+        const uint32_t xbytes = p.aux_dtype == NC_FP32 ? 4096u : 2048u;
         int acc = 0;
         uint32_t aph = 0;
         for (long u = blockIdx.x; u < p.units; u += gridDim.x) {
             int b, split, tm, tn;
             decode(p, u, b, split, tm, tn);
+            const int row = tm * BM + q * 32 + lane;
+            // the first aux block of this tile comes in while the tile's MMAs run
+            if (p.aux_tma) x_issue(x, &tmX, tn * BN + g * (BN / 2), row - lane, b, xbytes);
             if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
-            const int row = tm * BM + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            epilogue_tile<BN>(p, b, split, row, tn, tbase, g, stg);
+            epilogue_tile<BN>(p, b, split, row, tn, tbase, g, x.buf, x, &tmX, abort_flag);
             tc::fence_before();
             tc::mbar_arrive(&tempty[acc]);
             acc ^= 1;
             if (acc == 0) aph ^= 1;
         }
+        if (*abort_flag) x_drain(x);
     }
 
     tc::fence_before();
@@ -549,26 +656,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // CTAs' TMA loads complete on the leader's full barrier; the leader's commits
 // multicast to both CTAs' empty / accumulator-full barriers; both CTAs'
 // epilogue warps release an accumulator on the leader's barrier.
-constexpr int P_BN = 256, P_STAGES = 6;
+constexpr int P_BN = 256, P_STAGES = 5;
 constexpr int P_A_BYTES = 128 * BK * 2, P_B_BYTES = 128 * BK * 2;
 constexpr int P_STAGE = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM = P_STAGES * P_STAGE + 1024 + 256 + EPI_STG_BYTES;
+constexpr int P_SMEM = P_STAGES * P_STAGE + 1024 + BAR_BYTES + EPI_STG_BYTES;
 
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const TcParams p) {
+                    const __grid_constant__ CUtensorMap tmX, const TcParams p) {
     constexpr int S = P_STAGES;
     constexpr uint32_t IDESC = tc::idesc_bf16(256, P_BN, A_MN, B_MN);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * P_STAGE);
+    uint8_t* epi_smem = smem + S * P_STAGE;   // 1024-aligned: the swizzled TMA blocks need it
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi_smem + EPI_STG_BYTES);
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* xbar = drain + 1;   // [EPI_WARPS][2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2 * EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -584,10 +693,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(&tempty[a], 2 * EPI_WARPS);   // every epilogue warp of both CTAs
         }
         tc::mbar_init(drain, 1);
+        for (int i = 0; i < 2 * EPI_WARPS; ++i) tc::mbar_init(&xbar[i], 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch(&tmA);
         tc::tma_prefetch(&tmB);
+        if (p.aux_tma) tc::tma_prefetch(&tmX);
     }
     if (warp == 1) {
         tc::tmem_alloc2(tmem_slot, 512);
@@ -671,24 +782,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue (both CTAs)
         const int q = warp & 3, g = (warp - 2) >> 2;
-        uint8_t* stg = smem + S * P_STAGE + 256 + (warp - 2) * EPI_STG;
+        XPipe x{epi_smem + (warp - 2) * EPI_STG, xbar + 2 * (warp - 2), 0u, 0, 0, 0};
+        const uint32_t xbytes = p.aux_dtype == NC_FP32 ? 4096u : 2048u;
         const uint32_t tempty_leader = tc::mapa(tc::smem_u32(&tempty[0]), 0);
         int acc = 0;
         uint32_t aph = 0;
         for (long u = cluster; u < p.units; u += nclusters) {
             int b, split, tm, tn;
             decode(p, u, b, split, tm, tn);
+            const int row = tm * 256 + (int)rank * 128 + q * 32 + lane;
+            // the first aux block of this tile comes in while the tile's MMAs run
+            if (p.aux_tma) x_issue(x, &tmX, tn * P_BN + g * (P_BN / 2), row - lane, b, xbytes);
             if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
-            const int row = tm * 256 + (int)rank * 128 + q * 32 + lane;
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_BN);
-            epilogue_tile<P_BN>(p, b, split, row, tn, tbase, g, stg);
+            epilogue_tile<P_BN>(p, b, split, row, tn, tbase, g, x.buf, x, &tmX, abort_flag);
             tc::fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(tempty_leader + acc * 8);
             acc ^= 1;
             if (acc == 0) aph ^= 1;
         }
+        if (*abort_flag) x_drain(x);
     }
 
     tc::fence_before();
@@ -717,7 +832,8 @@ __global__ void splitk_reduce_kernel(const float* ws, int splits, int batch, int
 }
 
 template <int BN, bool A_MN, bool B_MN>
-int launch(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cudaStream_t s) {
+int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, const TcParams& p,
+           cudaStream_t s) {
     using C = Cfg<BN>;
     static bool attr = false;
     if (!attr) {
@@ -727,14 +843,15 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cuda
         attr = true;
     }
     const long grid = p.units < num_sms() ? p.units : num_sms();
-    gemm_tc_kernel<BN, A_MN, B_MN><<<(int)grid, NTHREADS, C::SMEM, s>>>(ma, mb, p);
+    gemm_tc_kernel<BN, A_MN, B_MN><<<(int)grid, NTHREADS, C::SMEM, s>>>(ma, mb, mx, p);
     note_launch();
     NC_LAUNCH_CHECK("gemm_tc");
     return NC_OK;
 }
 
 template <bool A_MN, bool B_MN>
-int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cudaStream_t s) {
+int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, const TcParams& p,
+            cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
         NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN>,
@@ -755,7 +872,7 @@ int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, cud
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    NC_TRY(cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN>, ma, mb, p), "gemm_tc2 launch"));
+    NC_TRY(cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN>, ma, mb, mx, p), "gemm_tc2 launch"));
     note_launch();
     NC_LAUNCH_CHECK("gemm_tc2");
     return NC_OK;
@@ -827,6 +944,28 @@ int make_map(CUtensorMap* m, const void* ptr, long inner, long outer, long batch
     return NC_OK;
 }
 
+// 3-D map of an fp32 / bf16 matrix [batch][outer][inner] for the epilogue's 32 x 32
+// blocks, swizzled so that row r's 16-byte chunk c lands at chunk c ^ (r & 7) (fp32,
+// 128-byte rows) or c ^ ((r >> 1) & 3) (bf16, 64-byte rows).
+int make_map_x(CUtensorMap* m, const void* ptr, int dt, long inner, long outer, long batch, long ld, long bs) {
+    auto fn = encode_fn();
+    if (!fn) return set_error(NC_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const int es = dt == NC_FP32 ? 4 : 2;
+    if (batch <= 1) bs = ld * outer;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)(batch < 1 ? 1 : batch)};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * es, (cuuint64_t)bs * es};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt == NC_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    dt == NC_FP32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(NC_ERR_CUDA, "cuTensorMapEncodeTiled (aux) failed (%d): inner %ld outer %ld ld %ld",
+                         (int)r, inner, outer, ld);
+    return NC_OK;
+}
+
 int num_sms() {
     static int n = 0;
     if (!n) {
@@ -889,28 +1028,38 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     p.flag = g_gemm_flag;
     p.rope = g.rope; p.rope_T = g.rope_T; p.rope_cols = g.rope_cols; p.rope_ld = g.rope_ld; p.delta = g.delta;
 
-    CUtensorMap ma, mb;
+    // the auxiliary matrix by TMA (32 x 32 blocks, 128 / 64-byte swizzle) when the
+    // epilogue reads one and its layout allows the copy
+    CUtensorMap ma, mb, mx;
+    const bool reads_aux = (g.epi == EPI_STORE && g.aux && g.beta != 0.f) || g.epi == EPI_RELU2_BWD ||
+                           g.epi == EPI_DELTA;
+    const int xes = g.aux_dtype == NC_FP32 ? 4 : 2;
+    if (reads_aux && p.splits == 1 && (g.ldaux * xes) % 16 == 0 && (g.batch <= 1 || (g.sAux * xes) % 16 == 0)) {
+        NC_TRY(make_map_x(&mx, g.aux, g.aux_dtype, g.N, g.M, g.batch, g.ldaux, g.sAux));
+        p.aux_tma = 1;
+    }
     if (!g.a_t) NC_TRY(make_map(&ma, g.A, g.K, g.M, g.batch, g.lda, g.sA, 64, BM));
     else        NC_TRY(make_map(&ma, g.A, g.M, g.K, g.batch, g.lda, g.sA, 64, 64));
     if (!g.b_t) NC_TRY(make_map(&mb, g.B, g.K, g.N, g.batch, g.ldb, g.sB, 64, pair ? 128 : bn));
     else        NC_TRY(make_map(&mb, g.B, g.N, g.K, g.batch, g.ldb, g.sB, 64, 64));
+    if (!p.aux_tma) mx = ma;   // unused
 
     int rc;
     if (pair) {
-        if (!g.a_t && !g.b_t) rc = launch2<false, false>(ma, mb, p, s);
-        else if (!g.a_t && g.b_t) rc = launch2<false, true>(ma, mb, p, s);
-        else if (g.a_t && !g.b_t) rc = launch2<true, false>(ma, mb, p, s);
-        else rc = launch2<true, true>(ma, mb, p, s);
+        if (!g.a_t && !g.b_t) rc = launch2<false, false>(ma, mb, mx, p, s);
+        else if (!g.a_t && g.b_t) rc = launch2<false, true>(ma, mb, mx, p, s);
+        else if (g.a_t && !g.b_t) rc = launch2<true, false>(ma, mb, mx, p, s);
+        else rc = launch2<true, true>(ma, mb, mx, p, s);
     } else if (bn == 256) {
-        if (!g.a_t && !g.b_t) rc = launch<256, false, false>(ma, mb, p, s);
-        else if (!g.a_t && g.b_t) rc = launch<256, false, true>(ma, mb, p, s);
-        else if (g.a_t && !g.b_t) rc = launch<256, true, false>(ma, mb, p, s);
-        else rc = launch<256, true, true>(ma, mb, p, s);
+        if (!g.a_t && !g.b_t) rc = launch<256, false, false>(ma, mb, mx, p, s);
+        else if (!g.a_t && g.b_t) rc = launch<256, false, true>(ma, mb, mx, p, s);
+        else if (g.a_t && !g.b_t) rc = launch<256, true, false>(ma, mb, mx, p, s);
+        else rc = launch<256, true, true>(ma, mb, mx, p, s);
     } else {
-        if (!g.a_t && !g.b_t) rc = launch<128, false, false>(ma, mb, p, s);
-        else if (!g.a_t && g.b_t) rc = launch<128, false, true>(ma, mb, p, s);
-        else if (g.a_t && !g.b_t) rc = launch<128, true, false>(ma, mb, p, s);
-        else rc = launch<128, true, true>(ma, mb, p, s);
+        if (!g.a_t && !g.b_t) rc = launch<128, false, false>(ma, mb, mx, p, s);
+        else if (!g.a_t && g.b_t) rc = launch<128, false, true>(ma, mb, mx, p, s);
+        else if (g.a_t && !g.b_t) rc = launch<128, true, false>(ma, mb, mx, p, s);
+        else rc = launch<128, true, true>(ma, mb, mx, p, s);
     }
     NC_TRY(rc);
     if (p.splits > 1) {
