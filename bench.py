@@ -50,9 +50,10 @@ NOMINAL_BF16_TFLOPS = 2250.0
 # copy bandwidth and library bf16 GEMM rates of this GPU pool.
 ROOF = {"gemm": "tensor", "attn_fwd": "tensor", "attn_bwd": "tensor", "muon_ns": "tensor",
         "norm": "hbm", "rope": "hbm", "ce": "hbm", "embed": "hbm", "muon_elem": "hbm", "adamw": "hbm"}
-# dram read+write bytes per launch of the dominant kernel class from the last
-# ncu capture of the current kernel code (profiles/), None when not measured.
-GEMM_TRAFFIC_PER_LAUNCH = None
+# dram read+write bytes per launch site of the dominant kernel class (the step's
+# GEMMs, each with its split-K reduce when it has one) from the last ncu capture
+# of the current GEMM code (profiles/d20_step_launches.md), None when not measured.
+GEMM_TRAFFIC_PER_LAUNCH = 1.224e9
 CPU_SAMPLE_T = 256
 
 
@@ -393,7 +394,7 @@ def main():
     roofline = None
     if g:
         kms, n, fl, by = L.nc_profile_read(m.h, 0)
-        roofline = {"bound": "tensor", "kernel": "gemm_tc_kernel (step GEMMs)", "achieved": g["achieved"],
+        roofline = {"bound": "tensor", "kernel": "gemm_tc2_kernel (the step's GEMMs, CTA pairs)", "achieved": g["achieved"],
                     "peak": pk["tensor"], "unit": "TFLOP/s", "frac": g["frac"],
                     "peak_kind": f"bf16 sustained ({pk['source']})",
                     "traffic": GEMM_TRAFFIC_PER_LAUNCH,

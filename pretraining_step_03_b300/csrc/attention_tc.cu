@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, FWD_TILES);
     // the heaviest (latest) query blocks first; (b, h) vary fastest
-    const int qb = p.nblk - 1 - blockIdx.y, h = blockIdx.x % p.H, b = blockIdx.x / p.H;
+    const int bh = blockIdx.y, qb = p.nblk - 1 - blockIdx.x, h = bh % p.H, b = bh / p.H;
     const int nkb = qb + 1;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* q_full = &sm.bar[0];
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(NT, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DQ_TILES);
-    const int qb = p.nblk - 1 - blockIdx.y, h = blockIdx.x % p.H, b = blockIdx.x / p.H;
+    const int bh = blockIdx.y, qb = p.nblk - 1 - blockIdx.x, h = bh % p.H, b = bh / p.H;
     const int nkb = qb + 1;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* qd_full = &sm.bar[0];
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(NT, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DKV_TILES);
-    const int kb = blockIdx.y, h = blockIdx.x % p.H, b = blockIdx.x / p.H;  // early keys (most work) first
+    const int bh = blockIdx.y, kb = blockIdx.x, h = bh % p.H, b = bh / p.H;  // early keys (most work) first
     const int nq = p.nblk - kb;        // query blocks kb .. nblk-1
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* kv_full = &sm.bar[0];
@@ -745,7 +745,7 @@ __global__ void __launch_bounds__(NT, 1)
             tc::fence_before();
             tc::mbar_arrive(ds_full);
             if (p.ds) {   // keep key r's dS for the dQ product: query chunks 4g+k and 8+4g+k
-                uint8_t* base = ds_tile(p, blockIdx.x, j, kb) + (r >> 6) * DS_HALF + (r & 63) * 16;
+                uint8_t* base = ds_tile(p, bh, j, kb) + (r >> 6) * DS_HALF + (r & 63) * 16;
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
@@ -795,7 +795,7 @@ __global__ void __launch_bounds__(DQS_NT, 2)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DQS_ST);
-    const int qb = p.nblk - 1 - blockIdx.y, h = blockIdx.x % p.H, b = blockIdx.x / p.H;
+    const int bh = blockIdx.y, qb = p.nblk - 1 - blockIdx.x, h = bh % p.H, b = bh / p.H;
     const int nu = 2 * (qb + 1);           // 64-key units up to the diagonal
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* full = &sm.bar[0];
@@ -808,7 +808,7 @@ __global__ void __launch_bounds__(DQS_NT, 2)
     const int col = h * HD;
 
     if (warp == 0 && lane == 0) {
-        const uint8_t* ds0 = ds_tile(p, blockIdx.x, qb, 0);
+        const uint8_t* ds0 = ds_tile(p, bh, qb, 0);
         int u = 0;
         for (; u < nu; ++u) {
             const int st = u % DQS_ST;
@@ -875,6 +875,11 @@ int maps(CUtensorMap* m, const void* ptr, long rows, long ld, int H) {
 
 uint32_t* g_attn_flag = nullptr;
 
+// Grids are (blocks of a sequence, batch x heads): the x index runs fastest, so the
+// CTAs of one batch-head are resident together and share its K/V (forward, dQ) or
+// Q/dO (dK/dV) tiles through L2 instead of re-reading them from HBM.
+constexpr long MAX_GRID_Y = 65535;
+
 bool attention_tc_supported(long ld, long ldo, long ldd, const void* q, const void* k, const void* v,
                             int D) {
     if (D != HD) return false;
@@ -885,6 +890,7 @@ bool attention_tc_supported(long ld, long ldo, long ldd, const void* q, const vo
 
 int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, bf16* o, long ldo,
                          float* lse, int B, int T, int H, cudaStream_t s) {
+    if ((long)B * H > MAX_GRID_Y) return set_error(NC_ERR_UNSUPPORTED, "attention: B*H = %ld > %ld", (long)B * H, MAX_GRID_Y);
     static bool init = false;
     if (!init) {
         NC_TRY(set_smem(attn_fwd_kernel, smem_bytes(FWD_TILES)));
@@ -898,7 +904,7 @@ int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, b
     AttnParams p{};
     p.T = T; p.H = H; p.nblk = ceil_div(T, BR); p.ldo = ldo; p.o = o; p.lse = lse;
     p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
-    attn_fwd_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(FWD_TILES), s>>>(mq, mk, mv, p);
+    attn_fwd_kernel<<<dim3(p.nblk, H * B), NT, smem_bytes(FWD_TILES), s>>>(mq, mk, mv, p);
     note_launch();
     NC_LAUNCH_CHECK("attn_fwd_kernel");
     return NC_OK;
@@ -914,6 +920,7 @@ int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, 
                           long ldo, const float* lse, const float* delta, bf16* dq, bf16* dk, bf16* dv,
                           long ldd, int B, int T, int H, const float2* rope, int rope_ld, bf16* ds,
                           cudaStream_t s) {
+    if ((long)B * H > MAX_GRID_Y) return set_error(NC_ERR_UNSUPPORTED, "attention: B*H = %ld > %ld", (long)B * H, MAX_GRID_Y);
     static bool init = false;
     if (!init) {
         NC_TRY(set_smem(attn_dq_kernel, smem_bytes(DQ_TILES)));
@@ -934,13 +941,13 @@ int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, 
     p.rope_ld = rope_ld;
     p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
     p.ds = ds; p.ds_bh = (long)p.nblk * (p.nblk + 1) / 2;
-    attn_dkdv_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);
+    attn_dkdv_kernel<<<dim3(p.nblk, H * B), NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);
     if (ds) {
         CUtensorMap mk64;
         NC_TRY(make_map(&mk64, k, (long)H * HD, rows, 1, ld, 0, 64, 64));
-        attn_dq_ds_kernel<<<dim3(H * B, p.nblk), DQS_NT, smem_bytes(DQS_ST), s>>>(mk64, p);
+        attn_dq_ds_kernel<<<dim3(p.nblk, H * B), DQS_NT, smem_bytes(DQS_ST), s>>>(mk64, p);
     } else {
-        attn_dq_kernel<<<dim3(H * B, p.nblk), NT, smem_bytes(DQ_TILES), s>>>(mq, mk, mv, mdo, p);
+        attn_dq_kernel<<<dim3(p.nblk, H * B), NT, smem_bytes(DQ_TILES), s>>>(mq, mk, mv, mdo, p);
     }
     note_launch(2);
     NC_LAUNCH_CHECK("attn backward kernels");
