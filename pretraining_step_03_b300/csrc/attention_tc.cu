@@ -21,17 +21,14 @@
 // TMA brings in (an M=128, N=128 MMA from shared memory already reads at the
 // SM's shared-memory bandwidth).
 //
-// forward (one CTA per 128-query block, keys in 128-blocks up to the diagonal):
-//   S_j = Q K_j^T into one of two TMEM buffers (the next S overlaps the
-//   softmax of this one); P_j = exp2(S_j*c - m) to shared memory; O += P_j V_j
-//   in TMEM.  The running max m is raised only when it grows by more than
-//   2^8, and O is then rescaled in TMEM (the rescale is rare after the first
-//   blocks; P stays <= 256).
-// Two groups of four softmax warps split each 128-column row (32-column
-// chunks g and g+2 go to group g), so every row has two threads; the forward
-// combines their row maxima through a shared-memory exchange guarded by an
-// mbarrier (bounded wait).  When given the RoPE table, the backward rotates
-// dq and dk back to the unrotated q, k frame in its epilogue.
+// forward (one CTA per pair of 128-query blocks, keys in 128-blocks up to the diagonal):
+//   S = Q K^T per query tile in TMEM; P = exp2(S*c - m) packed into TMEM over the
+//   first half of its S; O += P V in TMEM.  One thread per query row; the two
+//   tiles alternate on the tensor pipe (one tile's softmax overlaps the other
+//   tile's products).  The running max m is raised only when it grows by more
+//   than 2^8, and O is then rescaled in TMEM (rare after the first blocks; P
+//   stays <= 256).  When given the RoPE table, the backward rotates dq and dk
+//   back to the unrotated q, k frame in its epilogue.
 // backward, deterministic, no atomics:
 //   dK/dV kernel, one CTA per 128-key block, query blocks from the diagonal on:
 //     S^T = K Q^T, dP^T = V dO^T, P^T and dS^T packed into TMEM,
@@ -89,18 +86,6 @@ __device__ __forceinline__ void ld_half(uint32_t taddr, int g, float* v) {
     tc::tmem_ld32(taddr + g * 32, reinterpret_cast<uint32_t*>(v));
     tc::tmem_ld32(taddr + (g + 2) * 32, reinterpret_cast<uint32_t*>(v) + 32);
     tc::tmem_wait_ld();
-}
-
-// 32 packed bf16 pairs (this thread's 64 columns) into row r of a tile, 128-byte swizzle.
-__device__ __forceinline__ void store_half(uint8_t* tile, int r, int g, const uint32_t* w) {
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint8_t* dst = tile + a * ATOM + r * 128 + ((((4 * g + k) ^ (r & 7))) << 4);
-            const uint32_t* x = w + 16 * a + 4 * k;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(x[0], x[1], x[2], x[3]);
-        }
 }
 
 // this thread's 64 columns of an output row (bf16, row pointer at column 0)
@@ -211,16 +196,6 @@ __device__ __forceinline__ void teardown(Smem& s, uint32_t tmem, uint32_t* flag,
     }
 }
 
-// exchange one float with the other group's thread of the same row (bounded wait)
-__device__ __forceinline__ bool exchange(Smem& sm, uint64_t* xbar, int it, int g, int r, float mine,
-                                         float* other) {
-    float* x = sm.xch + (it & 1) * 256;
-    x[g * 128 + r] = mine;
-    tc::mbar_arrive(&xbar[it & 1]);
-    if (!tc::mbar_wait_warp(&xbar[it & 1], (it >> 1) & 1, sm.abort)) return false;
-    *other = x[(1 - g) * 128 + r];
-    return true;
-}
 
 // write this thread's 64 probabilities, packed bf16 pairs, into row columns
 // [16g, 16g+16) and [32+16g, 32+16g+16) of a TMEM region (the A-operand layout:
@@ -231,13 +206,22 @@ __device__ __forceinline__ void st_half_bf16(uint32_t taddr, int g, const uint32
 }
 
 // ===================================================================== forward
-// smem tiles: 0 Q | 1..3 K stages | 4..6 V stages
-// barriers: 0 q_full, 1-3 k_full, 4-6 k_empty, 7-9 v_full, 10-12 v_empty, 13-14 s_full,
-//           15-16 p_full, 17-18 o_done, 19-20 xbar
-// TMEM: S buffers at columns 0 and 128 (P_j overwrites the first 64 columns of its
-// S buffer as packed bf16 and is the A operand of O += P V), O at 256.
-constexpr int FWD_TILES = 7;
-constexpr int FWD_NST = 3;
+// One CTA per pair of consecutive 128-query blocks (tiles 0 and 1) of one batch-head;
+// both tiles stream the same K/V blocks.  Warps 2-5 do the softmax of tile 0 and
+// warps 6-9 that of tile 1, one thread per query row holding its whole 128-key score
+// row.  The MMA warp interleaves the tiles,
+//   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), PV_0(j+1), ...
+// so while one tile's softmax runs the tensor pipe works on the other tile.  S_t(j+1)
+// overwrites the TMEM columns whose packed P_t(j) PV_t(j) reads, so it is issued once
+// PV_t(j) has completed (an MMA's TMEM writes are not ordered after an earlier MMA's
+// TMEM operand reads); that also keeps O_t still while the softmax rescales it.
+// smem tiles: 0 Q_0 | 1 Q_1 | 2,3 K stages | 4,5 V stages
+// barriers: 0 q_full, 1-2 k_full, 3-4 k_empty, 5-6 v_full, 7-8 v_empty, 9-10 s_full[t],
+//           11-12 p_full[t], 13-14 o_done[t], 15 drain
+// TMEM: S_t at 128 t (P_t packed into its first 64 columns), O_t at 256 + 128 t.
+constexpr int FWD_TILES = 6;
+constexpr int FWD_NST = 2;
+constexpr int NSM_T = 128;   // softmax threads per tile
 
 __global__ void __launch_bounds__(NT, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -245,32 +229,36 @@ __global__ void __launch_bounds__(NT, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, FWD_TILES);
-    // the heaviest (latest) query blocks first; (b, h) vary fastest
-    const int bh = blockIdx.y, qb = p.nblk - 1 - blockIdx.x, h = bh % p.H, b = bh / p.H;
-    const int nkb = qb + 1;
+    // the heaviest (latest) query-block pairs first; the pairs of one batch-head together
+    const int npair = (p.nblk + 1) / 2;
+    const int bh = blockIdx.y, c = npair - 1 - blockIdx.x, h = bh % p.H, b = bh / p.H;
+    const int qb0 = 2 * c;
+    const bool has1 = qb0 + 1 < p.nblk;
+    const int nk = has1 ? qb0 + 2 : qb0 + 1;          // key blocks streamed (tile t uses 0 .. qb0 + t)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* q_full = &sm.bar[0];
     uint64_t* k_full = &sm.bar[1];
-    uint64_t* k_empty = &sm.bar[4];
-    uint64_t* v_full = &sm.bar[7];
-    uint64_t* v_empty = &sm.bar[10];
-    uint64_t* s_full = &sm.bar[13];
-    uint64_t* p_full = &sm.bar[15];
-    uint64_t* o_done = &sm.bar[17];
-    uint64_t* xbar = &sm.bar[19];
-    const uint32_t counts[21] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NSM, NSM, 1, 1, NSM, NSM};
-    setup(sm, 21, counts);
+    uint64_t* k_empty = &sm.bar[3];
+    uint64_t* v_full = &sm.bar[5];
+    uint64_t* v_empty = &sm.bar[7];
+    uint64_t* s_full = &sm.bar[9];
+    uint64_t* p_full = &sm.bar[11];
+    uint64_t* o_done = &sm.bar[13];
+    uint64_t* drain = &sm.bar[15];
+    const uint32_t counts[16] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NSM_T, NSM_T, 1, 1, 1};
+    setup(sm, 16, counts);
     const uint32_t tmem = *sm.tmem_slot;
-    uint8_t* Q = sm.base;
-    auto Kt = [&](int st) { return sm.base + (1 + st) * TILE; };
-    auto Vt = [&](int st) { return sm.base + (1 + FWD_NST + st) * TILE; };
+    auto Qt = [&](int t) { return sm.base + t * TILE; };
+    auto Kt = [&](int st) { return sm.base + (2 + st) * TILE; };
+    auto Vt = [&](int st) { return sm.base + (2 + FWD_NST + st) * TILE; };
     const int col = h * HD;
-    const int rowq = b * p.T + qb * BR;
 
     if (warp == 0 && lane == 0) {
-        tc::mbar_expect_tx(q_full, TILE);
-        load_tile(Q, &mq, q_full, col, rowq);
-        for (int j = 0; j < nkb; ++j) {
+        tc::mbar_expect_tx(q_full, (has1 ? 2 : 1) * TILE);
+        load_tile(Qt(0), &mq, q_full, col, b * p.T + qb0 * BR);
+        if (has1) load_tile(Qt(1), &mq, q_full, col, b * p.T + (qb0 + 1) * BR);
+        int issued = 0;
+        for (int j = 0; j < nk; ++j) {
             const int st = j % FWD_NST;
             const uint32_t ph = ((j / FWD_NST) & 1) ^ 1;
             if (!tc::mbar_wait(&k_empty[st], ph, sm.abort)) break;
@@ -279,116 +267,139 @@ __global__ void __launch_bounds__(NT, 1)
             if (!tc::mbar_wait(&v_empty[st], ph, sm.abort)) break;
             tc::mbar_expect_tx(&v_full[st], TILE);
             load_tile(Vt(st), &mv, &v_full[st], col, b * p.T + j * BR);
+            issued = j + 1;
+        }
+        if (*sm.abort) {   // let the copies still in flight land before the CTA exits
+            tc::mbar_wait_drain(q_full, 0);
+            for (int j = issued - 1; j >= 0 && j >= issued - FWD_NST; --j) {
+                tc::mbar_wait_drain(&k_full[j % FWD_NST], (j / FWD_NST) & 1);
+                tc::mbar_wait_drain(&v_full[j % FWD_NST], (j / FWD_NST) & 1);
+            }
         }
     } else if (warp == 1 && lane == 0) {
-        const uint32_t q0 = tc::smem_u32(Q);
         bool ok = tc::mbar_wait(q_full, 0, sm.abort);
-        auto issue_s = [&](int j) -> bool {
-            const int st = j % FWD_NST;
-            // P_{j-2} in this S buffer is the A operand of PV_{j-2}: an MMA's TMEM
-            // writes are not ordered after an earlier MMA's TMEM operand reads, so
-            // wait for PV_{j-2} to complete (PV_{j-1} keeps the pipe busy meanwhile)
-            if (j >= 2 && !tc::mbar_wait(&o_done[j & 1], ((j - 2) >> 1) & 1, sm.abort)) return false;
-            if (!tc::mbar_wait(&k_full[st], (j / FWD_NST) & 1, sm.abort)) return false;
+        // S_t(j) = Q_t K_j^T into TMEM 128 t
+        auto issue_s = [&](int t, int j) -> bool {
+            if (j > 0 && !tc::mbar_wait(&o_done[t], (j - 1) & 1, sm.abort)) return false;
             tc::fence_after();
-            const uint32_t k0 = tc::smem_u32(Kt(st));
+            const uint32_t q0 = tc::smem_u32(Qt(t)), k0 = tc::smem_u32(Kt(j % FWD_NST));
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16(tmem + (j & 1) * 128, dk_(q0, kk), dk_(k0, kk), IDESC_KK, kk > 0);
-            tc::mma_commit(&s_full[j & 1]);
-            tc::mma_commit(&k_empty[st]);
+            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128 * t, dk_(q0, kk), dk_(k0, kk), IDESC_KK, kk > 0);
+            tc::mma_commit(&s_full[t]);
             return true;
         };
-        if (ok) ok = issue_s(0);
-        for (int j = 0; ok && j < nkb; ++j) {
-            if (j + 1 < nkb && !issue_s(j + 1)) break;
-            const int st = j % FWD_NST;
-            if (!tc::mbar_wait(&p_full[j & 1], (j >> 1) & 1, sm.abort)) break;
-            if (!tc::mbar_wait(&v_full[st], (j / FWD_NST) & 1, sm.abort)) break;
+        // O_t += P_t(j) V_j, P_t(j) packed in TMEM 128 t
+        auto issue_pv = [&](int t, int j) -> bool {
+            if (!tc::mbar_wait(&p_full[t], j & 1, sm.abort)) return false;
             tc::fence_after();
-            const uint32_t v0 = tc::smem_u32(Vt(st));
+            const uint32_t v0 = tc::smem_u32(Vt(j % FWD_NST));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16_ts(tmem + 256, tmem + (j & 1) * 128 + kk * 8, dm_(v0, kk), IDESC_KM,
+                tc::mma_bf16_ts(tmem + 256 + 128 * t, tmem + 128 * t + kk * 8, dm_(v0, kk), IDESC_KM,
                                 (j > 0 || kk > 0));
-            tc::mma_commit(&o_done[j & 1]);
-            tc::mma_commit(&v_empty[st]);
+            tc::mma_commit(&o_done[t]);
+            return true;
+        };
+        auto wait_k = [&](int j) { return tc::mbar_wait(&k_full[j % FWD_NST], (j / FWD_NST) & 1, sm.abort); };
+        auto wait_v = [&](int j) { return tc::mbar_wait(&v_full[j % FWD_NST], (j / FWD_NST) & 1, sm.abort); };
+        // tile 0 takes key blocks 0 .. nk0-1, tile 1 (if any) 0 .. nk-1
+        const int nk0 = qb0 + 1;
+        if (ok) ok = wait_k(0) && issue_s(0, 0) && (!has1 || issue_s(1, 0));
+        if (ok) tc::mma_commit(&k_empty[0]);
+        for (int j = 0; ok && j < nk; ++j) {
+            if (!(ok = wait_v(j))) break;
+            const bool next = j + 1 < nk;
+            if (next && !(ok = wait_k(j + 1))) break;
+            if (j < nk0) {
+                if (!(ok = issue_pv(0, j))) break;
+                if (j + 1 < nk0 && !(ok = issue_s(0, j + 1))) break;
+            }
+            if (has1) {
+                if (!(ok = issue_pv(1, j))) break;
+                if (next && !(ok = issue_s(1, j + 1))) break;
+            }
+            tc::mma_commit(&v_empty[j % FWD_NST]);
+            if (next) tc::mma_commit(&k_empty[(j + 1) % FWD_NST]);
+        }
+        if (*sm.abort) {
+            tc::mma_commit(drain);
+            tc::mbar_wait_drain(drain, 0);
         }
     } else if (warp >= 2) {
-        const int g = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;
+        const int t = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
+        const int qb = qb0 + t;
+        const int nkt = qb + 1;
         const float c2 = p.scale * LOG2E;
         float m2 = -INFINITY, l = 0.f;
-        float s[64];
-        bool ok = true;
-        for (int j = 0; j < nkb; ++j) {
-            if (!(ok = tc::mbar_wait_warp(&s_full[j & 1], (j >> 1) & 1, sm.abort))) break;
+        bool ok = t == 0 || has1;
+        const uint32_t sb = tmem + lanes + 128 * t, ob = tmem + lanes + 256 + 128 * t;
+        for (int j = 0; ok && j < nkt; ++j) {
+            if (!(ok = tc::mbar_wait_warp(&s_full[t], j & 1, sm.abort))) break;
             tc::fence_after();
-            const uint32_t sb = tmem + lanes + (j & 1) * 128;
-            ld_half(sb, g, s);
+            float s[128];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) tc::tmem_ld32(sb + 32 * cc, reinterpret_cast<uint32_t*>(s) + 32 * cc);
+            tc::tmem_wait_ld();
             if (j == qb) {   // diagonal block: keys after the query are masked
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    if (col_of(g, i) > r) s[i] = -INFINITY;
+                for (int i = 0; i < 128; ++i)
+                    if (i > r) s[i] = -INFINITY;
             }
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], s[i]);
-            float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;   // in log2 units
-            float mo;
-            if (!(ok = exchange(sm, xbar, j, g, r, mx, &mo))) break;
-            mx = fmaxf(mx, mo);
-            if (j == 0) {
+            for (int i = 0; i < 128; ++i) m4[i & 3] = fmaxf(m4[i & 3], s[i]);
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;   // log2 units
+            // the running max moves only when it grows by more than 2^8 (P stays <= 256)
+            const bool need = j > 0 && mx > m2 + 8.f;
+            float alpha = 1.f;
+            if (j == 0) m2 = mx;
+            else if (need) {
+                alpha = exp2f(m2 - mx);
+                l *= alpha;
                 m2 = mx;
-            } else {
-                const bool need = mx > m2 + 8.f;
-                if (__any_sync(0xffffffffu, need)) {
-                    // O += P_{j-1} V_{j-1} must be complete before O is rescaled
-                    if (!(ok = tc::mbar_wait_warp(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, sm.abort))) break;
-                    tc::fence_after();
-                    const float alpha = need ? exp2f(m2 - mx) : 1.f;
-#pragma unroll 1
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t o[32];
-                        const uint32_t ta = tmem + lanes + 256 + (g + 2 * c) * 32;
-                        tc::tmem_ld32(ta, o);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tc::tmem_st32(ta, o);
-                    }
-                    tc::tmem_wait_st();
-                    if (need) {
-                        l *= alpha;
-                        m2 = mx;
-                    }
-                }
             }
-            uint32_t w[32];
             float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float a = exp2f(fmaf(s[2 * i], c2, -m2)), bb = exp2f(fmaf(s[2 * i + 1], c2, -m2));
-                sum4[i & 3] += a + bb;
-                w[i] = pack2(a, bb);
+            for (int h2 = 0; h2 < 2; ++h2) {   // P_t(j) packed into the first 64 columns of S_t
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float a = exp2f(fmaf(s[64 * h2 + 2 * i], c2, -m2));
+                    const float bb = exp2f(fmaf(s[64 * h2 + 2 * i + 1], c2, -m2));
+                    sum4[i & 3] += a + bb;
+                    w[i] = pack2(a, bb);
+                }
+                tc::tmem_st32(sb + 32 * h2, w);
             }
             l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-            st_half_bf16(sb, g, w);
+            if (__any_sync(0xffffffffu, need)) {
+                // O_t is still (S_t(j) was issued after PV_t(j-1) completed): rescale in place
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(ob + 32 * cc, o);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tc::tmem_st32(ob + 32 * cc, o);
+                }
+            }
             tc::tmem_wait_st();
             tc::fence_before();
-            tc::mbar_arrive(&p_full[j & 1]);
+            tc::mbar_arrive(&p_full[t]);
         }
-        float lo = 0.f;
-        if (ok && tc::mbar_wait_warp(&o_done[(nkb - 1) & 1], ((nkb - 1) >> 1) & 1, sm.abort) &&
-            exchange(sm, xbar, nkb, g, r, l, &lo)) {
+        if (ok && tc::mbar_wait_warp(&o_done[t], (nkt - 1) & 1, sm.abort)) {
             tc::fence_after();
-            const float lt = l + lo;
-            ld_half(tmem + lanes + 256, g, s);
-            const int t = qb * BR + r;
-            if (t < p.T) {
-                store_out_half(p.o + (long)(b * p.T + t) * p.ldo + col, g, s, 1.f / lt);
-                if (g == 0) p.lse[((long)b * p.H + h) * p.T + t] = (m2 + log2f(lt)) * LN2;
+            const int tq = qb * BR + r;
+            const float inv = 1.f / l;
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {
+                float v[64];
+                ld_half(ob, g, v);
+                if (tq < p.T) store_out_half(p.o + (long)(b * p.T + tq) * p.ldo + col, g, v, inv);
             }
+            if (tq < p.T) p.lse[((long)b * p.H + h) * p.T + tq] = (m2 + log2f(l)) * LN2;
         }
     }
     teardown(sm, tmem, p.flag);
@@ -904,7 +915,7 @@ int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, b
     AttnParams p{};
     p.T = T; p.H = H; p.nblk = ceil_div(T, BR); p.ldo = ldo; p.o = o; p.lse = lse;
     p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
-    attn_fwd_kernel<<<dim3(p.nblk, H * B), NT, smem_bytes(FWD_TILES), s>>>(mq, mk, mv, p);
+    attn_fwd_kernel<<<dim3((p.nblk + 1) / 2, H * B), NT, smem_bytes(FWD_TILES), s>>>(mq, mk, mv, p);
     note_launch();
     NC_LAUNCH_CHECK("attn_fwd_kernel");
     return NC_OK;

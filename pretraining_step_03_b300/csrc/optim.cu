@@ -68,59 +68,96 @@ __device__ float matrix_inv_norm(const float* partial, int mat, int chunks) {
     return inv;
 }
 
-// 32x32 tiles through shared memory; X[j][i] = g[i][j]*inv when transposed.
+// Four consecutive values to / from T (16-byte fp32 or 8-byte bf16 accesses).
+__device__ __forceinline__ void st4(float* p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void st4(bf16* p, float a, float b, float c, float d) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const bf16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// X = g * inv, written transposed (X[j][i] = g[i][j]) for tall matrices.  Straight
+// matrices are a flat vectorised scale; transposed ones go through 32x32 shared
+// tiles, each thread moving one 4-vector in and one out (row t/8, quad t%8).
 template <typename T>
-__global__ void muon_normalize_kernel(const float* g, const MuonMat* mats, const float* partial,
-                                      int chunks, T* xbase) {
+__global__ void __launch_bounds__(NT) muon_normalize_kernel(const float* g, const MuonMat* mats,
+                                                            const float* partial, int chunks, T* xbase) {
     __shared__ float tile[32][33];
     const MuonMat mm = mats[blockIdx.y];
     const float inv = matrix_inv_norm(partial, blockIdx.y, chunks);
     const float* gp = g + mm.off;
     T* x = xbase + mm.x_off;
+    if (!mm.tr) {
+        const long n4 = (long)mm.rows * mm.cols / 4;
+#pragma unroll 4
+        for (long i = (long)blockIdx.x * NT + threadIdx.x; i < n4; i += (long)gridDim.x * NT) {
+            const float4 v = ld4(gp + 4 * i);
+            st4(x + 4 * i, v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+        }
+        return;
+    }
     const int tr = mm.rows / 32, tc = mm.cols / 32;
+    const int ty = threadIdx.x / 8, tq = threadIdx.x % 8;
     for (int t = blockIdx.x; t < tr * tc; t += gridDim.x) {
         const int i0 = (t / tc) * 32, j0 = (t % tc) * 32;
-        if (!mm.tr) {
-            for (int y = threadIdx.y; y < 32; y += 8)
-                x[(long)(i0 + y) * mm.cols + j0 + threadIdx.x] =
-                    from_f<T>(gp[(long)(i0 + y) * mm.cols + j0 + threadIdx.x] * inv);
-        } else {
-            __syncthreads();
-            for (int y = threadIdx.y; y < 32; y += 8)
-                tile[y][threadIdx.x] = gp[(long)(i0 + y) * mm.cols + j0 + threadIdx.x];
-            __syncthreads();
-            for (int y = threadIdx.y; y < 32; y += 8)
-                x[(long)(j0 + y) * mm.rows + i0 + threadIdx.x] = from_f<T>(tile[threadIdx.x][y] * inv);
-        }
+        const float4 v = ld4(gp + (long)(i0 + ty) * mm.cols + j0 + 4 * tq);
+        __syncthreads();
+        tile[ty][4 * tq] = v.x; tile[ty][4 * tq + 1] = v.y; tile[ty][4 * tq + 2] = v.z; tile[ty][4 * tq + 3] = v.w;
+        __syncthreads();
+        // X row j0 + ty, columns i0 + 4 tq ..
+        st4(x + (long)(j0 + ty) * mm.rows + i0 + 4 * tq, tile[4 * tq][ty] * inv, tile[4 * tq + 1][ty] * inv,
+            tile[4 * tq + 2][ty] * inv, tile[4 * tq + 3][ty] * inv);
     }
 }
 
-// W -= step * X (transposed read when tr); refresh the bf16 copy.
+// W -= step * X (X read transposed for tall matrices); refresh the bf16 copy.
 template <typename T>
-__global__ void muon_apply_kernel(float* w, bf16* w16, const MuonMat* mats, const T* xbase,
-                                  float lr) {
+__global__ void __launch_bounds__(NT) muon_apply_kernel(float* w, bf16* w16, const MuonMat* mats,
+                                                        const T* xbase, float lr) {
     __shared__ float tile[32][33];
     const MuonMat mm = mats[blockIdx.y];
     const float step = lr * mm.scale;
     float* wp = w + mm.off;
     bf16* wp16 = w16 ? w16 + mm.off : nullptr;
     const T* x = xbase + mm.x_off;
+    if (!mm.tr) {
+        const long n4 = (long)mm.rows * mm.cols / 4;
+#pragma unroll 4
+        for (long i = (long)blockIdx.x * NT + threadIdx.x; i < n4; i += (long)gridDim.x * NT) {
+            const float4 xv = ld4(x + 4 * i);
+            float4 v = ld4(wp + 4 * i);
+            v.x -= step * xv.x; v.y -= step * xv.y; v.z -= step * xv.z; v.w -= step * xv.w;
+            st4(wp + 4 * i, v.x, v.y, v.z, v.w);
+            if (wp16) st4(wp16 + 4 * i, v.x, v.y, v.z, v.w);
+        }
+        return;
+    }
     const int tr = mm.rows / 32, tc = mm.cols / 32;
+    const int ty = threadIdx.x / 8, tq = threadIdx.x % 8;
     for (int t = blockIdx.x; t < tr * tc; t += gridDim.x) {
         const int i0 = (t / tc) * 32, j0 = (t % tc) * 32;
-        if (mm.tr) {
-            __syncthreads();
-            for (int y = threadIdx.y; y < 32; y += 8)   // X is [cols][rows]
-                tile[y][threadIdx.x] = to_f<T>(x[(long)(j0 + y) * mm.rows + i0 + threadIdx.x]);
-            __syncthreads();
-        }
-        for (int y = threadIdx.y; y < 32; y += 8) {
-            const long wi = (long)(i0 + y) * mm.cols + j0 + threadIdx.x;
-            const float xv = mm.tr ? tile[threadIdx.x][y] : to_f<T>(x[wi]);
-            const float nw = wp[wi] - step * xv;
-            wp[wi] = nw;
-            if (wp16) wp16[wi] = __float2bfloat16_rn(nw);
-        }
+        // X is [cols][rows]: its row j0 + ty holds W's column j0 + ty, rows i0 + 4 tq ..
+        const float4 xv = ld4(x + (long)(j0 + ty) * mm.rows + i0 + 4 * tq);
+        __syncthreads();
+        tile[4 * tq][ty] = xv.x; tile[4 * tq + 1][ty] = xv.y; tile[4 * tq + 2][ty] = xv.z; tile[4 * tq + 3][ty] = xv.w;
+        __syncthreads();
+        const long wi = (long)(i0 + ty) * mm.cols + j0 + 4 * tq;
+        float4 v = ld4(wp + wi);
+        v.x -= step * tile[ty][4 * tq]; v.y -= step * tile[ty][4 * tq + 1];
+        v.z -= step * tile[ty][4 * tq + 2]; v.w -= step * tile[ty][4 * tq + 3];
+        st4(wp + wi, v.x, v.y, v.z, v.w);
+        if (wp16) st4(wp16 + wi, v.x, v.y, v.z, v.w);
     }
 }
 
@@ -154,8 +191,7 @@ int muon_momentum(float* g, float* buf, const MuonMat* mats, int nmat, float mu,
 template <typename T>
 int muon_normalize(const float* g, const MuonMat* mats, int nmat, const float* partial, int chunks,
                    T* x, int blocks_per_mat, cudaStream_t s) {
-    muon_normalize_kernel<T><<<dim3(blocks_per_mat, nmat), dim3(32, 8), 0, s>>>(g, mats, partial,
-                                                                                chunks, x);
+    muon_normalize_kernel<T><<<dim3(blocks_per_mat, nmat), NT, 0, s>>>(g, mats, partial, chunks, x);
     note_launch();
     NC_LAUNCH_CHECK("muon_normalize");
     return NC_OK;
@@ -164,7 +200,7 @@ int muon_normalize(const float* g, const MuonMat* mats, int nmat, const float* p
 template <typename T>
 int muon_apply(float* w, bf16* w16, const MuonMat* mats, int nmat, const T* x, float lr,
                int blocks_per_mat, cudaStream_t s) {
-    muon_apply_kernel<T><<<dim3(blocks_per_mat, nmat), dim3(32, 8), 0, s>>>(w, w16, mats, x, lr);
+    muon_apply_kernel<T><<<dim3(blocks_per_mat, nmat), NT, 0, s>>>(w, w16, mats, x, lr);
     note_launch();
     NC_LAUNCH_CHECK("muon_apply");
     return NC_OK;
