@@ -303,7 +303,7 @@ def main():
         T, times, cores = cpu_baseline(w, steps=args.warmup + args.steps)
         t = times[args.warmup:] if len(times) > args.warmup else times
         v = T / (sum(t) / len(t))
-        line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0, "steps": len(t),
+        line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": len(t),
                 "warmup": args.warmup, "ms_per_step": 1000 * sum(t) / len(t), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": config, "impl": "reference",
