@@ -831,6 +831,45 @@ __global__ void splitk_reduce_kernel(const float* ws, int splits, int batch, int
     st_elem(C, b * sC + m * ldc + n, c_dtype, s);
 }
 
+// The same, four consecutive columns per thread (16-byte loads of every partial) and 32-bit
+// index arithmetic; needs N, ldc, ldaux multiples of 4, 16-byte aligned bases and fewer
+// than 2^31 quads.
+__global__ void __launch_bounds__(256) splitk_reduce4_kernel(const float* ws, int splits, int rows, int M,
+                                                             int N, void* C, long ldc, long sC, int c_dtype,
+                                                             const void* aux, long ldaux, long sAux,
+                                                             int aux_dtype, float alpha, float beta) {
+    const int n4 = N / 4;
+    const long total = (long)rows * N;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < rows * n4; i += gridDim.x * blockDim.x) {
+        const int r = i / n4, c = (i - r * n4) * 4;
+        const int b = r / M, m = r - b * M;
+        const long wi = (long)r * N + c;
+        float4 acc = reinterpret_cast<const float4*>(ws + wi)[0];
+        for (int k = 1; k < splits; ++k) {
+            const float4 v = reinterpret_cast<const float4*>(ws + (long)k * total + wi)[0];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        float o[4] = {acc.x * alpha, acc.y * alpha, acc.z * alpha, acc.w * alpha};
+        if (aux && beta != 0.f) {
+            const long ai = (long)b * sAux + (long)m * ldaux + c;
+            if (aux_dtype == NC_FP32) {
+                const float4 a = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(aux) + ai)[0];
+                o[0] += beta * a.x; o[1] += beta * a.y; o[2] += beta * a.z; o[3] += beta * a.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] += beta * ld_elem(aux, ai + e, aux_dtype);
+            }
+        }
+        const long ci = (long)b * sC + (long)m * ldc + c;
+        if (c_dtype == NC_FP32) {
+            reinterpret_cast<float4*>(reinterpret_cast<float*>(C) + ci)[0] = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) st_elem(C, ci + e, c_dtype, o[e]);
+        }
+    }
+}
+
 template <int BN, bool A_MN, bool B_MN>
 int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, const TcParams& p,
            cudaStream_t s) {
@@ -1064,9 +1103,21 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     NC_TRY(rc);
     if (p.splits > 1) {
         const long total = (long)g.batch * g.M * g.N;
-        splitk_reduce_kernel<<<ceil_div(total, 256), 256, 0, s>>>(
-            p.ws, p.splits, g.batch, g.M, g.N, g.C, g.ldc, g.sC, g.c_dtype, g.aux, g.ldaux, g.sAux,
-            g.aux_dtype, g.alpha, g.beta);
+        const bool vec = g.N % 4 == 0 && g.ldc % 4 == 0 && (!g.aux || g.ldaux % 4 == 0) &&
+                         (g.batch <= 1 || (g.sC % 4 == 0 && (!g.aux || g.sAux % 4 == 0))) &&
+                         (uintptr_t)g.C % 16 == 0 && (!g.aux || (uintptr_t)g.aux % 16 == 0) &&
+                         total / 4 < (1L << 31) - 65536L * 256;
+        if (vec) {
+            const long quads = total / 4;
+            const int blocks = (int)(quads / 256 < 8L * num_sms() ? ceil_div(quads, 256) : 8L * num_sms());
+            splitk_reduce4_kernel<<<blocks, 256, 0, s>>>(p.ws, p.splits, g.batch * g.M, g.M, g.N, g.C, g.ldc,
+                                                         g.sC, g.c_dtype, g.aux, g.ldaux, g.sAux, g.aux_dtype,
+                                                         g.alpha, g.beta);
+        } else {
+            splitk_reduce_kernel<<<ceil_div(total, 256), 256, 0, s>>>(
+                p.ws, p.splits, g.batch, g.M, g.N, g.C, g.ldc, g.sC, g.c_dtype, g.aux, g.ldaux, g.sAux,
+                g.aux_dtype, g.alpha, g.beta);
+        }
         note_launch();
         NC_LAUNCH_CHECK("splitk_reduce");
     }

@@ -161,20 +161,40 @@ __global__ void __launch_bounds__(NT) muon_apply_kernel(float* w, bf16* w16, con
     }
 }
 
-__global__ void adamw_kernel(float* w, bf16* w16, const float* g, float* m, float* v, long n,
-                             float lr, float b1, float b2, float eps, float wd, float bc1,
-                             float bc2) {
-    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const float gi = g[i];
-    const float mi = b1 * m[i] + (1.f - b1) * gi;
-    const float vi = b2 * v[i] + (1.f - b2) * gi * gi;
-    m[i] = mi;
-    v[i] = vi;
-    const float mhat = mi / bc1, vhat = vi / bc2;
-    const float nw = w[i] * (1.f - lr * wd) - lr * mhat / (sqrtf(vhat) + eps);
-    w[i] = nw;
-    if (w16) w16[i] = __float2bfloat16_rn(nw);
+__device__ __forceinline__ float adamw_one(float& w, float g, float& m, float& v, float lr, float b1, float b2,
+                                           float eps, float wd, float bc1, float bc2) {
+    m = b1 * m + (1.f - b1) * g;
+    v = b2 * v + (1.f - b2) * g * g;
+    const float mhat = m / bc1, vhat = v / bc2;
+    w = w * (1.f - lr * wd) - lr * mhat / (sqrtf(vhat) + eps);
+    return w;
+}
+
+// Four parameters per thread (16-byte accesses); the tail, if n is not a
+// multiple of 4, one per thread.
+__global__ void __launch_bounds__(NT) adamw_kernel(float* w, bf16* w16, const float* g, float* m, float* v,
+                                                   long n, float lr, float b1, float b2, float eps, float wd,
+                                                   float bc1, float bc2) {
+    const long n4 = n / 4;
+    for (long i = (long)blockIdx.x * NT + threadIdx.x; i < n4; i += (long)gridDim.x * NT) {
+        float4 wv = reinterpret_cast<float4*>(w)[i], mv = reinterpret_cast<float4*>(m)[i];
+        float4 vv = reinterpret_cast<float4*>(v)[i];
+        const float4 gv = reinterpret_cast<const float4*>(g)[i];
+        adamw_one(wv.x, gv.x, mv.x, vv.x, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(wv.y, gv.y, mv.y, vv.y, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(wv.z, gv.z, mv.z, vv.z, lr, b1, b2, eps, wd, bc1, bc2);
+        adamw_one(wv.w, gv.w, mv.w, vv.w, lr, b1, b2, eps, wd, bc1, bc2);
+        reinterpret_cast<float4*>(w)[i] = wv;
+        reinterpret_cast<float4*>(m)[i] = mv;
+        reinterpret_cast<float4*>(v)[i] = vv;
+        if (w16) st4(w16 + 4 * i, wv.x, wv.y, wv.z, wv.w);
+    }
+    for (long i = 4 * n4 + (long)blockIdx.x * NT + threadIdx.x; i < n; i += (long)gridDim.x * NT) {
+        float wi = w[i], mi = m[i], vi = v[i];
+        adamw_one(wi, g[i], mi, vi, lr, b1, b2, eps, wd, bc1, bc2);
+        w[i] = wi; m[i] = mi; v[i] = vi;
+        if (w16) w16[i] = __float2bfloat16_rn(wi);
+    }
 }
 
 }  // namespace
@@ -209,7 +229,9 @@ int muon_apply(float* w, bf16* w16, const MuonMat* mats, int nmat, const T* x, f
 int adamw(float* w, bf16* w16, const float* g, float* m, float* v, long n, float lr, float b1,
           float b2, float eps, float wd, float bc1, float bc2, cudaStream_t s) {
     if (n <= 0) return NC_OK;
-    adamw_kernel<<<ceil_div(n, 256), 256, 0, s>>>(w, w16, g, m, v, n, lr, b1, b2, eps, wd, bc1, bc2);
+    const long blocks = ceil_div(n / 4 > 0 ? n / 4 : 1, NT);
+    adamw_kernel<<<(int)(blocks < 16L * 148 ? blocks : 16L * 148), NT, 0, s>>>(w, w16, g, m, v, n, lr, b1, b2, eps,
+                                                                              wd, bc1, bc2);
     note_launch();
     NC_LAUNCH_CHECK("adamw");
     return NC_OK;
