@@ -1,0 +1,83 @@
+"""Muon and AdamW at the full d20 sizes against the fp64 oracle.
+
+The optimizer step of the d20 model (bf16 mode): Muon over all 120 block
+matrices (five bf16 Newton-Schulz iterations, the tall W1 matrices taken
+through their transpose), AdamW on the 65536 x 1280 embedding and LM head.
+Gradients are set on a sample of matrices (a square attention matrix, the
+output projection, a tall W1, a wide W2, wte and lm_head); every other
+matrix has a zero gradient and must stay unchanged.  Two steps, so the
+momentum and Adam moments are exercised.  Tolerances are those of the tiny
+optimizer test: weights cosine >= 0.999 and max-rel <= 2e-2; Muon's
+orthogonalised update cos >= 0.998 against the oracle and, in the oracle's
+singular basis, within 0.1 of its singular values and inside [0.6, 1.3]
+where those are >= 0.68; AdamW's update cos >= 0.999, max-rel <= 2e-2.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from tests._util import assert_close, cmp
+
+pytestmark = pytest.mark.gpu
+
+DEPTH, D, H, V = 20, 1280, 10, 65536
+HP = dict(muon_lr=0.02, momentum=0.95, lr_emb=0.2, lr_unemb=0.004, beta1=0.8, beta2=0.95, eps=1e-10,
+          wd=0.0)
+# wte | L0 wq | L0 wo | L7 w1 (5120 x 1280, tall) | L19 w2 (1280 x 5120, wide) | lm_head
+SEL = [0, 1, 4, 1 + 6 * 7 + 4, 1 + 6 * 19 + 5, 6 * DEPTH + 1]
+UNTOUCHED = [2, 1 + 6 * 10 + 0, 1 + 6 * 12 + 4]
+
+
+def _muon_update_checks(prev, got, xref, what):
+    r, c = got.shape
+    x = (prev - got) / (HP["muon_lr"] * np.sqrt(max(1.0, r / c)))
+    cos, _ = cmp(x, xref)
+    assert cos >= 0.998, f"{what}: Muon update cos {cos}"
+    u, sv, vt = np.linalg.svd(xref, full_matrices=False)
+    proj = np.einsum("ki,kl,il->i", u, x, vt)
+    sel = sv >= 0.68
+    assert sel.any(), what
+    assert np.all(np.abs(proj[sel] - sv[sel]) <= 0.1), (what, np.max(np.abs(proj[sel] - sv[sel])))
+    assert np.all((proj[sel] >= 0.6) & (proj[sel] <= 1.3)), (what, proj[sel].min(), proj[sel].max())
+
+
+def test_d20_optimizer_step_matches_oracle():
+    from pretraining_step_03_b300.model import Model
+    m = Model(DEPTH, D, H, V, 1, 128, dtype="bf16", seed=3)
+    rng = np.random.default_rng(7)
+    w = {i: m.get_param(i).astype(np.float64) for i in SEL}
+    still = {i: m.get_param(i) for i in UNTOUCHED}
+    buf = {i: np.zeros_like(w[i]) for i in SEL}
+    am = {i: np.zeros_like(w[i]) for i in SEL}
+    av = {i: np.zeros_like(w[i]) for i in SEL}
+    for step in (1, 2):
+        grads = {}
+        for i in SEL:
+            g = rng.normal(0.0, 1e-3, w[i].shape).astype(np.float32)
+            if step == 2:   # correlated with step 1 so the momentum matters
+                g = (0.5 * prev_g[i] + g).astype(np.float32)
+            grads[i] = g
+            m.set_grad(i, g)
+        prev_g = grads
+        m.muon_step(HP["muon_lr"], HP["momentum"], True, 5)
+        m.adamw_step(HP["lr_emb"], HP["lr_unemb"], HP["beta1"], HP["beta2"], HP["eps"], HP["wd"], step)
+        for i in SEL:
+            g = grads[i].astype(np.float64)
+            prev = w[i]
+            if i in (0, 6 * DEPTH + 1):
+                lr = HP["lr_emb"] if i == 0 else HP["lr_unemb"]
+                ref, am[i], av[i] = oracle.adamw_step(prev, g, am[i], av[i], lr, HP["beta1"], HP["beta2"],
+                                                      HP["eps"], HP["wd"], step)
+                got = m.get_param(i).astype(np.float64)
+                assert_close(got, ref, 0.999, 2e-2, f"step {step} AdamW weight {i}")
+                assert_close(got - prev, ref - prev, 0.999, 2e-2, f"step {step} AdamW update {i}")
+            else:
+                ref, buf[i], xref = oracle.muon_step(prev, g, buf[i], HP["muon_lr"], HP["momentum"], True, 5)
+                got = m.get_param(i).astype(np.float64)
+                assert_close(got, ref, 0.999, 2e-2, f"step {step} Muon weight {i}")
+                _muon_update_checks(prev, got, xref, f"step {step} matrix {i} {got.shape}")
+            w[i] = got   # both sides continue from the same weights
+        for i in UNTOUCHED:   # zero gradient: no update
+            np.testing.assert_array_equal(m.get_param(i), still[i])
+    assert m.check_flag() == 0
