@@ -225,7 +225,9 @@ template <typename T> T* W(nc_model* m, int i) {
 }
 
 int run_gemm(nc_model* m, const Gemm& g, int cat = NC_PROF_GEMM) {
-    Prof pr(m, cat, 2.0 * g.M * g.N * g.K * g.batch, 0.0);
+    // FLOPs actually executed (a symmetric product computes only its upper tiles)
+    const double frac = m->dtype == NC_BF16 ? gemm_tc_work_fraction(g) : 1.0;
+    Prof pr(m, cat, 2.0 * g.M * g.N * g.K * g.batch * frac, 0.0);
     if (g.in_dtype == NC_BF16) return gemm_tc(g, m->splitk, m->splitk_bytes, m->stream);
     return gemm_simt(g, m->stream);
 }
@@ -401,14 +403,14 @@ int muon(nc_model* m, float lr, float mu, int nesterov, int steps, const float* 
             T* y = Y + (grp == 0 ? 0 : sq);
             T* A = (T*)m->nsA + (grp == 0 ? 0 : (long)4 * Ld * d * d);
             T* Bm = (T*)m->nsB + (grp == 0 ? 0 : (long)4 * Ld * d * d);
-            {   // A = X X^T
+            {   // A = X X^T (symmetric: upper tiles computed, mirrored)
                 Gemm g = mk(m, r, r, c, x, c, false, x, c, false, A, r, act);
-                g.batch = n; g.sA = g.sB = (long)r * c; g.sC = (long)r * r;
+                g.batch = n; g.sA = g.sB = (long)r * c; g.sC = (long)r * r; g.sym = true;
                 NC_TRY(run_gemm(m, g, NC_PROF_MUON_NS));
             }
-            {   // B = c2 A A + c1 A
+            {   // B = c2 A A + c1 A (symmetric, as A is)
                 Gemm g = mk(m, r, r, r, A, r, false, A, r, true, Bm, r, act);
-                g.batch = n; g.sA = g.sB = g.sC = (long)r * r;
+                g.batch = n; g.sA = g.sB = g.sC = (long)r * r; g.sym = true;
                 g.alpha = coef[2]; g.aux = A; g.ldaux = r; g.sAux = (long)r * r; g.aux_dtype = act;
                 g.beta = coef[1];
                 NC_TRY(run_gemm(m, g, NC_PROF_MUON_NS));

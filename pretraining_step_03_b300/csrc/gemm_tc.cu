@@ -54,6 +54,7 @@ struct TcParams {
     int rope_T, rope_cols, rope_ld;
     float* delta;
     int aux_tma;      // the auxiliary matrix comes through the per-warp TMA buffers
+    int sym;          // symmetric C: upper-triangle tiles only, mirrored (tiles_m == tiles_n)
 };
 
 template <int BN> struct Cfg {
@@ -67,6 +68,17 @@ template <int BN> struct Cfg {
 
 __device__ __forceinline__ void decode(const TcParams& p, long u, int& b, int& split, int& tm,
                                        int& tn) {
+    if (p.sym) {   // tiles (tm, tn), tn >= tm, row by row
+        const long tiles = (long)p.tiles_m * (p.tiles_m + 1) / 2;
+        long t = u % tiles;
+        b = (int)(u / tiles);
+        split = 0;
+        int i = 0;
+        while (t >= p.tiles_m - i) { t -= p.tiles_m - i; ++i; }
+        tm = i;
+        tn = i + (int)t;
+        return;
+    }
     const long tiles = (long)p.tiles_m * p.tiles_n;
     const long t = u % tiles, bs = u / tiles;
     split = (int)(bs % p.splits);
@@ -375,12 +387,59 @@ __device__ __forceinline__ void epilogue32(const TcParams& p, int b, int split, 
 
 // The epilogue of one accumulator tile for one row (this thread's TMEM lane),
 // columns of group g (the first or second half of the tile).
+// The transposed copy of a finished 32 x 32 chunk of a symmetric C: lane i holds
+// row r0 + i, columns n0 .. n0+31 (final values); they are written to rows
+// n0 .. n0+31, columns r0 .. r0+31.  coop: all 32 rows and columns are in range.
+__device__ __forceinline__ void mirror32(const TcParams& p, uint8_t* stg, int b, int row, int n0, const float* v,
+                                         bool coop) {
+    const int lane = threadIdx.x & 31;
+    const int r0 = row - lane;
+    if (!coop) {
+        if (row < p.M)
+            for (int j = 0; j < 32 && n0 + j < p.N; ++j)
+                st_elem(p.C, (long)b * p.sC + (long)(n0 + j) * p.ldc + row, p.c_dtype, v[j]);
+        return;
+    }
+    float t[32];
+    __syncwarp();
+    if (p.c_dtype == NC_FP32) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            t[r] = *reinterpret_cast<const float*>(stg + r * 128 + ((((lane >> 2) ^ (r & 7))) << 4) + (lane & 3) * 4);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * c + 2 * e], v[8 * c + 2 * e + 1]);
+                w[e] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            t[r] = __bfloat162float(*reinterpret_cast<const bf16*>(
+                stg + r * 64 + ((((lane >> 3) ^ ((r >> 1) & 3))) << 4) + (lane & 7) * 2));
+    }
+    __syncwarp();
+    wst32(stg, p.C, (long)b * p.sC + (long)n0 * p.ldc + r0, p.ldc, p.c_dtype, t);
+}
+
 // With p.aux_tma the block of the first chunk was issued by the caller; each chunk
 // issues the next one before waiting for its own.
-template <int BN>
+// MIRROR (compile time, symmetric products only): also write the transposed copy of
+// each chunk when `mirror` (an off-diagonal tile).
+template <int BN, bool MIRROR>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int split, int row, int tn,
                                               uint32_t tbase, int g, uint8_t* stg, XPipe& x,
-                                              const CUtensorMap* mx, volatile int* abort) {
+                                              const CUtensorMap* mx, volatile int* abort, bool mirror) {
     const int lane = threadIdx.x & 31;
     const bool rows_ok = __all_sync(0xffffffffu, row < p.M);
     const uint32_t xbytes = p.aux_dtype == NC_FP32 ? 4096u : 2048u;
@@ -483,6 +542,10 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
         if (row < p.M && n0 < p.N) {
             epilogue32(p, b, split, row, n0, v, xb ? const_cast<uint8_t*>(xb) : stg,
                        rows_ok && n0 + 32 <= p.N, xb ? a : nullptr);
+        }
+        if constexpr (MIRROR) {
+            if (mirror && n0 < p.N)   // symmetric C: the transposed copy of this chunk (warp-uniform)
+                mirror32(p, xb ? const_cast<uint8_t*>(xb) : stg, b, row, n0, v, rows_ok && n0 + 32 <= p.N);
         }
     }
 }
@@ -629,7 +692,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            epilogue_tile<BN>(p, b, split, row, tn, tbase, g, x.buf, x, &tmX, abort_flag);
+            epilogue_tile<BN, false>(p, b, split, row, tn, tbase, g, x.buf, x, &tmX, abort_flag, false);
             tc::fence_before();
             tc::mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -661,7 +724,7 @@ constexpr int P_A_BYTES = 128 * BK * 2, P_B_BYTES = 128 * BK * 2;
 constexpr int P_STAGE = P_A_BYTES + P_B_BYTES;
 constexpr int P_SMEM = P_STAGES * P_STAGE + 1024 + BAR_BYTES + EPI_STG_BYTES;
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, bool SYM>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmX, const TcParams p) {
@@ -796,7 +859,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_BN);
-            epilogue_tile<P_BN>(p, b, split, row, tn, tbase, g, x.buf, x, &tmX, abort_flag);
+            epilogue_tile<P_BN, SYM>(p, b, split, row, tn, tbase, g, x.buf, x, &tmX, abort_flag,
+                                     SYM && tm != tn);
             tc::fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(tempty_leader + acc * 8);
@@ -888,12 +952,12 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, 
     return NC_OK;
 }
 
-template <bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, bool SYM = false>
 int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, const TcParams& p,
             cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN>,
+        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN, SYM>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM),
                           "gemm_tc2 smem attribute"));
         attr = true;
@@ -911,7 +975,7 @@ int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx,
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    NC_TRY(cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN>, ma, mb, mx, p), "gemm_tc2 launch"));
+    NC_TRY(cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN, SYM>, ma, mb, mx, p), "gemm_tc2 launch"));
     note_launch();
     NC_LAUNCH_CHECK("gemm_tc2");
     return NC_OK;
@@ -1038,6 +1102,12 @@ bool gemm_tc_supported(const Gemm& g) {
 // CTA pairs (256 x 256 tiles) for every GEMM big enough to fill them.
 static bool use_pairs(const Gemm& g) { return g.M >= 256 && g.N >= 256; }
 
+double gemm_tc_work_fraction(const Gemm& g) {
+    if (!(g.sym && use_pairs(g) && g.M == g.N && g.epi == EPI_STORE && !g.a_t)) return 1.0;
+    const double t = ceil_div(g.M, 256);
+    return (t * (t + 1) / 2) / (t * t);
+}
+
 size_t gemm_tc_splitk_bytes(const Gemm& g) {
     const bool pair = use_pairs(g);
     const int bm = pair ? 256 : BM, bn = pair ? P_BN : (g.N > 128 ? 256 : 128);
@@ -1056,10 +1126,12 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     p.tiles_m = ceil_div(g.M, bm);
     p.tiles_n = ceil_div(g.N, bn);
     p.num_kb = ceil_div(g.K, BK);
-    p.splits = pick_splits(g, p.tiles_m * p.tiles_n, p.num_kb, pair ? num_sms() / 2 : num_sms());
+    p.sym = g.sym && pair && g.M == g.N && g.epi == EPI_STORE && !g.a_t;
+    p.splits = p.sym ? 1 : pick_splits(g, p.tiles_m * p.tiles_n, p.num_kb, pair ? num_sms() / 2 : num_sms());
     size_t need = p.splits > 1 ? (size_t)p.splits * g.batch * g.M * g.N * 4 : 0;
     if (need > ws_bytes || ws == nullptr) p.splits = 1;
-    p.units = (long)p.tiles_m * p.tiles_n * p.splits * g.batch;
+    p.units = p.sym ? (long)p.tiles_m * (p.tiles_m + 1) / 2 * g.batch
+                    : (long)p.tiles_m * p.tiles_n * p.splits * g.batch;
     p.C = g.C; p.ldc = g.ldc; p.sC = g.sC; p.c_dtype = g.c_dtype;
     p.aux = g.aux; p.ldaux = g.ldaux; p.sAux = g.sAux; p.aux_dtype = g.aux_dtype;
     p.alpha = g.alpha; p.beta = g.beta; p.epi = g.epi;
@@ -1085,7 +1157,9 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
 
     int rc;
     if (pair) {
-        if (!g.a_t && !g.b_t) rc = launch2<false, false>(ma, mb, mx, p, s);
+        if (p.sym && !g.a_t) rc = g.b_t ? launch2<false, true, true>(ma, mb, mx, p, s)
+                                        : launch2<false, false, true>(ma, mb, mx, p, s);
+        else if (!g.a_t && !g.b_t) rc = launch2<false, false>(ma, mb, mx, p, s);
         else if (!g.a_t && g.b_t) rc = launch2<false, true>(ma, mb, mx, p, s);
         else if (g.a_t && !g.b_t) rc = launch2<true, false>(ma, mb, mx, p, s);
         else rc = launch2<true, true>(ma, mb, mx, p, s);

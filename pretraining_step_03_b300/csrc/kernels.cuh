@@ -31,7 +31,13 @@ struct Gemm {
     int rope_T = 0, rope_cols = 0; //   row position = row % rope_T
     int rope_ld = 0;
     float* delta = nullptr;        // EPI_DELTA: [B, N/128, rope_T] row statistics (row = b*rope_T + t)
+    // C is symmetric (M == N, e.g. X X^T): the CTA-pair path computes only the 256 x 256
+    // tiles on and above the diagonal and writes each off-diagonal tile a second time,
+    // transposed.  Ignored (full computation) where the pair path does not apply.
+    bool sym = false;
 };
+// Fraction of the 2*M*N*K products gemm_tc executes for g (below 1 for symmetric C).
+double gemm_tc_work_fraction(const Gemm& g);
 
 int gemm_simt(const Gemm& g, cudaStream_t s);
 // 3-D bf16 TMA map over [batch][outer][inner], 128-byte swizzle, zero OOB fill.

@@ -42,18 +42,20 @@ def _muon_update_checks(prev, got, xref, what):
     assert np.all((proj[sel] >= 0.6) & (proj[sel] <= 1.3)), (what, proj[sel].min(), proj[sel].max())
 
 
-def test_d20_optimizer_step_matches_oracle():
+def _optimizer_parity(depth, d, h, v, sel, untouched, seed):
     from pretraining_step_03_b300.model import Model
-    m = Model(DEPTH, D, H, V, 1, 128, dtype="bf16", seed=3)
+    m = Model(depth, d, h, v, 1, 128, dtype="bf16", seed=seed)
     rng = np.random.default_rng(7)
-    w = {i: m.get_param(i).astype(np.float64) for i in SEL}
-    still = {i: m.get_param(i) for i in UNTOUCHED}
-    buf = {i: np.zeros_like(w[i]) for i in SEL}
-    am = {i: np.zeros_like(w[i]) for i in SEL}
-    av = {i: np.zeros_like(w[i]) for i in SEL}
+    last = 6 * depth + 1
+    w = {i: m.get_param(i).astype(np.float64) for i in sel}
+    still = {i: m.get_param(i) for i in untouched}
+    buf = {i: np.zeros_like(w[i]) for i in sel}
+    am = {i: np.zeros_like(w[i]) for i in sel}
+    av = {i: np.zeros_like(w[i]) for i in sel}
+    prev_g = {}
     for step in (1, 2):
         grads = {}
-        for i in SEL:
+        for i in sel:
             g = rng.normal(0.0, 1e-3, w[i].shape).astype(np.float32)
             if step == 2:   # correlated with step 1 so the momentum matters
                 g = (0.5 * prev_g[i] + g).astype(np.float32)
@@ -62,10 +64,10 @@ def test_d20_optimizer_step_matches_oracle():
         prev_g = grads
         m.muon_step(HP["muon_lr"], HP["momentum"], True, 5)
         m.adamw_step(HP["lr_emb"], HP["lr_unemb"], HP["beta1"], HP["beta2"], HP["eps"], HP["wd"], step)
-        for i in SEL:
+        for i in sel:
             g = grads[i].astype(np.float64)
             prev = w[i]
-            if i in (0, 6 * DEPTH + 1):
+            if i in (0, last):
                 lr = HP["lr_emb"] if i == 0 else HP["lr_unemb"]
                 ref, am[i], av[i] = oracle.adamw_step(prev, g, am[i], av[i], lr, HP["beta1"], HP["beta2"],
                                                       HP["eps"], HP["wd"], step)
@@ -78,6 +80,18 @@ def test_d20_optimizer_step_matches_oracle():
                 assert_close(got, ref, 0.999, 2e-2, f"step {step} Muon weight {i}")
                 _muon_update_checks(prev, got, xref, f"step {step} matrix {i} {got.shape}")
             w[i] = got   # both sides continue from the same weights
-        for i in UNTOUCHED:   # zero gradient: no update
+        for i in untouched:   # zero gradient: no update
             np.testing.assert_array_equal(m.get_param(i), still[i])
     assert m.check_flag() == 0
+
+
+def test_d20_optimizer_step_matches_oracle():
+    _optimizer_parity(DEPTH, D, H, V, SEL, UNTOUCHED, seed=3)
+
+
+def test_ragged_width_optimizer_step_matches_oracle():
+    """d_model 384 = 256 + 128: Newton-Schulz products with a ragged 256-tile edge
+    (the symmetric products mirror full and partial 32 x 32 chunks)."""
+    depth = 2
+    sel = [0, 1, 1 + 4, 1 + 5, 6 + 1 + 3, 6 * depth + 1]
+    _optimizer_parity(depth, 384, 3, 512, sel, [2, 6 + 1 + 1], seed=4)
