@@ -32,11 +32,13 @@ namespace {
 
 constexpr int BM = 128, BK = 64, NTHREADS = 320, GROUP_M = 8;
 constexpr int EPI_WARPS = 8;   // two groups of four, each owns half the tile columns
-// Per epilogue warp: two 4 KB buffers, each a 32 x 32 block (fp32 or bf16) laid out with
-// the 128-byte (fp32) / 64-byte (bf16) TMA swizzle.  They receive the auxiliary matrix by
-// TMA one chunk ahead and then serve as the staging of the coalesced store.
+// Per epilogue warp: 8 KB holding a ring of 32 x 32 blocks laid out with the 128-byte
+// (fp32, 4 KB) / 64-byte (bf16, 2 KB) TMA swizzle: two fp32 or four bf16 slots.  They
+// receive the auxiliary matrix by TMA, a whole tile's chunks ahead where they fit, and
+// then serve as the staging of the coalesced store.
 constexpr int EPI_BUF = 4096;
 constexpr int EPI_STG = 2 * EPI_BUF;
+constexpr int XSLOTS_MAX = 4;
 constexpr int EPI_STG_BYTES = EPI_WARPS * EPI_STG;
 constexpr int BAR_BYTES = 512;   // mbarriers, TMEM slot, abort flag (after the staging)
 
@@ -240,43 +242,54 @@ __device__ __forceinline__ void st16_bf16(bf16* dst, const float* v) {
 }
 
 // The auxiliary-matrix pipeline of one epilogue warp: 32 x 32 blocks come in by TMA
-// into its two buffers, one chunk ahead, in issue order.
+// into a ring of slots (two of 4 KB for fp32, four of 2 KB for bf16), consumed in
+// issue order.  Kept in three registers: the buffer's and the barriers' shared
+// addresses and a packed state word.
 struct XPipe {
-    uint8_t* buf;       // 2 x EPI_BUF
-    uint64_t* bar;      // 2 mbarriers (arrival count 1)
-    uint32_t phase;     // bit k: parity of buffer k's next completion
-    int issue, head;    // buffer of the next issue / of the oldest outstanding block
-    int pending;        // bit k: buffer k holds an issued, unconsumed block
+    uint32_t buf;       // shared address of the 8 KB ring
+    uint32_t bar;       // shared address of XSLOTS_MAX mbarriers (arrival count 1)
+    uint32_t st;        // bits 0-1 issue slot, 2-3 head slot, 4-7 phases, 8-11 pending, 12 fp32
+    __device__ __forceinline__ int slots() const { return (st >> 12) & 1 ? 2 : 4; }
+    __device__ __forceinline__ uint32_t bytes() const { return (st >> 12) & 1 ? 4096u : 2048u; }
+    __device__ __forceinline__ uint64_t* barp(int k) const {
+        return reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bar + 8 * k));
+    }
+    __device__ __forceinline__ uint8_t* bufp(int k) const {
+        return reinterpret_cast<uint8_t*>(__cvta_shared_to_generic(buf + k * bytes()));
+    }
 };
 
-__device__ __forceinline__ void x_issue(XPipe& x, const CUtensorMap* m, int n0, int row0, int b,
-                                        uint32_t bytes) {
-    const int k = x.issue;
-    x.issue ^= 1;
-    x.pending |= 1 << k;
-    __syncwarp();   // every lane is done with buffer k (aux read or store staging)
+__device__ __forceinline__ XPipe x_make(uint8_t* buf, uint64_t* bar, bool f32) {
+    return XPipe{tc::smem_u32(buf), tc::smem_u32(bar), f32 ? 1u << 12 : 0u};
+}
+
+__device__ __forceinline__ void x_issue(XPipe& x, const CUtensorMap* m, int n0, int row0, int b) {
+    const int k = x.st & 3;
+    const int nk = k + 1 == x.slots() ? 0 : k + 1;
+    x.st = (x.st & ~3u) | nk | (1u << (8 + k));
+    __syncwarp();   // every lane is done with slot k (aux read or store staging)
     if ((threadIdx.x & 31) == 0) {
         tc::fence_async_smem();   // those generic-proxy accesses before the TMA write
-        tc::mbar_expect_tx(&x.bar[k], bytes);
-        tc::tma_load_3d(x.buf + k * EPI_BUF, m, &x.bar[k], n0, row0, b);
+        tc::mbar_expect_tx(x.barp(k), x.bytes());
+        tc::tma_load_3d(x.bufp(k), m, x.barp(k), n0, row0, b);
     }
 }
 
 // The oldest outstanding block, once it has landed (null if the CTA aborted).
 __device__ __forceinline__ uint8_t* x_wait(XPipe& x, volatile int* abort) {
-    const int k = x.head;
-    if (!tc::mbar_wait_warp(&x.bar[k], (x.phase >> k) & 1, abort)) return nullptr;
-    x.head ^= 1;
-    x.phase ^= 1u << k;
-    x.pending &= ~(1 << k);
-    return x.buf + k * EPI_BUF;
+    const int k = (x.st >> 2) & 3;
+    if (!tc::mbar_wait_warp(x.barp(k), (x.st >> (4 + k)) & 1, abort)) return nullptr;
+    const int nk = k + 1 == x.slots() ? 0 : k + 1;
+    x.st = ((x.st & ~(3u << 2)) | (nk << 2)) ^ (1u << (4 + k));
+    x.st &= ~(1u << (8 + k));
+    return x.bufp(k);
 }
 
 // After an abort: let issued copies land before the CTA exits.
 __device__ __forceinline__ void x_drain(XPipe& x) {
     if ((threadIdx.x & 31) != 0) return;
-    for (int k = 0; k < 2; ++k)
-        if (x.pending & (1 << k)) tc::mbar_wait_drain(&x.bar[k], (x.phase >> k) & 1);
+    for (int k = 0; k < x.slots(); ++k)
+        if ((x.st >> (8 + k)) & 1) tc::mbar_wait_drain(x.barp(k), (x.st >> (4 + k)) & 1);
 }
 
 // This lane's 32 values of a TMA-loaded block (the layout of wst32's staging).
@@ -432,8 +445,8 @@ __device__ __forceinline__ void mirror32(const TcParams& p, uint8_t* stg, int b,
     wst32(stg, p.C, (long)b * p.sC + (long)n0 * p.ldc + r0, p.ldc, p.c_dtype, t);
 }
 
-// With p.aux_tma the block of the first chunk was issued by the caller; each chunk
-// issues the next one before waiting for its own.
+// With p.aux_tma the blocks of the first x.slots chunks were issued by the caller;
+// once a chunk is done, the block x.slots chunks ahead goes into its slot.
 // MIRROR (compile time, symmetric products only): also write the transposed copy of
 // each chunk when `mirror` (an off-diagonal tile).
 template <int BN, bool MIRROR>
@@ -442,7 +455,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
                                               const CUtensorMap* mx, volatile int* abort, bool mirror) {
     const int lane = threadIdx.x & 31;
     const bool rows_ok = __all_sync(0xffffffffu, row < p.M);
-    const uint32_t xbytes = p.aux_dtype == NC_FP32 ? 4096u : 2048u;
+    const int cend = (g + 1) * (BN / 64);
     if (p.epi == EPI_ROPE) {
         // chunk pairs (a, a+2) hold head-dim pairs (j, j+64) of one 128-wide head; each
         // is done in two 16-column halves (bounded registers), staged for coalesced stores
@@ -502,7 +515,6 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
             const uint8_t* xb = nullptr;
             float o[32];
             if (p.aux_tma) {
-                if (c + 1 < (g + 1) * (BN / 64)) x_issue(x, mx, n0 + 32, row - lane, b, xbytes);
                 if (!(xb = x_wait(x, abort))) break;
                 x_row(xb, NC_BF16, o);
             }
@@ -524,6 +536,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
                     dot = 0.f;
                 }
             }
+            if (p.aux_tma && c + x.slots() < cend) x_issue(x, mx, n0 + 32 * x.slots(), row - lane, b);
         }
     } else
 #pragma unroll 1
@@ -535,7 +548,6 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
         const uint8_t* xb = nullptr;
         float a[32];
         if (p.aux_tma) {
-            if (c + 1 < (g + 1) * (BN / 64)) x_issue(x, mx, n0 + 32, row - lane, b, xbytes);
             if (!(xb = x_wait(x, abort))) break;
             x_row(xb, p.aux_dtype, a);
         }
@@ -547,6 +559,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
             if (mirror && n0 < p.N)   // symmetric C: the transposed copy of this chunk (warp-uniform)
                 mirror32(p, xb ? const_cast<uint8_t*>(xb) : stg, b, row, n0, v, rows_ok && n0 + 32 <= p.N);
         }
+        if (p.aux_tma && c + x.slots() < cend) x_issue(x, mx, n0 + 32 * x.slots(), row - lane, b);
     }
 }
 
@@ -566,8 +579,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint64_t* xbar = drain + 1;   // [EPI_WARPS][2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2 * EPI_WARPS);
+    uint64_t* xbar = drain + 1;   // [EPI_WARPS][XSLOTS_MAX]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + XSLOTS_MAX * EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -581,7 +594,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(&tempty[a], EPI_WARPS * 32);
         }
         tc::mbar_init(drain, 1);
-        for (int i = 0; i < 2 * EPI_WARPS; ++i) tc::mbar_init(&xbar[i], 1);
+        for (int i = 0; i < XSLOTS_MAX * EPI_WARPS; ++i) tc::mbar_init(&xbar[i], 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch(&tmA);
@@ -679,20 +692,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3, g = (warp - 2) >> 2;
-        XPipe x{epi_smem + (warp - 2) * EPI_STG, xbar + 2 * (warp - 2), 0u, 0, 0, 0};
-        const uint32_t xbytes = p.aux_dtype == NC_FP32 ? 4096u : 2048u;
+        const bool xf32 = p.aux_dtype == NC_FP32;
+        XPipe x = x_make(epi_smem + (warp - 2) * EPI_STG, xbar + XSLOTS_MAX * (warp - 2), xf32);
         int acc = 0;
         uint32_t aph = 0;
         for (long u = blockIdx.x; u < p.units; u += gridDim.x) {
             int b, split, tm, tn;
             decode(p, u, b, split, tm, tn);
             const int row = tm * BM + q * 32 + lane;
-            // the first aux block of this tile comes in while the tile's MMAs run
-            if (p.aux_tma) x_issue(x, &tmX, tn * BN + g * (BN / 2), row - lane, b, xbytes);
+            if (p.aux_tma)   // this tile's first blocks come in while its MMAs run
+                for (int k = 0; k < x.slots() && k < BN / 64; ++k)
+                    x_issue(x, &tmX, tn * BN + g * (BN / 2) + 32 * k, row - lane, b);
             if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            epilogue_tile<BN, false>(p, b, split, row, tn, tbase, g, x.buf, x, &tmX, abort_flag, false);
+            epilogue_tile<BN, false>(p, b, split, row, tn, tbase, g, x.bufp(0), x, &tmX, abort_flag, false);
             tc::fence_before();
             tc::mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -739,8 +753,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint64_t* xbar = drain + 1;   // [EPI_WARPS][2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2 * EPI_WARPS);
+    uint64_t* xbar = drain + 1;   // [EPI_WARPS][XSLOTS_MAX]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + XSLOTS_MAX * EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -756,7 +770,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc::mbar_init(&tempty[a], 2 * EPI_WARPS);   // every epilogue warp of both CTAs
         }
         tc::mbar_init(drain, 1);
-        for (int i = 0; i < 2 * EPI_WARPS; ++i) tc::mbar_init(&xbar[i], 1);
+        for (int i = 0; i < XSLOTS_MAX * EPI_WARPS; ++i) tc::mbar_init(&xbar[i], 1);
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch(&tmA);
@@ -845,8 +859,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue (both CTAs)
         const int q = warp & 3, g = (warp - 2) >> 2;
-        XPipe x{epi_smem + (warp - 2) * EPI_STG, xbar + 2 * (warp - 2), 0u, 0, 0, 0};
-        const uint32_t xbytes = p.aux_dtype == NC_FP32 ? 4096u : 2048u;
+        const bool xf32 = p.aux_dtype == NC_FP32;
+        XPipe x = x_make(epi_smem + (warp - 2) * EPI_STG, xbar + XSLOTS_MAX * (warp - 2), xf32);
         const uint32_t tempty_leader = tc::mapa(tc::smem_u32(&tempty[0]), 0);
         int acc = 0;
         uint32_t aph = 0;
@@ -854,12 +868,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             int b, split, tm, tn;
             decode(p, u, b, split, tm, tn);
             const int row = tm * 256 + (int)rank * 128 + q * 32 + lane;
-            // the first aux block of this tile comes in while the tile's MMAs run
-            if (p.aux_tma) x_issue(x, &tmX, tn * P_BN + g * (P_BN / 2), row - lane, b, xbytes);
+            if (p.aux_tma)   // this tile's first blocks come in while its MMAs run
+                for (int k = 0; k < x.slots() && k < P_BN / 64; ++k)
+                    x_issue(x, &tmX, tn * P_BN + g * (P_BN / 2) + 32 * k, row - lane, b);
             if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_BN);
-            epilogue_tile<P_BN, SYM>(p, b, split, row, tn, tbase, g, x.buf, x, &tmX, abort_flag,
+            epilogue_tile<P_BN, SYM>(p, b, split, row, tn, tbase, g, x.bufp(0), x, &tmX, abort_flag,
                                      SYM && tm != tn);
             tc::fence_before();
             __syncwarp();
