@@ -67,6 +67,7 @@ struct nc_model {
     void* yf;
     float* rf;
     void* logits;      // [M, V]
+    float2* lse_part;  // [M, V/128] (max, sum exp) partials from the LM-head GEMM (bf16 mode)
     float* nll;
     float* g;          // residual gradient fp32 [M, d]
     void* gT;          // its act-type copy (bf16 mode)
@@ -161,6 +162,7 @@ void layout(nc_model* m, char* base, size_t* total) {
         m->yf = c.take(M * d * act);
         m->rf = (float*)c.take(M * 4);
         m->logits = c.take(M * V * act);
+        m->lse_part = m->dtype == NC_BF16 && V % 128 == 0 ? (float2*)c.take((size_t)M * (V / 128) * 8) : nullptr;
         m->nll = (float*)c.take(M * 4);
         m->g = (float*)c.take(M * d * 4);
         m->gT = m->dtype == NC_BF16 ? c.take(M * d * act) : nullptr;
@@ -321,10 +323,21 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         }
     }
     NC_TRY(norm_f(m->x, m->yf, m->rf));
-    NC_TRY(run_gemm(m, mk(m, M, V, d, m->yf, d, false, W<T>(m, iu), d, false, m->logits, V, act)));
+    const float2* lse_part = nullptr;
+    {   // logits; in bf16 mode the epilogue also leaves each row's softmax partials
+        Gemm g = mk(m, M, V, d, m->yf, d, false, W<T>(m, iu), d, false, m->logits, V, act);
+        if (m->lse_part) {
+            g.epi = EPI_LSE;
+            g.lse_part = m->lse_part;
+            if (gemm_tc_supported(g)) lse_part = m->lse_part;
+            else g.epi = EPI_STORE;
+        }
+        NC_TRY(run_gemm(m, g));
+    }
     {
         Prof pr(m, NC_PROF_CE, 0, 2.0 * M * V * ab + M * 16.0);
-        NC_TRY(cross_entropy<T>((T*)m->logits, tgt, m->nll, M, V, grad_scale / (float)M, m->flag, s));
+        NC_TRY(cross_entropy<T>((T*)m->logits, tgt, m->nll, M, V, grad_scale / (float)M, m->flag, s,
+                                lse_part));
         NC_TRY(loss_reduce(m->nll, tgt, tb, M, V, out, m->flag, s));
     }
 

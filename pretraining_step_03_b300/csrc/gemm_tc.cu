@@ -57,6 +57,7 @@ struct TcParams {
     float* delta;
     int aux_tma;      // the auxiliary matrix comes through the per-warp TMA buffers
     int sym;          // symmetric C: upper-triangle tiles only, mirrored (tiles_m == tiles_n)
+    float2* lse_part; // EPI_LSE: [M][N/128] (max, sum exp) partials
 };
 
 template <int BN> struct Cfg {
@@ -447,16 +448,23 @@ __device__ __forceinline__ void mirror32(const TcParams& p, uint8_t* stg, int b,
 
 // With p.aux_tma the blocks of the first x.slots chunks were issued by the caller;
 // once a chunk is done, the block x.slots chunks ahead goes into its slot.
+// Epilogue families a kernel instance is compiled for (each instance carries only its
+// own epilogue code, which keeps the register budget of the others).
+enum EpiFamily { EF_ANY = 0, EF_GEN = 1, EF_ROPE = 2, EF_DELTA = 3, EF_LSE = 4 };
+constexpr int epi_family(int epi) {
+    return epi == EPI_ROPE ? EF_ROPE : epi == EPI_DELTA ? EF_DELTA : epi == EPI_LSE ? EF_LSE : EF_GEN;
+}
+
 // MIRROR (compile time, symmetric products only): also write the transposed copy of
 // each chunk when `mirror` (an off-diagonal tile).
-template <int BN, bool MIRROR>
+template <int BN, bool MIRROR, int EF = EF_ANY>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int split, int row, int tn,
                                               uint32_t tbase, int g, uint8_t* stg, XPipe& x,
                                               const CUtensorMap* mx, volatile int* abort, bool mirror) {
     const int lane = threadIdx.x & 31;
     const bool rows_ok = __all_sync(0xffffffffu, row < p.M);
     const int cend = (g + 1) * (BN / 64);
-    if (p.epi == EPI_ROPE) {
+    if ((EF == EF_ANY || EF == EF_ROPE) && p.epi == EPI_ROPE) {
         // chunk pairs (a, a+2) hold head-dim pairs (j, j+64) of one 128-wide head; each
         // is done in two 16-column halves (bounded registers), staged for coalesced stores
         uint8_t* stg_b = stg + 2048;
@@ -502,7 +510,39 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
                 flush_bf16(stg_b, p.C, ci + 64 - (long)lane * p.ldc, p.ldc);
             }
         }
-    } else if (p.epi == EPI_DELTA) {
+    } else if ((EF == EF_ANY || EF == EF_LSE) && p.epi == EPI_LSE) {
+        // logits (bf16) out, and this row's (max, sum exp(z - max)) over the 128 columns of
+        // this half of the tile, taken over the rounded values the cross-entropy will read
+        constexpr float L2E = 1.4426950408889634f;
+        float mx = -INFINITY, se = 0.f;
+#pragma unroll 1
+        for (int c = g * (BN / 64); c < (g + 1) * (BN / 64); ++c) {
+            float v[32];
+            tc::tmem_ld32(tbase + c * 32, reinterpret_cast<uint32_t*>(v));
+            tc::tmem_wait_ld();
+            const int n0 = tn * BN + c * 32;
+            if (n0 < p.N) {   // warp-uniform
+                float cm = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * p.alpha));
+                    cm = fmaxf(cm, v[j]);
+                }
+                if (cm > mx) {
+                    se = mx == -INFINITY ? 0.f : se * exp2f((mx - cm) * L2E);
+                    mx = cm;
+                }
+                const float ml = mx * L2E;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) se += exp2f(fmaf(v[j], L2E, -ml));
+                const long ci = (long)b * p.sC + (long)row * p.ldc + n0;
+                if (rows_ok) wst32(stg, p.C, ci - (long)lane * p.ldc, p.ldc, NC_BF16, v);
+                else if (row < p.M) st32(p.C, ci, NC_BF16, v);
+            }
+        }
+        const int grp = (tn * BN + g * (BN / 2)) / 128;
+        if (row < p.M && grp * 128 < p.N) p.lse_part[(long)row * (p.N / 128) + grp] = make_float2(mx, se);
+    } else if ((EF == EF_ANY || EF == EF_DELTA) && p.epi == EPI_DELTA) {
         // dO (bf16) out; per 128-column head the dot product with O (aux) of the
         // rounded values, i.e. exactly what the attention backward will consume
         float dot = 0.f;
@@ -738,7 +778,7 @@ constexpr int P_A_BYTES = 128 * BK * 2, P_B_BYTES = 128 * BK * 2;
 constexpr int P_STAGE = P_A_BYTES + P_B_BYTES;
 constexpr int P_SMEM = P_STAGES * P_STAGE + 1024 + BAR_BYTES + EPI_STG_BYTES;
 
-template <bool A_MN, bool B_MN, bool SYM>
+template <bool A_MN, bool B_MN, bool SYM, int EF>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmX, const TcParams p) {
@@ -874,7 +914,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_BN);
-            epilogue_tile<P_BN, SYM>(p, b, split, row, tn, tbase, g, x.bufp(0), x, &tmX, abort_flag,
+            epilogue_tile<P_BN, SYM, EF>(p, b, split, row, tn, tbase, g, x.bufp(0), x, &tmX, abort_flag,
                                      SYM && tm != tn);
             tc::fence_before();
             __syncwarp();
@@ -967,12 +1007,12 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, 
     return NC_OK;
 }
 
-template <bool A_MN, bool B_MN, bool SYM = false>
+template <bool A_MN, bool B_MN, bool SYM = false, int EF = EF_GEN>
 int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, const TcParams& p,
             cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN, SYM>,
+        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN, SYM, EF>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM),
                           "gemm_tc2 smem attribute"));
         attr = true;
@@ -990,7 +1030,7 @@ int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx,
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    NC_TRY(cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN, SYM>, ma, mb, mx, p), "gemm_tc2 launch"));
+    NC_TRY(cuda_check(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<A_MN, B_MN, SYM, EF>, ma, mb, mx, p), "gemm_tc2 launch"));
     note_launch();
     NC_LAUNCH_CHECK("gemm_tc2");
     return NC_OK;
@@ -1108,6 +1148,11 @@ bool gemm_tc_supported(const Gemm& g) {
     if (g.N % 8) return false;
     if (g.epi == EPI_ROPE && (g.N % 128 || !g.rope || g.rope_T <= 0 || g.rope_ld < g.rope_T ||
                               g.c_dtype != NC_BF16)) return false;
+    if (g.epi == EPI_LSE && (g.N % 128 || g.N < 256 || !g.lse_part || g.c_dtype != NC_BF16 || g.batch != 1))
+        return false;
+    // the CTA-pair instances of the special epilogues exist for the layouts the step uses
+    if ((g.epi == EPI_ROPE || g.epi == EPI_LSE) && (g.a_t || g.b_t)) return false;
+    if (g.epi == EPI_DELTA && (g.a_t || !g.b_t)) return false;
     if (g.epi == EPI_DELTA && (g.N % 128 || g.N < 256 || !g.delta || !g.aux || g.rope_T <= 0 || g.c_dtype != NC_BF16 ||
                                g.aux_dtype != NC_BF16 || g.batch != 1))
         return false;
@@ -1153,6 +1198,7 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     p.ws = p.splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
     p.flag = g_gemm_flag;
     p.rope = g.rope; p.rope_T = g.rope_T; p.rope_cols = g.rope_cols; p.rope_ld = g.rope_ld; p.delta = g.delta;
+    p.lse_part = g.lse_part;
 
     // the auxiliary matrix by TMA (32 x 32 blocks, 128 / 64-byte swizzle) when the
     // epilogue reads one and its layout allows the copy
@@ -1172,8 +1218,12 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
 
     int rc;
     if (pair) {
+        const int ef = epi_family(g.epi);
         if (p.sym && !g.a_t) rc = g.b_t ? launch2<false, true, true>(ma, mb, mx, p, s)
                                         : launch2<false, false, true>(ma, mb, mx, p, s);
+        else if (ef == EF_ROPE) rc = launch2<false, false, false, EF_ROPE>(ma, mb, mx, p, s);
+        else if (ef == EF_LSE) rc = launch2<false, false, false, EF_LSE>(ma, mb, mx, p, s);
+        else if (ef == EF_DELTA) rc = launch2<false, true, false, EF_DELTA>(ma, mb, mx, p, s);
         else if (!g.a_t && !g.b_t) rc = launch2<false, false>(ma, mb, mx, p, s);
         else if (!g.a_t && g.b_t) rc = launch2<false, true>(ma, mb, mx, p, s);
         else if (g.a_t && !g.b_t) rc = launch2<true, false>(ma, mb, mx, p, s);

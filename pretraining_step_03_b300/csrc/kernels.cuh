@@ -16,6 +16,8 @@ enum EpiKind {
     EPI_RELU2_BWD = 2,  // C = alpha*acc * 2*sqrt(aux)          (aux = a = relu(h)^2, so 2 sqrt(a) = 2 relu(h))
     EPI_ROPE = 3,       // C = alpha*acc with columns < rope_cols rotated by RoPE (head dim 128)
     EPI_DELTA = 4,      // C = alpha*acc (bf16) and delta[b, h, t] = sum over head h of bf16(C) * aux
+    EPI_LSE = 5,        // C = alpha*acc (bf16) and, per row and 128-column group k, lse_part[row][k] =
+                        //   (max z, sum exp(z - max)) over the stored (rounded) values z
 };
 
 struct Gemm {
@@ -35,6 +37,7 @@ struct Gemm {
     // tiles on and above the diagonal and writes each off-diagonal tile a second time,
     // transposed.  Ignored (full computation) where the pair path does not apply.
     bool sym = false;
+    float2* lse_part = nullptr;    // EPI_LSE: [M][N/128]
 };
 // Fraction of the 2*M*N*K products gemm_tc executes for g (below 1 for symmetric C).
 double gemm_tc_work_fraction(const Gemm& g);
@@ -63,10 +66,12 @@ int rmsnorm_backward(const T* dy, const T* y, const float* r, const float* g_in,
 template <typename T>
 int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* table, int table_ld, float sign,
                cudaStream_t s);
-// logits [M, V] -> dlogits in place; nll [M]
+// logits [M, V] -> dlogits in place; nll [M].  lse_part (bf16 only, optional): the
+// per-row (max, sum exp) partials of every 128-column group, left by the LM-head GEMM
+// (EPI_LSE); with them the logits are read once instead of twice.
 template <typename T>
 int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float scale,
-                  uint32_t* flag, cudaStream_t s);
+                  uint32_t* flag, cudaStream_t s, const float2* lse_part = nullptr);
 int loss_reduce(const float* nll, const int32_t* tgt, const int32_t* token_bytes, int M, int V,
                 float* out, uint32_t* flag, cudaStream_t s);
 struct EmbedBwdWs {

@@ -268,6 +268,69 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_online_kernel(bf16* z, const i
     }
 }
 
+// The same with the per-row (max, sum exp) partials of every 128-column group already
+// left by the LM-head GEMM's epilogue: combine them (fixed order), then one pass that
+// writes dlogits = scale * (softmax - onehot) over the logits in place.
+__global__ void __launch_bounds__(CE2_THREADS) ce_stats_kernel(bf16* z, const float2* part, const int32_t* tgt,
+                                                               float* nll, int V, float scale, uint32_t* flag) {
+    __shared__ float shm[32], shs[32];
+    __shared__ float zt_s, lse_s;
+    const long row = blockIdx.x;
+    const int ng = V / 128;
+    uint4* zr = reinterpret_cast<uint4*>(z + row * V);
+    const int nv = V / (8 * CE2_THREADS);
+    const int t = tgt[row];
+    const bool ok = t >= 0 && t < V;
+    if (threadIdx.x == 0) {
+        if (!ok) flag_set(flag, NC_FLAG_TOKEN_RANGE);
+        zt_s = ok ? __bfloat162float(z[row * V + t]) : 0.f;
+    }
+    float m = -INFINITY, se = 0.f;
+    for (int k = threadIdx.x; k < ng; k += CE2_THREADS) {
+        const float2 ps = part[row * ng + k];
+        ms_combine(m, se, ps.x, ps.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, se, o);
+        ms_combine(m, se, m2, s2);
+    }
+    const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
+    if (lane == 0) { shm[wid] = m; shs[wid] = se; }
+    __syncthreads();
+    if (wid == 0) {
+        float m1 = lane < CE2_THREADS / 32 ? shm[lane] : -INFINITY;
+        float s1 = lane < CE2_THREADS / 32 ? shs[lane] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m1, o), s2 = __shfl_xor_sync(0xffffffffu, s1, o);
+            ms_combine(m1, s1, m2, s2);
+        }
+        if (lane == 0) {
+            lse_s = m1 + logf(s1);
+            nll[row] = ok ? lse_s - zt_s : 0.f;
+        }
+    }
+    __syncthreads();   // zt_s was read before any thread overwrites z
+    const float lsel = lse_s * CE_LOG2E;
+#pragma unroll 4
+    for (int k = 0; k < nv; ++k) {
+        const int base = (threadIdx.x + k * CE2_THREADS) * 8;
+        const uint4 u = zr[threadIdx.x + k * CE2_THREADS];
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            float p0 = exp2f(fmaf(f.x, CE_LOG2E, -lsel)), p1 = exp2f(fmaf(f.y, CE_LOG2E, -lsel));
+            if (base + 2 * e == t) p0 -= 1.f;
+            if (base + 2 * e + 1 == t) p1 -= 1.f;
+            __nv_bfloat162 h = __floats2bfloat162_rn(p0 * scale, p1 * scale);
+            w[e] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        zr[threadIdx.x + k * CE2_THREADS] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // Single CTA, fixed summation order: loss = mean nll; bpb = sum(nll | bytes>0) / (ln2 * sum bytes).
 __global__ void loss_reduce_kernel(const float* nll, const int32_t* tgt, const int32_t* tb, int M,
                                    int V, float* out, uint32_t* flag) {
@@ -472,9 +535,15 @@ int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* tabl
 
 template <typename T>
 int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float scale,
-                  uint32_t* flag, cudaStream_t s) {
+                  uint32_t* flag, cudaStream_t s, const float2* lse_part) {
     if (M <= 0) return NC_OK;
     if constexpr (sizeof(T) == 2) {
+        if (lse_part && V % (8 * CE2_THREADS) == 0 && V % 128 == 0 && (uintptr_t)logits % 16 == 0) {
+            ce_stats_kernel<<<M, CE2_THREADS, 0, s>>>(logits, lse_part, tgt, nll, V, scale, flag);
+            note_launch();
+            NC_LAUNCH_CHECK("cross_entropy");
+            return NC_OK;
+        }
         if (V % (8 * CE2_THREADS) == 0 && (uintptr_t)logits % 16 == 0) {
             ce_online_kernel<<<M, CE2_THREADS, 0, s>>>(logits, tgt, nll, V, scale, flag);
             note_launch();
@@ -551,7 +620,7 @@ int cast_f32_bf16(const float* x, bf16* y, long n, cudaStream_t s) {
                                      T*, int, int, cudaStream_t);                               \
     template int rope_apply<T>(T*, long, int, int, int, int, const float2*, int, float, cudaStream_t); \
     template int cross_entropy<T>(T*, const int32_t*, float*, int, int, float, uint32_t*,       \
-                                  cudaStream_t);
+                                  cudaStream_t, const float2*);
 NC_INST(float)
 NC_INST(bf16)
 #undef NC_INST
