@@ -72,6 +72,38 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* m, ui
     tc::tma_load_3d(dst + ATOM, m, bar, col0 + 64, row0, 0);
 }
 
+// Two fp32 lanes in one 64-bit register for the packed f32x2 arithmetic, and the
+// single-instruction base-2 exponential (approximate, flush-to-zero: the
+// probabilities it produces are rounded to bf16 anyway).
+__device__ __forceinline__ uint64_t f2pk(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2upk(uint64_t v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float ex2a(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -359,20 +391,30 @@ __global__ void __launch_bounds__(NT, 1)
                 l *= alpha;
                 m2 = mx;
             }
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            // P_t(j) packed into the first 64 columns of S_t; scale, shift and the row sum
+            // two lanes at a time
+            const uint64_t c22 = f2pk(c2, c2), nm2 = f2pk(-m2, -m2);
+            uint64_t sum2[2] = {f2pk(0.f, 0.f), f2pk(0.f, 0.f)};
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {   // P_t(j) packed into the first 64 columns of S_t
+            for (int h2 = 0; h2 < 2; ++h2) {
                 uint32_t w[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float a = exp2f(fmaf(s[64 * h2 + 2 * i], c2, -m2));
-                    const float bb = exp2f(fmaf(s[64 * h2 + 2 * i + 1], c2, -m2));
-                    sum4[i & 3] += a + bb;
+                    float a, bb;
+                    f2upk(ffma2(f2pk(s[64 * h2 + 2 * i], s[64 * h2 + 2 * i + 1]), c22, nm2), a, bb);
+                    a = ex2a(a);
+                    bb = ex2a(bb);
+                    sum2[i & 1] = fadd2(sum2[i & 1], f2pk(a, bb));
                     w[i] = pack2(a, bb);
                 }
                 tc::tmem_st32(sb + 32 * h2, w);
             }
-            l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+            {
+                float x0, x1, y0, y1;
+                f2upk(sum2[0], x0, x1);
+                f2upk(sum2[1], y0, y1);
+                l += (x0 + x1) + (y0 + y1);
+            }
             if (__any_sync(0xffffffffu, need)) {
                 // O_t is still (S_t(j) was issued after PV_t(j-1) completed): rescale in place
 #pragma unroll 1
@@ -680,13 +722,13 @@ __global__ void __launch_bounds__(NT, 1)
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
             const int j = kb + i;
-            float* stat = sm.xch + (i & 1) * 256;          // [lse2 | D] of this query block
+            float* stat = sm.xch + (i & 1) * 256;          // [-lse2 | -D] of this query block
             {
                 const float cur = nxt;
                 if (i + 1 < nq) nxt = fetch(j + 1);
                 const bool valid = j * BR + r < p.T;
-                if (g == 0) stat[r] = valid ? cur * LOG2E : INFINITY;
-                else stat[128 + r] = valid ? cur : 0.f;
+                if (g == 0) stat[r] = valid ? -cur * LOG2E : -INFINITY;
+                else stat[128 + r] = valid ? -cur : 0.f;
             }
             tc::mbar_arrive(&sbar[i & 1]);
             if (!(ok = tc::mbar_wait_warp(&sbar[i & 1], (i >> 1) & 1, sm.abort))) break;
@@ -696,18 +738,19 @@ __global__ void __launch_bounds__(NT, 1)
             tc::fence_before();
             tc::mbar_arrive(s_free);
             // P^T[r][c] = exp2(S^T*c2 - lse2[c]), zero where key r > query c; this
-            // thread's columns are two contiguous runs of 32 (statistics as float4)
+            // thread's columns are two contiguous runs of 32 (statistics as pairs), the
+            // scale and shift two lanes at a time
+            const uint64_t c22 = f2pk(c2, c2);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-                const float4* l4 = reinterpret_cast<const float4*>(stat + 64 * h2 + 32 * g);
+                const uint64_t* l2 = reinterpret_cast<const uint64_t*>(stat + 64 * h2 + 32 * g);
 #pragma unroll
-                for (int k4 = 0; k4 < 8; ++k4) {
-                    const float4 lv = l4[k4];
-                    float* x = s + 32 * h2 + 4 * k4;
-                    x[0] = exp2f(fmaf(x[0], c2, -lv.x));
-                    x[1] = exp2f(fmaf(x[1], c2, -lv.y));
-                    x[2] = exp2f(fmaf(x[2], c2, -lv.z));
-                    x[3] = exp2f(fmaf(x[3], c2, -lv.w));
+                for (int k2 = 0; k2 < 16; ++k2) {
+                    float* x = s + 32 * h2 + 2 * k2;
+                    float a, bb;
+                    f2upk(ffma2(f2pk(x[0], x[1]), c22, l2[k2]), a, bb);
+                    x[0] = ex2a(a);
+                    x[1] = ex2a(bb);
                 }
             }
             if (i == 0) {
@@ -738,16 +781,16 @@ __global__ void __launch_bounds__(NT, 1)
                         tc::tmem_ld32(tmem + lanes + 192 + 32 * g, d);
                         tc::tmem_wait_ld();
                     }
-                    const float4* d4 = reinterpret_cast<const float4*>(stat + 128 + 64 * h2 + 32 * g);
+                    const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(stat + 128 + 64 * h2 + 32 * g);
 #pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4) {
-                        const float4 dv4 = d4[k4];
-                        const float* x = s + 32 * h2 + 4 * k4;
-                        const uint32_t* y = d + 4 * k4;
-                        wd[16 * h2 + 2 * k4] = pack2(x[0] * (__uint_as_float(y[0]) - dv4.x),
-                                                     x[1] * (__uint_as_float(y[1]) - dv4.y));
-                        wd[16 * h2 + 2 * k4 + 1] = pack2(x[2] * (__uint_as_float(y[2]) - dv4.z),
-                                                         x[3] * (__uint_as_float(y[3]) - dv4.w));
+                    for (int k2 = 0; k2 < 16; ++k2) {   // (dP^T - D) * P^T, two lanes at a time
+                        const float* x = s + 32 * h2 + 2 * k2;
+                        const uint32_t* y = d + 2 * k2;
+                        float a, bb;
+                        f2upk(fmul2(f2pk(x[0], x[1]),
+                                    fadd2(f2pk(__uint_as_float(y[0]), __uint_as_float(y[1])), nd2[k2])),
+                              a, bb);
+                        wd[16 * h2 + k2] = pack2(a, bb);
                     }
                 }
             }
