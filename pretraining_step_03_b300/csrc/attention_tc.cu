@@ -72,38 +72,6 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* m, ui
     tc::tma_load_3d(dst + ATOM, m, bar, col0 + 64, row0, 0);
 }
 
-// Two fp32 lanes in one 64-bit register for the packed f32x2 arithmetic, and the
-// single-instruction base-2 exponential (approximate, flush-to-zero: the
-// probabilities it produces are rounded to bf16 anyway).
-__device__ __forceinline__ uint64_t f2pk(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void f2upk(uint64_t v, float& a, float& b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ float ex2a(float x) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -380,7 +348,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < 128; ++i) m4[i & 3] = fmaxf(m4[i & 3], s[i]);
+            for (int i = 0; i < 128; i += 2) m4[(i >> 1) & 3] = tc::fmax3(m4[(i >> 1) & 3], s[i], s[i + 1]);
             const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c2;   // log2 units
             // the running max moves only when it grows by more than 2^8 (P stays <= 256)
             const bool need = j > 0 && mx > m2 + 8.f;
@@ -393,26 +361,26 @@ __global__ void __launch_bounds__(NT, 1)
             }
             // P_t(j) packed into the first 64 columns of S_t; scale, shift and the row sum
             // two lanes at a time
-            const uint64_t c22 = f2pk(c2, c2), nm2 = f2pk(-m2, -m2);
-            uint64_t sum2[2] = {f2pk(0.f, 0.f), f2pk(0.f, 0.f)};
+            const uint64_t c22 = tc::f2pk(c2, c2), nm2 = tc::f2pk(-m2, -m2);
+            uint64_t sum2[2] = {tc::f2pk(0.f, 0.f), tc::f2pk(0.f, 0.f)};
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 uint32_t w[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     float a, bb;
-                    f2upk(ffma2(f2pk(s[64 * h2 + 2 * i], s[64 * h2 + 2 * i + 1]), c22, nm2), a, bb);
-                    a = ex2a(a);
-                    bb = ex2a(bb);
-                    sum2[i & 1] = fadd2(sum2[i & 1], f2pk(a, bb));
+                    tc::f2upk(tc::ffma2(tc::f2pk(s[64 * h2 + 2 * i], s[64 * h2 + 2 * i + 1]), c22, nm2), a, bb);
+                    a = tc::ex2a(a);
+                    bb = tc::ex2a(bb);
+                    sum2[i & 1] = tc::fadd2(sum2[i & 1], tc::f2pk(a, bb));
                     w[i] = pack2(a, bb);
                 }
                 tc::tmem_st32(sb + 32 * h2, w);
             }
             {
                 float x0, x1, y0, y1;
-                f2upk(sum2[0], x0, x1);
-                f2upk(sum2[1], y0, y1);
+                tc::f2upk(sum2[0], x0, x1);
+                tc::f2upk(sum2[1], y0, y1);
                 l += (x0 + x1) + (y0 + y1);
             }
             if (__any_sync(0xffffffffu, need)) {
@@ -740,7 +708,7 @@ __global__ void __launch_bounds__(NT, 1)
             // P^T[r][c] = exp2(S^T*c2 - lse2[c]), zero where key r > query c; this
             // thread's columns are two contiguous runs of 32 (statistics as pairs), the
             // scale and shift two lanes at a time
-            const uint64_t c22 = f2pk(c2, c2);
+            const uint64_t c22 = tc::f2pk(c2, c2);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const uint64_t* l2 = reinterpret_cast<const uint64_t*>(stat + 64 * h2 + 32 * g);
@@ -748,9 +716,9 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int k2 = 0; k2 < 16; ++k2) {
                     float* x = s + 32 * h2 + 2 * k2;
                     float a, bb;
-                    f2upk(ffma2(f2pk(x[0], x[1]), c22, l2[k2]), a, bb);
-                    x[0] = ex2a(a);
-                    x[1] = ex2a(bb);
+                    tc::f2upk(tc::ffma2(tc::f2pk(x[0], x[1]), c22, l2[k2]), a, bb);
+                    x[0] = tc::ex2a(a);
+                    x[1] = tc::ex2a(bb);
                 }
             }
             if (i == 0) {
@@ -787,8 +755,8 @@ __global__ void __launch_bounds__(NT, 1)
                         const float* x = s + 32 * h2 + 2 * k2;
                         const uint32_t* y = d + 2 * k2;
                         float a, bb;
-                        f2upk(fmul2(f2pk(x[0], x[1]),
-                                    fadd2(f2pk(__uint_as_float(y[0]), __uint_as_float(y[1])), nd2[k2])),
+                        tc::f2upk(tc::fmul2(tc::f2pk(x[0], x[1]),
+                                    tc::fadd2(tc::f2pk(__uint_as_float(y[0]), __uint_as_float(y[1])), nd2[k2])),
                               a, bb);
                         wd[16 * h2 + k2] = pack2(a, bb);
                     }

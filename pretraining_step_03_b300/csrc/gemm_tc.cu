@@ -522,19 +522,30 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
             tc::tmem_wait_ld();
             const int n0 = tn * BN + c * 32;
             if (n0 < p.N) {   // warp-uniform
-                float cm = -INFINITY;
+                float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * p.alpha));
-                    cm = fmaxf(cm, v[j]);
-                }
+                for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * p.alpha));
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) c4[(j >> 1) & 3] = tc::fmax3(c4[(j >> 1) & 3], v[j], v[j + 1]);
+                const float cm = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
                 if (cm > mx) {
-                    se = mx == -INFINITY ? 0.f : se * exp2f((mx - cm) * L2E);
+                    se = mx == -INFINITY ? 0.f : se * tc::ex2a((mx - cm) * L2E);
                     mx = cm;
                 }
-                const float ml = mx * L2E;
+                // sum of exp2(v * log2 e - mx * log2 e), two lanes at a time
+                const uint64_t l2 = tc::f2pk(L2E, L2E), nml = tc::f2pk(-mx * L2E, -mx * L2E);
+                uint64_t s2 = tc::f2pk(0.f, 0.f);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) se += exp2f(fmaf(v[j], L2E, -ml));
+                for (int j = 0; j < 32; j += 2) {
+                    float e0, e1;
+                    tc::f2upk(tc::ffma2(tc::f2pk(v[j], v[j + 1]), l2, nml), e0, e1);
+                    s2 = tc::fadd2(s2, tc::f2pk(tc::ex2a(e0), tc::ex2a(e1)));
+                }
+                {
+                    float x0, x1;
+                    tc::f2upk(s2, x0, x1);
+                    se += x0 + x1;
+                }
                 const long ci = (long)b * p.sC + (long)row * p.ldc + n0;
                 if (rows_ok) wst32(stg, p.C, ci - (long)lane * p.ldc, p.ldc, NC_BF16, v);
                 else if (row < p.M) st32(p.C, ci, NC_BF16, v);
