@@ -285,9 +285,8 @@ def main():
     if args.workload in ("attn", "optim", "gemm"):
         return kernel_workload(args)
     w = WORKLOADS[args.workload]
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from pretraining_step_03_b300 import replicas
+    rank, world, local = replicas.rank_env()
     tokens_per_step = w["B"] * w["T"] * w["n_micro"]
     fpt = shapes.flops_per_token(w["depth"], w["d_model"], w["vocab"], w["T"])
     fpt_causal = shapes.flops_per_token(w["depth"], w["d_model"], w["vocab"], w["T"], causal=True)
@@ -330,7 +329,7 @@ def main():
 
     # ------------------------------------------------ inputs (seeded per rank)
     nm, B, T = w["n_micro"], w["B"], w["T"]
-    tok, tgt = synth.zipf_rows(nm * B, T, w["vocab"], seed=1 + rank)
+    tok, tgt = synth.zipf_rows(nm * B, T, w["vocab"], seed=replicas.data_seed(rank))
     tb_host = synth.token_bytes_binomial(w["vocab"], seed=2)
     m = Model(w["depth"], w["d_model"], w["n_head"], w["vocab"], B, T, dtype="bf16", seed=0, device=dev)
     tb = torch.from_numpy(tb_host).to(dev)
@@ -369,11 +368,7 @@ def main():
     launches = L.nc_launch_count() - launches0
     clk = clocks.stop()
     L.nc_profile(m.h, 0)
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = replicas.max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
     loss = loss_d.cpu().numpy().mean(axis=0)
     flag = m.check_flag()
     pk = peaks()
@@ -417,15 +412,11 @@ def main():
     for i in range(args.steps):
         host_step(1001 + i)
     barrier()
-    e2e_s = (time.perf_counter() - t0) / args.steps
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * tokens_per_step / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    e2e_s = replicas.max_over_ranks((time.perf_counter() - t0) / args.steps, dist, dev)
+    e2e = {"value": replicas.job_rate(world, tokens_per_step, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": 8, "ms_per_step": 1000 * e2e_s}
 
-    value = world * tokens_per_step / (ms * 1e-3)
+    value = replicas.job_rate(world, tokens_per_step, ms * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
