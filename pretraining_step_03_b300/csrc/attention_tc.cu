@@ -231,7 +231,8 @@ __global__ void __launch_bounds__(NT, 1)
     Smem sm = carve(smem_raw, FWD_TILES);
     // the heaviest (latest) query-block pairs first; the pairs of one batch-head together
     const int npair = (p.nblk + 1) / 2;
-    const int bh = blockIdx.y, c = npair - 1 - blockIdx.x, h = bh % p.H, b = bh / p.H;
+    const int bh = blockIdx.y, c = npair - 1 - (int)blockIdx.x, h = bh % p.H, b = bh / p.H;
+    if (c < 0) return;                 // (a grid wider than the sequence: nothing to do)
     const int qb0 = 2 * c;
     const bool has1 = qb0 + 1 < p.nblk;
     const int nk = has1 ? qb0 + 2 : qb0 + 1;          // key blocks streamed (tile t uses 0 .. qb0 + t)
@@ -430,7 +431,8 @@ __global__ void __launch_bounds__(NT, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DQ_TILES);
-    const int bh = blockIdx.y, qb = p.nblk - 1 - blockIdx.x, h = bh % p.H, b = bh / p.H;
+    const int bh = blockIdx.y, qb = p.nblk - 1 - (int)blockIdx.x, h = bh % p.H, b = bh / p.H;
+    if (qb < 0) return;                // (a grid wider than the sequence: nothing to do)
     const int nkb = qb + 1;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* qd_full = &sm.bar[0];
@@ -549,21 +551,21 @@ __global__ void __launch_bounds__(NT, 1)
 
 // ===================================================================== dK, dV
 // smem tiles: 0 K | 1 V | 2..4 Q stages | 5,6 dO stages
-// barriers: 0 kv_full, 1-3 q_full, 4-6 q_empty, 7-8 do_full, 9-10 do_empty, 11 s_full,
-//           12 dp_full, 13 s_free, 14 p_full, 15 ds_full, 16 dv_done, 17 dk_done,
-//           18-19 stat barriers
-// TMEM: S^T at 0, dP^T at 128, dV at 256, dK at 384.  The packed bf16 operands go into
-// the dP^T region once it has been read, each group only into the 64 columns it read
-// itself (so the two groups never wait for each other): group g puts its P^T slices
-// at 128 + 32g .. +31 and its dS^T slices at 192 + 32g .. +31, and the products take
-// each 16-query K slice from where its group left it (pk_col).  Tensor-pipe order in
-// steady state: dV_i, dK_i, dP^T_{i+1} (once dV_i and dK_i, whose A operands it
-// overwrites, have completed), S^T_{i+2} (once the softmax has read S^T_{i+1}); the
-// softmax's exp phase for block i+1 runs under dV_i / dK_i and its dS phase under
-// S^T_{i+2}.  P^T is released to dV before dS^T is computed.  Three Q stages let
-// Q_{i+2} arrive while Q_i (for dK_i) is still in use.
+// barriers: 0 kv_full, 1-3 q_full, 4-6 q_empty, 7-8 do_full, 9-10 do_empty (one arrival
+//           from each chain), 11 s_full, 12 dp_full, 14 p_full, 15 ds_full, 16 dv_done,
+//           17 dk_done, 18-19 stat barriers
+// TMEM: S^T at 0, dP^T at 128, dV at 256, dK at 384.  Each softmax group packs its bf16
+// operands only into the columns it read itself (the two groups never wait for each
+// other): P^T over S^T (group g at 32g .. 32g+31), dS^T over dP^T (at 192 + 32g ..); the
+// products take each 16-query K slice from where its group left it (pk_col).  That gives
+// two chains per query block, S^T -> P^T -> dV and dP^T -> dS^T -> dK, and each has an
+// issuing thread of its own (warp 1 and the last warp).  A commit tracks only its own
+// thread's products, and an issue that waits for a tensor-pipe slot holds back only its
+// own chain, so P^T_i goes to dV_i as soon as it exists while dK_{i-1} or dP^T_i is still
+// in the pipe.  Three Q stages let the loads run ahead.
 constexpr int DKV_TILES = 7;
 constexpr int DKV_QST = 3, DKV_DST = 2;
+constexpr int DKV_NT = NT + 32;          // + the second issuing warp
 
 // TMEM column (relative to the packed region) of K slice kk (queries 16kk .. 16kk+15)
 // of a packed operand: queries [32g, 32g+32) and [64+32g, 64+32g+32) belong to group g,
@@ -572,7 +574,7 @@ __host__ __device__ constexpr uint32_t pk_col(int kk) {
     return 32u * ((kk >> 1) & 1) + 16u * (kk >> 2) + 8u * (kk & 1);
 }
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(DKV_NT, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                      const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                      const AttnParams p) {
@@ -580,6 +582,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DKV_TILES);
     const int bh = blockIdx.y, kb = blockIdx.x, h = bh % p.H, b = bh / p.H;  // early keys (most work) first
+    if (kb >= p.nblk) return;          // (a grid wider than the sequence: nothing to do)
     const int nq = p.nblk - kb;        // query blocks kb .. nblk-1
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* kv_full = &sm.bar[0];
@@ -589,13 +592,12 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* do_empty = &sm.bar[9];
     uint64_t* s_full = &sm.bar[11];
     uint64_t* dp_full = &sm.bar[12];
-    uint64_t* s_free = &sm.bar[13];
     uint64_t* p_full = &sm.bar[14];
     uint64_t* ds_full = &sm.bar[15];
     uint64_t* dv_done = &sm.bar[16];
     uint64_t* dk_done = &sm.bar[17];
     uint64_t* sbar = &sm.bar[18];
-    const uint32_t counts[20] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, NSM, NSM, NSM, 1, 1, NSM, NSM};
+    const uint32_t counts[20] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 2, 2, 1, 1, 1, NSM, NSM, 1, 1, NSM, NSM};
     setup(sm, 20, counts);
     const uint32_t tmem = *sm.tmem_slot;
     uint8_t* K = sm.base;
@@ -628,37 +630,41 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
     } else if (warp == 1 && lane == 0) {
-        const uint32_t k0 = tc::smem_u32(K), v0 = tc::smem_u32(V);
-        auto issue_st = [&](int i) -> bool {   // S^T_i = K Q_i^T
-            if (!tc::mbar_wait(&q_full[i % DKV_QST], (i / DKV_QST) & 1, sm.abort)) return false;
+        // chain one: S^T_i = K Q_i^T, then dV += P^T_i dO_i (P^T_i packed over S^T_i)
+        const uint32_t k0 = tc::smem_u32(K);
+        bool ok = tc::mbar_wait(kv_full, 0, sm.abort);
+        for (int i = 0; ok && i < nq; ++i) {
+            const uint32_t qn = tc::smem_u32(Qt(i)), do0 = tc::smem_u32(dOt(i));
+            // S^T_i overwrites P^T_{i-1}, which dV_{i-1} reads: that product has completed
+            if (i > 0 && !(ok = tc::mbar_wait(dv_done, (i - 1) & 1, sm.abort))) break;
+            if (!(ok = tc::mbar_wait(&q_full[i % DKV_QST], (i / DKV_QST) & 1, sm.abort))) break;
             tc::fence_after();
-            const uint32_t qn = tc::smem_u32(Qt(i));
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem, dk_(k0, kk), dk_(qn, kk), IDESC_KK, kk > 0);
             tc::mma_commit(s_full);
-            return true;
-        };
-        auto issue_dpt = [&](int i) -> bool {  // dP^T_i = V dO_i^T
-            if (!tc::mbar_wait(&do_full[i % DKV_DST], (i / DKV_DST) & 1, sm.abort)) return false;
-            tc::fence_after();
-            const uint32_t don = tc::smem_u32(dOt(i));
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128, dk_(v0, kk), dk_(don, kk), IDESC_KK, kk > 0);
-            tc::mma_commit(dp_full);
-            return true;
-        };
-        bool ok = tc::mbar_wait(kv_full, 0, sm.abort) && issue_st(0) && issue_dpt(0);
-        // S^T_1 as soon as the softmax has read S^T_0
-        if (ok && nq > 1) ok = tc::mbar_wait(s_free, 0, sm.abort) && issue_st(1);
-        for (int i = 0; ok && i < nq; ++i) {
-            const uint32_t q0 = tc::smem_u32(Qt(i)), do0 = tc::smem_u32(dOt(i));
             if (!(ok = tc::mbar_wait(p_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                tc::mma_bf16_ts(tmem + 256, tmem + 128 + pk_col(kk), dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
+                tc::mma_bf16_ts(tmem + 256, tmem + pk_col(kk), dm_(do0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dv_done);
             tc::mma_commit(&do_empty[i % DKV_DST]);
+        }
+    } else if (warp == DKV_NT / 32 - 1 && lane == 0) {
+        // chain two: dP^T_i = V dO_i^T, then dK += dS^T_i Q_i (dS^T_i packed over dP^T_i)
+        const uint32_t v0 = tc::smem_u32(V);
+        bool ok = tc::mbar_wait(kv_full, 0, sm.abort);
+        for (int i = 0; ok && i < nq; ++i) {
+            const uint32_t q0 = tc::smem_u32(Qt(i)), don = tc::smem_u32(dOt(i));
+            // dP^T_i overwrites dS^T_{i-1}, which dK_{i-1} reads: that product has completed
+            if (i > 0 && !(ok = tc::mbar_wait(dk_done, (i - 1) & 1, sm.abort))) break;
+            if (!(ok = tc::mbar_wait(&do_full[i % DKV_DST], (i / DKV_DST) & 1, sm.abort))) break;
+            tc::fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16(tmem + 128, dk_(v0, kk), dk_(don, kk), IDESC_KK, kk > 0);
+            tc::mma_commit(dp_full);
+            tc::mma_commit(&do_empty[i % DKV_DST]);
+            // Q_i: S^T_i has completed (the softmax read it before dS^T_i exists)
             if (!(ok = tc::mbar_wait(ds_full, i & 1, sm.abort))) break;
             tc::fence_after();
 #pragma unroll
@@ -666,17 +672,8 @@ __global__ void __launch_bounds__(NT, 1)
                 tc::mma_bf16_ts(tmem + 384, tmem + 192 + pk_col(kk), dm_(q0, kk), IDESC_KM, (i > 0 || kk > 0));
             tc::mma_commit(dk_done);
             tc::mma_commit(&q_empty[i % DKV_QST]);
-            if (i + 1 < nq) {
-                if (!(ok = tc::mbar_wait(dv_done, i & 1, sm.abort))) break;
-                if (!(ok = tc::mbar_wait(dk_done, i & 1, sm.abort))) break;
-                if (!(ok = issue_dpt(i + 1))) break;
-            }
-            if (i + 2 < nq) {
-                if (!(ok = tc::mbar_wait(s_free, (i + 1) & 1, sm.abort))) break;
-                if (!(ok = issue_st(i + 2))) break;
-            }
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < 10) {
         const int g = (warp - 2) >> 2, q = warp & 3, r = q * 32 + lane;   // r = key row of the block
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
         const float c2 = p.scale * LOG2E;
@@ -686,39 +683,46 @@ __global__ void __launch_bounds__(NT, 1)
         const float* src = (g == 0 ? p.lse : p.delta) + srow;
         auto fetch = [&](int jb) { const int t = jb * BR + r; return t < p.T ? src[t] : NAN; };
         float nxt = fetch(kb);
+        // publish query block i's statistics: [-lse2 | -D] in exchange buffer i % 2
+        auto put_stat = [&](int i) {
+            const int j = kb + i;
+            float* stat = sm.xch + (i & 1) * 256;
+            const float cur = nxt;
+            if (i + 1 < nq) nxt = fetch(j + 1);
+            const bool valid = j * BR + r < p.T;
+            if (g == 0) stat[r] = valid ? -cur * LOG2E : -INFINITY;
+            else stat[128 + r] = valid ? -cur : 0.f;
+            tc::mbar_arrive(&sbar[i & 1]);
+        };
+        put_stat(0);
         float s[64];
         bool ok = true;
         for (int i = 0; i < nq; ++i) {
             const int j = kb + i;
-            float* stat = sm.xch + (i & 1) * 256;          // [-lse2 | -D] of this query block
-            {
-                const float cur = nxt;
-                if (i + 1 < nq) nxt = fetch(j + 1);
-                const bool valid = j * BR + r < p.T;
-                if (g == 0) stat[r] = valid ? -cur * LOG2E : -INFINITY;
-                else stat[128 + r] = valid ? -cur : 0.f;
-            }
-            tc::mbar_arrive(&sbar[i & 1]);
+            const float* stat = sm.xch + (i & 1) * 256;
             if (!(ok = tc::mbar_wait_warp(&sbar[i & 1], (i >> 1) & 1, sm.abort))) break;
             if (!(ok = tc::mbar_wait_warp(s_full, i & 1, sm.abort))) break;
             tc::fence_after();
             ld_half(tmem + lanes, g, s);
-            tc::fence_before();
-            tc::mbar_arrive(s_free);
             // P^T[r][c] = exp2(S^T*c2 - lse2[c]), zero where key r > query c; this
             // thread's columns are two contiguous runs of 32 (statistics as pairs), the
             // scale and shift two lanes at a time
             const uint64_t c22 = tc::f2pk(c2, c2);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-                const uint64_t* l2 = reinterpret_cast<const uint64_t*>(stat + 64 * h2 + 32 * g);
+                // (16-byte broadcast loads: shared memory is the tensor core's operand path)
+                const float4* l4 = reinterpret_cast<const float4*>(stat + 64 * h2 + 32 * g);
 #pragma unroll
-                for (int k2 = 0; k2 < 16; ++k2) {
-                    float* x = s + 32 * h2 + 2 * k2;
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 l = l4[k4];
+                    float* x = s + 32 * h2 + 4 * k4;
                     float a, bb;
-                    tc::f2upk(tc::ffma2(tc::f2pk(x[0], x[1]), c22, l2[k2]), a, bb);
+                    tc::f2upk(tc::ffma2(tc::f2pk(x[0], x[1]), c22, tc::f2pk(l.x, l.y)), a, bb);
                     x[0] = tc::ex2a(a);
                     x[1] = tc::ex2a(bb);
+                    tc::f2upk(tc::ffma2(tc::f2pk(x[2], x[3]), c22, tc::f2pk(l.z, l.w)), a, bb);
+                    x[2] = tc::ex2a(a);
+                    x[3] = tc::ex2a(bb);
                 }
             }
             if (i == 0) {
@@ -726,39 +730,40 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int e = 0; e < 64; ++e)
                     if (r > col_of(g, e)) s[e] = 0.f;
             }
+            {   // P^T into this group's S^T columns (already read): dV_i can start now
+                uint32_t wp[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) wp[e] = pack2(s[2 * e], s[2 * e + 1]);
+                tc::tmem_st32(tmem + lanes + 32 * g, wp);
+                tc::tmem_wait_st();
+                tc::fence_before();
+                tc::mbar_arrive(p_full);
+            }
             uint32_t wd[32];
             {
                 uint32_t d[32];   // this thread's dP^T, one 32-query chunk at a time
-                {
-                    uint32_t wp[32];
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) wp[e] = pack2(s[2 * e], s[2 * e + 1]);
-                    if (!(ok = tc::mbar_wait_warp(dp_full, i & 1, sm.abort))) break;
-                    tc::fence_after();
-                    tc::tmem_ld32(tmem + lanes + 128 + 32 * g, d);
-                    tc::tmem_wait_ld();
-                    // P^T into the columns just read; dV_i can start while dS^T is formed
-                    tc::tmem_st32(tmem + lanes + 128 + 32 * g, wp);
-                    tc::tmem_wait_st();
-                }
-                tc::fence_before();
-                tc::mbar_arrive(p_full);
+                if (!(ok = tc::mbar_wait_warp(dp_full, i & 1, sm.abort))) break;
+                tc::fence_after();
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {   // dS^T = P^T (dP^T - D[c])
-                    if (h2 == 1) {
-                        tc::tmem_ld32(tmem + lanes + 192 + 32 * g, d);
-                        tc::tmem_wait_ld();
-                    }
-                    const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(stat + 128 + 64 * h2 + 32 * g);
+                    tc::tmem_ld32(tmem + lanes + 128 + 64 * h2 + 32 * g, d);
+                    tc::tmem_wait_ld();
+                    const float4* nd4 = reinterpret_cast<const float4*>(stat + 128 + 64 * h2 + 32 * g);
 #pragma unroll
-                    for (int k2 = 0; k2 < 16; ++k2) {   // (dP^T - D) * P^T, two lanes at a time
-                        const float* x = s + 32 * h2 + 2 * k2;
-                        const uint32_t* y = d + 2 * k2;
-                        float a, bb;
-                        tc::f2upk(tc::fmul2(tc::f2pk(x[0], x[1]),
-                                    tc::fadd2(tc::f2pk(__uint_as_float(y[0]), __uint_as_float(y[1])), nd2[k2])),
-                              a, bb);
-                        wd[16 * h2 + k2] = pack2(a, bb);
+                    for (int k4 = 0; k4 < 8; ++k4) {   // (dP^T - D) * P^T, two lanes at a time
+                        const float4 nd = nd4[k4];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int k2 = 2 * k4 + u;
+                            const float* x = s + 32 * h2 + 2 * k2;
+                            const uint32_t* y = d + 2 * k2;
+                            float a, bb;
+                            tc::f2upk(tc::fmul2(tc::f2pk(x[0], x[1]),
+                                        tc::fadd2(tc::f2pk(__uint_as_float(y[0]), __uint_as_float(y[1])),
+                                                  u ? tc::f2pk(nd.z, nd.w) : tc::f2pk(nd.x, nd.y))),
+                                  a, bb);
+                            wd[16 * h2 + k2] = pack2(a, bb);
+                        }
                     }
                 }
             }
@@ -766,6 +771,10 @@ __global__ void __launch_bounds__(NT, 1)
             tc::tmem_wait_st();
             tc::fence_before();
             tc::mbar_arrive(ds_full);
+            // the next block's statistics go out before this block's dS store, so that no
+            // thread waits on another's stores (every thread has read buffer (i+1) % 2,
+            // block i-1's, since the barrier of block i)
+            if (i + 1 < nq) put_stat(i + 1);
             if (p.ds) {   // keep key r's dS for the dQ product: query chunks 4g+k and 8+4g+k
                 uint8_t* base = ds_tile(p, bh, j, kb) + (r >> 6) * DS_HALF + (r & 63) * 16;
 #pragma unroll
@@ -817,7 +826,8 @@ __global__ void __launch_bounds__(DQS_NT, 2)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (misaligned(smem_raw, p.flag)) return;
     Smem sm = carve(smem_raw, DQS_ST);
-    const int bh = blockIdx.y, qb = p.nblk - 1 - blockIdx.x, h = bh % p.H, b = bh / p.H;
+    const int bh = blockIdx.y, qb = p.nblk - 1 - (int)blockIdx.x, h = bh % p.H, b = bh / p.H;
+    if (qb < 0) return;                // (a grid wider than the sequence: nothing to do)
     const int nu = 2 * (qb + 1);           // 64-key units up to the diagonal
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     uint64_t* full = &sm.bar[0];
@@ -963,7 +973,7 @@ int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, 
     p.rope_ld = rope_ld;
     p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
     p.ds = ds; p.ds_bh = (long)p.nblk * (p.nblk + 1) / 2;
-    attn_dkdv_kernel<<<dim3(p.nblk, H * B), NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);
+    attn_dkdv_kernel<<<dim3(p.nblk, H * B), DKV_NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);
     if (ds) {
         CUtensorMap mk64;
         NC_TRY(make_map(&mk64, k, (long)H * HD, rows, 1, ld, 0, 64, 64));
