@@ -30,5 +30,8 @@ from .model import (  # noqa: F401
     forward,
     backward,
     loss_and_grads,
+    eval_sums,
+    bpb_of_sums,
 )
 from .optim import newton_schulz, muon_step, adamw_step  # noqa: F401
+from . import schedule  # noqa: F401

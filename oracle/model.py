@@ -253,3 +253,22 @@ def backward(cache, cfg, grad_scale=1.0):
 def loss_and_grads(params, cfg, tokens, targets, token_bytes, grad_scale=1.0):
     loss, bpb, cache = forward(params, cfg, tokens, targets, token_bytes)
     return loss, bpb, backward(cache, cfg, grad_scale)
+
+
+def eval_sums(params, cfg, tokens, targets, token_bytes):
+    """Evaluation pass of one batch (section 预搜检: validation bits per byte).
+
+    Returns (sum nll, sum nll over targets with bytes > 0, sum bytes), so that
+    bits per byte over several batches is the corpus ratio of sums,
+    sums[1] / (ln 2 * sums[2]).
+    """
+    _, _, cache = forward(params, cfg, tokens, targets, token_bytes)
+    nll = cache["nll"]
+    nbytes = np.asarray(token_bytes, dtype=np.int64)[cache["tgt"]]
+    return float(np.sum(nll)), float(np.sum(nll[nbytes > 0])), float(np.sum(nbytes))
+
+
+def bpb_of_sums(sums):
+    """Bits per byte from the running sums of ``eval_sums``."""
+    return sums[1] / (np.log(2.0) * sums[2])
+
