@@ -9,8 +9,14 @@ vocab 65536, bf16, 32 x 2048 tokens per step drawn from a Zipf(1.1) stream
 weights.  Replicas only: with --gpus N (under torchrun) every rank trains its
 own replica on its own data; there is no collective on the data path.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload d20|d30|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload d20|d20x8|d26|d30|eval|tiny]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+  d20x8  the pages' whole optimizer step: 8 accumulated micro-batches of 32 x 2048
+         (524,288 tokens), learning rates from the run's schedule (nc_lr_schedule)
+  d26    depth 26 (d_model 1664, 13 heads), 2 x 16 x 2048 tokens, scheduled rates
+  eval   the evaluation pass: d20 forward, loss and bits per byte over 32 x 2048
+         tokens per step, no backward (its own metric: evaluation tokens/s)
 
 Kernel-level workloads (profiling harnesses, not the headline):
   --workload attn    causal attention forward+backward alone, B=32 (or --batch),
@@ -40,11 +46,19 @@ WORKLOADS = {
     "gemm": dict(B=32, T=2048, d=1280, F=5120),
     "optim": dict(depth=20, d_model=1280, n_head=10, vocab=65536),
     "d20": dict(depth=20, d_model=1280, n_head=10, vocab=65536, B=32, T=2048, n_micro=1),
+    "d20x8": dict(depth=20, d_model=1280, n_head=10, vocab=65536, B=32, T=2048, n_micro=8, schedule=True),
+    "d26": dict(depth=26, d_model=1664, n_head=13, vocab=65536, B=16, T=2048, n_micro=2, schedule=True),
     "d30": dict(depth=30, d_model=1920, n_head=15, vocab=65536, B=16, T=2048, n_micro=2),
+    "eval": dict(depth=20, d_model=1280, n_head=10, vocab=65536, B=32, T=2048, n_micro=1),
     "tiny": dict(depth=2, d_model=128, n_head=2, vocab=512, B=4, T=64, n_micro=1),
 }
 HP = dict(muon_lr=0.02, momentum=0.95, ns_steps=5, coefs=(3.4445, -4.7750, 2.0315), lr_emb=0.2,
           lr_unemb=0.004, beta1=0.8, beta2=0.95, eps=1e-10, wd=0.0)
+# The scheduled workloads take the rates above as given at width SCHED_D_REF, scale the
+# AdamW ones by sqrt(SCHED_D_REF / d_model) and apply the linear warm-down multiplier over
+# the last SCHED_WARMDOWN of a 20-tokens-per-parameter run (nc_lr_schedule).
+SCHED_D_REF, SCHED_WARMDOWN = 1280, 0.2
+EVAL_METRIC = "evaluation tokens/sec (forward, loss and bits per byte) for d20 on 1 B300"
 NOMINAL_BF16_TFLOPS = 2250.0
 # Rooflines: the kernel class -> (bound, peak key).  Peaks are the measured
 # copy bandwidth and library bf16 GEMM rates of this GPU pool.
@@ -120,7 +134,7 @@ def gpu_id_for(torch, dev):
 
 
 # ---------------------------------------------------------------- oracle timing
-def cpu_baseline(w, steps=1):
+def cpu_baseline(w, steps=1, forward_only=False):
     """The fp64 oracle as it stands, on a bounded sample, in a fresh process."""
     code = (
         "import sys, time, json, os\n"
@@ -129,7 +143,7 @@ def cpu_baseline(w, steps=1):
         "import oracle\n"
         "from oracle.model import Config\n"
         "from pretraining_step_03_b300 import synth\n"
-        f"w = {json.dumps(w)}\n"
+        f"w = json.loads({json.dumps(json.dumps(w))})\n"
         f"T = min({CPU_SAMPLE_T}, w['T'])\n"
         "cfg = Config(w['depth'], w['d_model'], w['n_head'], w['vocab'])\n"
         "params = synth.init_params(w['depth'], w['d_model'], w['n_head'], w['vocab'], seed=0)\n"
@@ -138,7 +152,8 @@ def cpu_baseline(w, steps=1):
         "ts = []\n"
         f"for _ in range({steps}):\n"
         "    t0 = time.perf_counter()\n"
-        "    oracle.loss_and_grads(params, cfg, tok, tgt, tb)\n"
+        + ("    oracle.eval_sums(params, cfg, tok, tgt, tb)\n" if forward_only else
+           "    oracle.loss_and_grads(params, cfg, tok, tgt, tb)\n") +
         "    ts.append(time.perf_counter() - t0)\n"
         "print(json.dumps({'T': T, 'times': ts}))\n")
     cores = len(os.sched_getaffinity(0))
@@ -272,6 +287,154 @@ def kernel_workload(args):
 
 
 # ---------------------------------------------------------------- main
+# ---------------------------------------------------------------- evaluation pass
+def kernel_table(L, m, steps, pk):
+    kernels = {}
+    for c, name in enumerate(L.PROF_NAMES):
+        kms, n, fl, by = L.nc_profile_read(m.h, c)
+        if n == 0:
+            continue
+        if ROOF[name] == "tensor":
+            ach = fl / (kms * 1e-3) / 1e12
+            peak, unit = pk["tensor"], "TFLOP/s"
+        else:
+            ach = by / (kms * 1e-3) / 1e9
+            peak, unit = pk["hbm"], "GB/s"
+        kernels[name] = {"ms_per_step": kms / steps, "launch_sites_per_step": n / steps,
+                         "achieved": ach, "unit": unit, "peak": peak, "frac": ach / peak}
+    return kernels
+
+
+def eval_workload(args):
+    """d20 forward + loss + bits per byte over 32 x 2048 tokens per step, no backward;
+    the byte-weighted sums run across the steps as over a validation set."""
+    w = WORKLOADS["eval"]
+    from pretraining_step_03_b300 import replicas
+    rank, world, local = replicas.rank_env()
+    B, T = w["B"], w["T"]
+    fpt = shapes.eval_flops_per_token(w["depth"], w["d_model"], w["vocab"], T)
+    config = {"workload": "eval", "depth": w["depth"], "d_model": w["d_model"], "n_head": w["n_head"],
+              "vocab": w["vocab"], "batch": B * world, "seq_len": T, "parallelism": f"replicas{world}",
+              "tokens": "zipf(1.1)", "l2": "inputs larger than L2 (8.6 GB of logits per step)"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        Tc, times, cores = cpu_baseline(w, steps=args.warmup + args.steps, forward_only=True)
+        t = times[args.warmup:] if len(times) > args.warmup else times
+        v = Tc / (sum(t) / len(t))
+        print(json.dumps({"metric": EVAL_METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+                          "steps": len(t), "warmup": args.warmup, "ms_per_step": 1000 * sum(t) / len(t),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": config, "impl": "reference",
+                          "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                           "sample": f"forward and loss of 1x{Tc} tokens at full widths"},
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    import numpy as np
+    import torch
+    from pretraining_step_03_b300 import _lib as L
+    from pretraining_step_03_b300.model import Model
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    tok, tgt = synth.zipf_rows(B, T, w["vocab"], seed=replicas.data_seed(rank) + 100)
+    tb_host = synth.token_bytes_binomial(w["vocab"], seed=2)
+    m = Model(w["depth"], w["d_model"], w["n_head"], w["vocab"], B, T, dtype="bf16", seed=0, device=dev)
+    tb = torch.from_numpy(tb_host).to(dev)
+    tok_d = torch.from_numpy(tok.reshape(-1)).to(dev)
+    tgt_d = torch.from_numpy(tgt.reshape(-1)).to(dev)
+    sums = torch.zeros(3, dtype=torch.float64, device=dev)
+    loss_d = torch.zeros(2, dtype=torch.float32, device=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        m.eval_loss(tok_d, tgt_d, tb, B, T, accumulate=int(i > 0), sums=sums, out=loss_d)
+    barrier()
+    stream = torch.cuda.current_stream(dev)
+    clocks = Clocks(gpu_id_for(torch, dev))
+    time.sleep(0.4)
+    L.nc_profile(m.h, 1)
+    launches0 = L.nc_launch_count()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        m.eval_loss(tok_d, tgt_d, tb, B, T, accumulate=int(i > 0), sums=sums, out=loss_d)
+    e1.record(stream)
+    barrier()
+    launches = L.nc_launch_count() - launches0
+    clk = clocks.stop()
+    L.nc_profile(m.h, 0)
+    ms = replicas.max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
+    pk = peaks()
+    kernels = kernel_table(L, m, args.steps, pk)
+    s_host = sums.cpu().numpy()
+    loss = loss_d.cpu().numpy()
+    g = kernels.get("gemm")
+    roofline = None
+    if g:
+        kms, n, fl, by = L.nc_profile_read(m.h, 0)
+        roofline = {"bound": "tensor", "kernel": "gemm_tc2_kernel (the forward GEMMs, CTA pairs)",
+                    "achieved": g["achieved"], "peak": pk["tensor"], "unit": "TFLOP/s", "frac": g["frac"],
+                    "peak_kind": f"bf16 sustained ({pk['source']})", "traffic": None,
+                    "flops_per_launch": fl / n}
+    # end to end: pinned host tokens/targets in, the running sums out, every step
+    tok_h = torch.from_numpy(tok.reshape(-1).copy()).pin_memory()
+    tgt_h = torch.from_numpy(tgt.reshape(-1).copy()).pin_memory()
+    sums_h = torch.zeros(3, dtype=torch.float64).pin_memory()
+    tok_s, tgt_s = torch.empty_like(tok_d), torch.empty_like(tgt_d)
+
+    def host_step(i):
+        tok_s.copy_(tok_h, non_blocking=True)
+        tgt_s.copy_(tgt_h, non_blocking=True)
+        m.eval_loss(tok_s, tgt_s, tb, B, T, accumulate=int(i > 0), sums=sums)
+        sums_h.copy_(sums, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    host_step(0)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        host_step(i + 1)
+    barrier()
+    e2e_s = replicas.max_over_ranks((time.perf_counter() - t0) / args.steps, dist, dev)
+    value = replicas.job_rate(world, B * T, ms * 1e-3)
+    line = {
+        "metric": EVAL_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+        "mfu": {"nominal_2250": value / world * fpt / (NOMINAL_BF16_TFLOPS * 1e12),
+                "measured_sustained": value / world * fpt / (pk["tensor"] * 1e12),
+                "flop_per_token": fpt},
+        "loss": float(loss[0]), "bpb": float(loss[1]),
+        "bpb_over_steps": float(s_host[1] / (np.log(2.0) * s_host[2])) if s_host[2] > 0 else None,
+        "device_flag": m.check_flag(), "gpu_launches": int(launches), "roofline": roofline,
+        "kernels": kernels,
+        "e2e": {"value": replicas.job_rate(world, B * T, e2e_s), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * B * T * 4, "d2h_bytes_per_step": 24, "ms_per_step": 1000 * e2e_s},
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        Tc, times, cores = cpu_baseline(w, steps=1, forward_only=True)
+        line["cpu_baseline"] = {"value": Tc / times[0], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"forward and loss of 1x{Tc} tokens at full widths (fp64 NumPy)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -284,6 +447,8 @@ def main():
     args = ap.parse_args()
     if args.workload in ("attn", "optim", "gemm"):
         return kernel_workload(args)
+    if args.workload == "eval":
+        return eval_workload(args)
     w = WORKLOADS[args.workload]
     from pretraining_step_03_b300 import replicas
     rank, world, local = replicas.rank_env()
@@ -295,6 +460,10 @@ def main():
               "micro_batch": w["B"], "grad_accum": w["n_micro"], "seq_len": w["T"],
               "parallelism": f"replicas{world}", "tokens": "zipf(1.1)",
               "l2": "inputs larger than L2 (47+ GB activation stash per step)"}
+    if w.get("schedule"):
+        config["lr_schedule"] = {"run_steps": shapes.chinchilla_steps(w["depth"], w["d_model"], w["n_head"],
+                                                                      w["vocab"], tokens_per_step),
+                                 "warmdown_frac": SCHED_WARMDOWN, "d_ref": SCHED_D_REF}
 
     if args.impl == "reference":
         if rank != 0:
@@ -337,12 +506,21 @@ def main():
     tgt_d = torch.from_numpy(tgt.reshape(nm, B * T)).to(dev)
     loss_d = torch.zeros(nm, 2, dtype=torch.float32, device=dev)
 
+    n_run = shapes.chinchilla_steps(w["depth"], w["d_model"], w["n_head"], w["vocab"], tokens_per_step)
+
+    def rates(i):
+        if not w.get("schedule"):
+            return HP["muon_lr"], HP["lr_emb"], HP["lr_unemb"]
+        return L.nc_lr_schedule(i % n_run, n_run, SCHED_WARMDOWN, w["d_model"], SCHED_D_REF,
+                                (HP["muon_lr"], HP["lr_emb"], HP["lr_unemb"]))
+
     def step(i):
+        lr_m, lr_e, lr_u = rates(i)
         for j in range(nm):
             m.forward_backward(tok_d[j], tgt_d[j], tb, B, T, accumulate=int(j > 0), grad_scale=1.0 / nm,
                                out=loss_d[j])
-        m.muon_step(HP["muon_lr"], HP["momentum"], True, HP["ns_steps"], HP["coefs"])
-        m.adamw_step(HP["lr_emb"], HP["lr_unemb"], HP["beta1"], HP["beta2"], HP["eps"], HP["wd"], i + 1)
+        m.muon_step(lr_m, HP["momentum"], True, HP["ns_steps"], HP["coefs"])
+        m.adamw_step(lr_e, lr_u, HP["beta1"], HP["beta2"], HP["eps"], HP["wd"], i + 1)
 
     def barrier():
         if dist is not None:
@@ -372,19 +550,7 @@ def main():
     loss = loss_d.cpu().numpy().mean(axis=0)
     flag = m.check_flag()
     pk = peaks()
-    kernels = {}
-    for c, name in enumerate(L.PROF_NAMES):
-        kms, n, fl, by = L.nc_profile_read(m.h, c)
-        if n == 0:
-            continue
-        if ROOF[name] == "tensor":
-            ach = fl / (kms * 1e-3) / 1e12
-            peak, unit = pk["tensor"], "TFLOP/s"
-        else:
-            ach = by / (kms * 1e-3) / 1e9
-            peak, unit = pk["hbm"], "GB/s"
-        kernels[name] = {"ms_per_step": kms / args.steps, "launch_sites_per_step": n / args.steps,
-                         "achieved": ach, "unit": unit, "peak": peak, "frac": ach / peak}
+    kernels = kernel_table(L, m, args.steps, pk)
     g = kernels.get("gemm")
     roofline = None
     if g:
@@ -402,7 +568,8 @@ def main():
     tgt_h = torch.from_numpy(tgt.reshape(-1).copy()).pin_memory()
 
     def host_step(i):
-        return m.train_step(tok_h, tgt_h, tb, B, T, nm, HP["muon_lr"], HP["lr_emb"], HP["lr_unemb"], i,
+        lr_m, lr_e, lr_u = rates(i)
+        return m.train_step(tok_h, tgt_h, tb, B, T, nm, lr_m, lr_e, lr_u, i,
                             HP["momentum"], HP["ns_steps"], HP["coefs"], HP["beta1"], HP["beta2"], HP["eps"],
                             HP["wd"])
 

@@ -113,6 +113,23 @@ NC_API int nc_forward_backward(nc_model* m, const int32_t* tokens, const int32_t
                         float grad_scale, float* loss_bpb_out);
 
 /*
+ * Evaluation pass (section 预搜检: the run reports validation bits per byte
+ * from time to time): forward and loss of one batch, no backward.  The
+ * gradients, optimizer state and weights are not touched.
+ * tokens, targets, token_bytes: as for nc_forward_backward.
+ * sums: device double[3], required: {sum of nll (nats), sum of nll over the
+ * targets with token_bytes > 0, sum of token_bytes}, set (accumulate = 0) or
+ * added to (accumulate = 1), so that bits per byte over many batches is the
+ * ratio of sums sums[1] / (ln 2 * sums[2]).
+ * loss_bpb_out: device float[2] or NULL <- {mean nll, bpb} of this batch,
+ * bit-identical to what nc_forward_backward reports for the same batch and
+ * weights.  Asynchronous.
+ */
+NC_API int nc_eval_loss(nc_model* m, const int32_t* tokens, const int32_t* targets,
+                        const int32_t* token_bytes, int B, int T, int accumulate, double* sums,
+                        float* loss_bpb_out);
+
+/*
  * Muon on every block matrix (section 预搜检: Muon optimises the matrices):
  * buf = momentum*buf + g; g' = g + momentum*buf if nesterov else buf;
  * X = g'/(|g'|_F + 1e-7), transposed when rows > cols; ns_steps iterations of
@@ -146,6 +163,23 @@ NC_API int nc_train_step(nc_model* m, const int32_t* tokens_host, const int32_t*
                   float muon_lr, float muon_momentum, int ns_steps, const float ns_coef[3],
                   float lr_emb, float lr_unemb, float beta1, float beta2, float eps,
                   float weight_decay, int adam_step, float* loss_bpb_host);
+
+/*
+ * Learning rates of optimizer step `step` (0-based) of an n_steps run (section
+ * 预搜检: the rate scales as 1/sqrt(dim), and the multiplier lrm falls
+ * linearly to 0 near the end of training).  Host arithmetic, no device work.
+ *   lrm = 1 for step < n_steps - W, else (n_steps - step) / W, where
+ *   W = round(warmdown_frac * n_steps) warm-down steps (W = 0: lrm = 1).
+ *   out[0] = lrm * base[0]                          (Muon; its update size is
+ *            already fixed by the orthogonalisation and sqrt(max(1, rows/cols)))
+ *   out[1] = lrm * base[1] * sqrt(d_ref / d_model)  (AdamW, embedding)
+ *   out[2] = lrm * base[2] * sqrt(d_ref / d_model)  (AdamW, unembedding)
+ * base: host float[3], the rates at width d_ref.  out: host float[3].
+ * Errors: NC_ERR_ARG for n_steps < 1, step outside [0, n_steps),
+ * warmdown_frac outside [0, 1], d_model or d_ref < 1, or null pointers.
+ */
+NC_API int nc_lr_schedule(int step, int n_steps, float warmdown_frac, int d_model, int d_ref,
+                          const float base[3], float out[3]);
 
 /* Host <-> device copies of one tensor as fp32 (n = rows*cols elements).
  * nc_set_params also refreshes the bf16 compute copy.  slot is one of

@@ -40,6 +40,8 @@ SIGNATURES = {
     "nc_num_params": (_I, [_V, ctypes.POINTER(_I)]),
     "nc_param_info": (_I, [_V, _I, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "nc_forward_backward": (_I, [_V, _V, _V, _V, _I, _I, _I, _F, _V]),
+    "nc_eval_loss": (_I, [_V, _V, _V, _V, _I, _I, _I, _V, _V]),
+    "nc_lr_schedule": (_I, [_I, _I, _F, _I, _I, ctypes.POINTER(_F), ctypes.POINTER(_F)]),
     "nc_muon_step": (_I, [_V, _F, _F, _I, _I, ctypes.POINTER(_F)]),
     "nc_adamw_step": (_I, [_V, _F, _F, _F, _F, _F, _F, _I]),
     "nc_train_step": (_I, [_V, _V, _V, _V, _I, _I, _I, _F, _F, _I, ctypes.POINTER(_F), _F, _F, _F,
@@ -131,6 +133,17 @@ def nc_param_info(m, index):
 def nc_forward_backward(m, tokens, targets, token_bytes, B, T, accumulate, grad_scale, loss_bpb_out):
     _check(lib().nc_forward_backward(m, tokens, targets, token_bytes, B, T, accumulate, grad_scale,
                                      loss_bpb_out))
+
+
+def nc_eval_loss(m, tokens, targets, token_bytes, B, T, accumulate, sums, loss_bpb_out):
+    _check(lib().nc_eval_loss(m, tokens, targets, token_bytes, B, T, accumulate, sums, loss_bpb_out))
+
+
+def nc_lr_schedule(step, n_steps, warmdown_frac, d_model, d_ref, base):
+    """Returns (muon_lr, lr_emb, lr_unemb) of optimizer step `step` (0-based)."""
+    out = (ctypes.c_float * 3)()
+    _check(lib().nc_lr_schedule(step, n_steps, warmdown_frac, d_model, d_ref, _f3(base), out))
+    return tuple(float(x) for x in out)
 
 
 def nc_muon_step(m, lr, momentum, nesterov, ns_steps, ns_coef):

@@ -255,8 +255,12 @@ int weight_grad(nc_model* m, float* dW, int rows, int cols, const void* dY, long
 }
 
 template <typename T>
+// backward = false: the forward and the loss only (the evaluation pass); the logits are
+// not turned into their gradient and no gradient is touched.  sums (optional): running
+// loss totals, see loss_reduce.
 int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const int32_t* tb, int B,
-                     int T_, int accumulate, float grad_scale, float* out) {
+                     int T_, int accumulate, float grad_scale, float* out, bool backward = true,
+                     double* sums = nullptr, int sum_acc = 0) {
     const int d = m->d, H = m->H, Dh = m->Dh, V = m->V, F = m->F;
     const int M = B * T_;
     const int act = m->dtype;
@@ -335,11 +339,14 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         NC_TRY(run_gemm(m, g));
     }
     {
-        Prof pr(m, NC_PROF_CE, 0, 2.0 * M * V * ab + M * 16.0);
+        const double ce_bytes = backward ? 2.0 * M * V * ab
+                                         : (lse_part ? M * (V / 128) * 8.0 : (double)M * V * ab);
+        Prof pr(m, NC_PROF_CE, 0, ce_bytes + M * 16.0);
         NC_TRY(cross_entropy<T>((T*)m->logits, tgt, m->nll, M, V, grad_scale / (float)M, m->flag, s,
-                                lse_part));
-        NC_TRY(loss_reduce(m->nll, tgt, tb, M, V, out, m->flag, s));
+                                lse_part, backward));
+        NC_TRY(loss_reduce(m->nll, tgt, tb, M, V, out, m->flag, s, sums, sum_acc));
     }
+    if (!backward) return NC_OK;
 
     // ------------------------------------------------ backward
     float* G = m->grads;
@@ -652,6 +659,23 @@ int nc_forward_backward(nc_model* m, const int32_t* tokens, const int32_t* targe
     return forward_backward<float>(m, tokens, targets, token_bytes, B, T, accumulate, grad_scale, loss_bpb_out);
 }
 
+int nc_eval_loss(nc_model* m, const int32_t* tokens, const int32_t* targets, const int32_t* token_bytes,
+                 int B, int T, int accumulate, double* sums, float* loss_bpb_out) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    if (!tokens || !targets || !token_bytes || !sums) return set_error(NC_ERR_ARG, "null pointer");
+    if (B < 1 || T < 1 || T > m->maxT || (long)B * T > m->maxM)
+        return set_error(NC_ERR_ARG, "B=%d T=%d exceeds the arena's max_B*max_T=%ld / max_T=%d", B, T,
+                         m->maxM, m->maxT);
+    if (accumulate != 0 && accumulate != 1) return set_error(NC_ERR_ARG, "accumulate must be 0 or 1");
+    g_gemm_flag = m->flag;
+    g_attn_flag = m->flag;
+    if (m->dtype == NC_BF16)
+        return forward_backward<bf16>(m, tokens, targets, token_bytes, B, T, 0, 1.f, loss_bpb_out, false,
+                                      sums, accumulate);
+    return forward_backward<float>(m, tokens, targets, token_bytes, B, T, 0, 1.f, loss_bpb_out, false,
+                                   sums, accumulate);
+}
+
 int nc_muon_step(nc_model* m, float lr, float momentum, int nesterov, int ns_steps, const float ns_coef[3]) {
     if (!m || !ns_coef) return set_error(NC_ERR_ARG, "null argument");
     if (ns_steps < 0 || ns_steps > 100) return set_error(NC_ERR_ARG, "ns_steps %d", ns_steps);
@@ -706,6 +730,23 @@ int nc_train_step(nc_model* m, const int32_t* tokens_host, const int32_t* target
     for (int i = 0; i < n_micro; ++i) { a += tmp[2 * i]; b += tmp[2 * i + 1]; }
     loss_bpb_host[0] = (float)(a / n_micro);
     loss_bpb_host[1] = (float)(b / n_micro);
+    return NC_OK;
+}
+
+int nc_lr_schedule(int step, int n_steps, float warmdown_frac, int d_model, int d_ref, const float base[3],
+                   float out[3]) {
+    if (!base || !out) return set_error(NC_ERR_ARG, "null pointer");
+    if (n_steps < 1 || step < 0 || step >= n_steps)
+        return set_error(NC_ERR_ARG, "step %d outside [0, n_steps = %d)", step, n_steps);
+    if (!(warmdown_frac >= 0.f && warmdown_frac <= 1.f))
+        return set_error(NC_ERR_ARG, "warmdown_frac %g outside [0, 1]", (double)warmdown_frac);
+    if (d_model < 1 || d_ref < 1) return set_error(NC_ERR_ARG, "d_model %d, d_ref %d", d_model, d_ref);
+    const long w = lround((double)warmdown_frac * n_steps);
+    const double lrm = (w == 0 || step < n_steps - w) ? 1.0 : (double)(n_steps - step) / (double)w;
+    const double width = sqrt((double)d_ref / (double)d_model);
+    out[0] = (float)(lrm * base[0]);
+    out[1] = (float)(lrm * base[1] * width);
+    out[2] = (float)(lrm * base[2] * width);
     return NC_OK;
 }
 

@@ -68,12 +68,16 @@ int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* tabl
                cudaStream_t s);
 // logits [M, V] -> dlogits in place; nll [M].  lse_part (bf16 only, optional): the
 // per-row (max, sum exp) partials of every 128-column group, left by the LM-head GEMM
-// (EPI_LSE); with them the logits are read once instead of twice.
+// (EPI_LSE); with them the logits are read once instead of twice.  grad = false: nll
+// only, the logits are left untouched.
 template <typename T>
 int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float scale,
-                  uint32_t* flag, cudaStream_t s, const float2* lse_part = nullptr);
+                  uint32_t* flag, cudaStream_t s, const float2* lse_part = nullptr, bool grad = true);
+// out (optional): {mean nll, bpb of this batch}; sums (optional): device double[3]
+// {sum nll, sum nll over targets with bytes > 0, sum bytes}, set (accumulate = 0) or
+// added to (accumulate = 1).  One CTA, fixed summation order.
 int loss_reduce(const float* nll, const int32_t* tgt, const int32_t* token_bytes, int M, int V,
-                float* out, uint32_t* flag, cudaStream_t s);
+                float* out, uint32_t* flag, cudaStream_t s, double* sums = nullptr, int accumulate = 0);
 struct EmbedBwdWs {
     int* hist;       // [nchunks * V]
     int* rank;       // [M]

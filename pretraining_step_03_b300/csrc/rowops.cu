@@ -148,7 +148,7 @@ __device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
 // z <- scale * (softmax(z) - onehot(target)) in place.
 template <typename T>
 __global__ void __launch_bounds__(CE_THREADS) ce_kernel(T* z, const int32_t* tgt, float* nll, int V,
-                                                        float scale, uint32_t* flag) {
+                                                        float scale, int grad, uint32_t* flag) {
     __shared__ float sh[32];
     __shared__ float zt_s;
     const long row = blockIdx.x;
@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(CE_THREADS) ce_kernel(T* z, const int32_t* tgt
     const float lse = mx + logf(se);
     __syncthreads();  // zt_s was read before any thread overwrites z
     if (threadIdx.x == 0) nll[row] = ok ? lse - zt_s : 0.f;
+    if (!grad) return;   // (loss only: the logits stay as they are)
     for (int j = threadIdx.x; j < V; j += blockDim.x) {
         float p = expf(to_f<T>(zr[j]) - lse);
         if (j == t) p -= 1.f;
@@ -191,7 +192,7 @@ __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s
 }
 
 __global__ void __launch_bounds__(CE2_THREADS) ce_online_kernel(bf16* z, const int32_t* tgt, float* nll,
-                                                                int V, float scale, uint32_t* flag) {
+                                                                int V, float scale, int grad, uint32_t* flag) {
     __shared__ float shm[32], shs[32];
     __shared__ float zt_s, lse_s;
     const long row = blockIdx.x;
@@ -249,6 +250,7 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_online_kernel(bf16* z, const i
         }
     }
     __syncthreads();   // zt_s was read before any thread overwrites z
+    if (!grad) return;   // (loss only: the logits stay as they are)
     const float lsel = lse_s * CE_LOG2E;
 #pragma unroll 4
     for (int k = 0; k < nv; ++k) {
@@ -272,7 +274,8 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_online_kernel(bf16* z, const i
 // left by the LM-head GEMM's epilogue: combine them (fixed order), then one pass that
 // writes dlogits = scale * (softmax - onehot) over the logits in place.
 __global__ void __launch_bounds__(CE2_THREADS) ce_stats_kernel(bf16* z, const float2* part, const int32_t* tgt,
-                                                               float* nll, int V, float scale, uint32_t* flag) {
+                                                               float* nll, int V, float scale, int grad,
+                                                               uint32_t* flag) {
     __shared__ float shm[32], shs[32];
     __shared__ float zt_s, lse_s;
     const long row = blockIdx.x;
@@ -312,6 +315,7 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_stats_kernel(bf16* z, const fl
         }
     }
     __syncthreads();   // zt_s was read before any thread overwrites z
+    if (!grad) return;   // (loss only: the logits stay as they are)
     const float lsel = lse_s * CE_LOG2E;
 #pragma unroll 4
     for (int k = 0; k < nv; ++k) {
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_stats_kernel(bf16* z, const fl
 
 // Single CTA, fixed summation order: loss = mean nll; bpb = sum(nll | bytes>0) / (ln2 * sum bytes).
 __global__ void loss_reduce_kernel(const float* nll, const int32_t* tgt, const int32_t* tb, int M,
-                                   int V, float* out, uint32_t* flag) {
+                                   int V, float* out, double* sums, int accumulate, uint32_t* flag) {
     __shared__ double s_nll[1024], s_pos[1024], s_bytes[1024];
     double a = 0, b = 0, c = 0;
     for (int i = threadIdx.x; i < M; i += blockDim.x) {
@@ -359,8 +363,15 @@ __global__ void loss_reduce_kernel(const float* nll, const int32_t* tgt, const i
         float loss = (float)(s_nll[0] / M);
         float bpb = s_bytes[0] > 0 ? (float)(s_pos[0] / (0.6931471805599453 * s_bytes[0])) : 0.f;
         if (!isfinite(loss)) flag_set(flag, NC_FLAG_NONFINITE);
-        out[0] = loss;
-        out[1] = bpb;
+        if (out) {
+            out[0] = loss;
+            out[1] = bpb;
+        }
+        if (sums) {   // running totals over batches: sum nll, sum nll where bytes > 0, sum bytes
+            sums[0] = (accumulate ? sums[0] : 0.0) + s_nll[0];
+            sums[1] = (accumulate ? sums[1] : 0.0) + s_pos[0];
+            sums[2] = (accumulate ? sums[2] : 0.0) + s_bytes[0];
+        }
     }
 }
 
@@ -535,31 +546,31 @@ int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* tabl
 
 template <typename T>
 int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float scale,
-                  uint32_t* flag, cudaStream_t s, const float2* lse_part) {
+                  uint32_t* flag, cudaStream_t s, const float2* lse_part, bool grad) {
     if (M <= 0) return NC_OK;
     if constexpr (sizeof(T) == 2) {
         if (lse_part && V % (8 * CE2_THREADS) == 0 && V % 128 == 0 && (uintptr_t)logits % 16 == 0) {
-            ce_stats_kernel<<<M, CE2_THREADS, 0, s>>>(logits, lse_part, tgt, nll, V, scale, flag);
+            ce_stats_kernel<<<M, CE2_THREADS, 0, s>>>(logits, lse_part, tgt, nll, V, scale, grad, flag);
             note_launch();
             NC_LAUNCH_CHECK("cross_entropy");
             return NC_OK;
         }
         if (V % (8 * CE2_THREADS) == 0 && (uintptr_t)logits % 16 == 0) {
-            ce_online_kernel<<<M, CE2_THREADS, 0, s>>>(logits, tgt, nll, V, scale, flag);
+            ce_online_kernel<<<M, CE2_THREADS, 0, s>>>(logits, tgt, nll, V, scale, grad, flag);
             note_launch();
             NC_LAUNCH_CHECK("cross_entropy");
             return NC_OK;
         }
     }
-    ce_kernel<T><<<M, CE_THREADS, 0, s>>>(logits, tgt, nll, V, scale, flag);
+    ce_kernel<T><<<M, CE_THREADS, 0, s>>>(logits, tgt, nll, V, scale, grad, flag);
     note_launch();
     NC_LAUNCH_CHECK("cross_entropy");
     return NC_OK;
 }
 
 int loss_reduce(const float* nll, const int32_t* tgt, const int32_t* token_bytes, int M, int V,
-                float* out, uint32_t* flag, cudaStream_t s) {
-    loss_reduce_kernel<<<1, 1024, 0, s>>>(nll, tgt, token_bytes, M, V, out, flag);
+                float* out, uint32_t* flag, cudaStream_t s, double* sums, int accumulate) {
+    loss_reduce_kernel<<<1, 1024, 0, s>>>(nll, tgt, token_bytes, M, V, out, sums, accumulate, flag);
     note_launch();
     NC_LAUNCH_CHECK("loss_reduce");
     return NC_OK;
@@ -620,7 +631,7 @@ int cast_f32_bf16(const float* x, bf16* y, long n, cudaStream_t s) {
                                      T*, int, int, cudaStream_t);                               \
     template int rope_apply<T>(T*, long, int, int, int, int, const float2*, int, float, cudaStream_t); \
     template int cross_entropy<T>(T*, const int32_t*, float*, int, int, float, uint32_t*,       \
-                                  cudaStream_t, const float2*);
+                                  cudaStream_t, const float2*, bool);
 NC_INST(float)
 NC_INST(bf16)
 #undef NC_INST

@@ -79,6 +79,16 @@ class Model:
                               accumulate, grad_scale, out.data_ptr())
         return out
 
+    def eval_loss(self, tokens, targets, token_bytes, B, T, accumulate=0, sums=None, out=None):
+        """Forward and loss only.  Returns the device double[3] running sums
+        {sum nll, sum nll over byte-counted targets, sum bytes}; ``out`` (device
+        float[2], optional) receives this batch's {loss, bpb}."""
+        if sums is None:
+            sums = self.torch.zeros(3, dtype=self.torch.float64, device=self.device)
+        L.nc_eval_loss(self.h, tokens.data_ptr(), targets.data_ptr(), token_bytes.data_ptr(), B, T,
+                       accumulate, sums.data_ptr(), 0 if out is None else out.data_ptr())
+        return sums
+
     def muon_step(self, lr, momentum=0.95, nesterov=True, ns_steps=5, coefs=NS_COEFS):
         L.nc_muon_step(self.h, lr, momentum, int(nesterov), ns_steps, coefs)
 

@@ -46,3 +46,16 @@ def flops_per_token(depth, d_model, vocab, seq_len, causal=False):
     n_matmul = 12 * d_model * d_model * depth + vocab * d_model
     attn = (6 if causal else 12) * depth * d_model * seq_len
     return 6 * n_matmul + attn
+
+
+def chinchilla_steps(depth, d_model, n_head, vocab, tokens_per_step, tokens_per_param=20):
+    """Optimizer steps of a run that trains on tokens_per_param tokens per
+    parameter (section 预搜检: 560M x 20 ~ 11.2B tokens, ~21,400 steps of
+    524,288 tokens at d20)."""
+    return round(tokens_per_param * n_params(depth, d_model, n_head, vocab) / tokens_per_step)
+
+
+def eval_flops_per_token(depth, d_model, vocab, seq_len, causal=False):
+    """Forward-only FLOPs per evaluated token: a third of flops_per_token."""
+    return flops_per_token(depth, d_model, vocab, seq_len, causal) / 3
+
