@@ -35,3 +35,4 @@ from .model import (  # noqa: F401
 )
 from .optim import newton_schulz, muon_step, adamw_step  # noqa: F401
 from . import schedule  # noqa: F401
+from . import generate  # noqa: F401
