@@ -9,7 +9,7 @@ vocab 65536, bf16, 32 x 2048 tokens per step drawn from a Zipf(1.1) stream
 weights.  Replicas only: with --gpus N (under torchrun) every rank trains its
 own replica on its own data; there is no collective on the data path.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload d20|d20x8|d26|d30|eval|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload d20|d20x8|d26|d30|eval|decode|tiny]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
 
   d20x8  the pages' whole optimizer step: 8 accumulated micro-batches of 32 x 2048
@@ -17,6 +17,8 @@ own replica on its own data; there is no collective on the data path.
   d26    depth 26 (d_model 1664, 13 heads), 2 x 16 x 2048 tokens, scheduled rates
   eval   the evaluation pass: d20 forward, loss and bits per byte over 32 x 2048
          tokens per step, no backward (its own metric: evaluation tokens/s)
+  decode inference with the KV cache: prefill of 32 prompts of 1024 tokens, then one
+         greedy decode step for all 32 sequences per timed step (decode tokens/s)
 
 Kernel-level workloads (profiling harnesses, not the headline):
   --workload attn    causal attention forward+backward alone, B=32 (or --batch),
@@ -50,6 +52,7 @@ WORKLOADS = {
     "d26": dict(depth=26, d_model=1664, n_head=13, vocab=65536, B=16, T=2048, n_micro=2, schedule=True),
     "d30": dict(depth=30, d_model=1920, n_head=15, vocab=65536, B=16, T=2048, n_micro=2),
     "eval": dict(depth=20, d_model=1280, n_head=10, vocab=65536, B=32, T=2048, n_micro=1),
+    "decode": dict(depth=20, d_model=1280, n_head=10, vocab=65536, B=32, T=1024, n_micro=1, cache_T=2048),
     "tiny": dict(depth=2, d_model=128, n_head=2, vocab=512, B=4, T=64, n_micro=1),
 }
 HP = dict(muon_lr=0.02, momentum=0.95, ns_steps=5, coefs=(3.4445, -4.7750, 2.0315), lr_emb=0.2,
@@ -59,6 +62,7 @@ HP = dict(muon_lr=0.02, momentum=0.95, ns_steps=5, coefs=(3.4445, -4.7750, 2.031
 # the last SCHED_WARMDOWN of a 20-tokens-per-parameter run (nc_lr_schedule).
 SCHED_D_REF, SCHED_WARMDOWN = 1280, 0.2
 EVAL_METRIC = "evaluation tokens/sec (forward, loss and bits per byte) for d20 on 1 B300"
+DECODE_METRIC = "decode tokens/sec (greedy, KV cache, 32 sequences after 1024-token prompts) for d20 on 1 B300"
 NOMINAL_BF16_TFLOPS = 2250.0
 # Rooflines: the kernel class -> (bound, peak key).  Peaks are the measured
 # copy bandwidth and library bf16 GEMM rates of this GPU pool.
@@ -288,6 +292,17 @@ def kernel_workload(args):
 
 # ---------------------------------------------------------------- main
 # ---------------------------------------------------------------- evaluation pass
+def profiled_pass(L, m, run, n, barrier):
+    """The per-kernel-class breakdown comes from n more steps run after the timed region
+    with the library's CUDA-event profiler on (its events are kept out of the timing)."""
+    L.nc_profile(m.h, 1)
+    for i in range(n):
+        run(i)
+    barrier()
+    L.nc_profile(m.h, 0)
+    return n
+
+
 def kernel_table(L, m, steps, pk):
     kernels = {}
     for c, name in enumerate(L.PROF_NAMES):
@@ -364,7 +379,6 @@ def eval_workload(args):
     stream = torch.cuda.current_stream(dev)
     clocks = Clocks(gpu_id_for(torch, dev))
     time.sleep(0.4)
-    L.nc_profile(m.h, 1)
     launches0 = L.nc_launch_count()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -375,10 +389,11 @@ def eval_workload(args):
     barrier()
     launches = L.nc_launch_count() - launches0
     clk = clocks.stop()
-    L.nc_profile(m.h, 0)
     ms = replicas.max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
     pk = peaks()
-    kernels = kernel_table(L, m, args.steps, pk)
+    n_prof = profiled_pass(L, m, lambda i: m.eval_loss(tok_d, tgt_d, tb, B, T, accumulate=1, sums=sums,
+                                                        out=loss_d), args.steps, barrier)
+    kernels = kernel_table(L, m, n_prof, pk)
     s_host = sums.cpu().numpy()
     loss = loss_d.cpu().numpy()
     g = kernels.get("gemm")
@@ -435,6 +450,169 @@ def eval_workload(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- inference with the KV cache
+def oracle_decode_time(w):
+    """The oracle's cache-free greedy step (the full forward over a 1 x 256 prompt)."""
+    code = (
+        "import sys, time, json\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import oracle\n"
+        "from oracle.model import Config\n"
+        "from oracle import generate as og\n"
+        "from pretraining_step_03_b300 import synth\n"
+        f"w = json.loads({json.dumps(json.dumps(w))})\n"
+        f"T = {CPU_SAMPLE_T}\n"
+        "cfg = Config(w['depth'], w['d_model'], w['n_head'], w['vocab'])\n"
+        "params = synth.init_params(w['depth'], w['d_model'], w['n_head'], w['vocab'], seed=0)\n"
+        "tok, _ = synth.zipf_rows(1, T, w['vocab'], seed=1)\n"
+        "t0 = time.perf_counter()\n"
+        "og.greedy(params, cfg, tok, 1)\n"
+        "print(json.dumps({'T': T, 'time': time.perf_counter() - t0}))\n")
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores),
+               MKL_NUM_THREADS=str(cores), CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed:\n" + r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["T"], d["time"], cores
+
+
+def decode_workload(args):
+    w = WORKLOADS["decode"]
+    from pretraining_step_03_b300 import replicas
+    rank, world, local = replicas.rank_env()
+    B, T0, cT = w["B"], w["T"], w["cache_T"]
+    L_, d, V = w["depth"], w["d_model"], w["vocab"]
+    config = {"workload": "decode", "depth": L_, "d_model": d, "n_head": w["n_head"], "vocab": V,
+              "batch": B * world, "prompt_len": T0, "cache_T": cT, "parallelism": f"replicas{world}",
+              "tokens": "zipf(1.1) prompts, greedy continuation",
+              "l2": "inputs larger than L2 (1.1 GB of weights and 3.4+ GB of KV cache read per step)"}
+    sample_line = "greedy next token after a 1x256 prompt by the cache-free definition (full fp64 forward)"
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        Tc, t, cores = oracle_decode_time(w)   # one bounded sample (a d20 fp64 forward)
+        times = [t]
+        v = 1.0 / t
+        print(json.dumps({"metric": DECODE_METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+                          "steps": len(times), "warmup": 0, "ms_per_step": 1000 / v, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": config, "impl": "reference",
+                          "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                           "sample": sample_line},
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    import numpy as np
+    import torch
+    from pretraining_step_03_b300 import _lib as L
+    from pretraining_step_03_b300.model import Model
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if T0 + args.warmup + 2 * args.steps + 1 > cT:
+        raise SystemExit("decode: prompt + steps exceed the cache")
+    prompt, _ = synth.zipf_rows(B, T0, V, seed=replicas.data_seed(rank) + 200)
+    m = Model(L_, d, w["n_head"], V, B, cT, dtype="bf16", seed=0, device=dev)
+    cache = m.kv_cache(B, cT)
+    toks = torch.zeros(1 + args.warmup + 2 * args.steps + 1, B, dtype=torch.int32, device=dev)
+    p_d = torch.from_numpy(prompt.reshape(-1)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # prefill (timed on its own: a second call overwrites the same cache rows)
+    m.prefill(cache, p_d, B, T0, next_tok=toks[0])
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    m.prefill(cache, p_d, B, T0, next_tok=toks[0])
+    e1.record(stream)
+    barrier()
+    prefill_ms = e0.elapsed_time(e1)
+    for i in range(args.warmup):
+        m.decode_step(cache, toks[i], B, T0 + i, next_tok=toks[i + 1])
+    barrier()
+    clocks = Clocks(gpu_id_for(torch, dev))
+    time.sleep(0.4)
+    launches0 = L.nc_launch_count()
+    barrier()
+    e0.record(stream)
+    for i in range(args.warmup, args.warmup + args.steps):
+        m.decode_step(cache, toks[i], B, T0 + i, next_tok=toks[i + 1])
+    e1.record(stream)
+    barrier()
+    launches = L.nc_launch_count() - launches0
+    clk = clocks.stop()
+    ms = replicas.max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
+    pk = peaks()
+    i0 = args.warmup + args.steps
+    n_prof = profiled_pass(L, m, lambda i: m.decode_step(cache, toks[i0 + i], B, T0 + i0 + i,
+                                                          next_tok=toks[i0 + i + 1]), args.steps, barrier)
+    kernels = kernel_table(L, m, n_prof, pk)
+    flag = m.check_flag()
+    # algorithmic bytes of one decode step: every weight once, the cache read up to the
+    # step's position (mean over the timed steps) and the new k, v written
+    n_mean = T0 + args.warmup + (args.steps + 1) / 2.0
+    wbytes = (12 * d * d * L_ + V * d) * 2
+    kvbytes = 2 * L_ * B * n_mean * d * 2 + 2 * L_ * B * d * 2
+    achieved = (wbytes + kvbytes) / (ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "the decode step (weights by the swapped tcgen05 GEMMs, cache by "
+                "decode_attn_kernel)", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"], "peak_kind": f"copy bandwidth ({pk['source']})",
+                "traffic": None, "bytes_per_step": wbytes + kvbytes}
+    # end to end: this step's tokens from pinned host memory in, the next tokens out
+    tok_h = torch.from_numpy(toks[args.warmup].cpu().numpy().copy()).pin_memory()
+    nxt_h = torch.zeros(B, dtype=torch.int32).pin_memory()
+    t_in = torch.empty(B, dtype=torch.int32, device=dev)
+    t_out = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def host_step(pos):
+        t_in.copy_(tok_h, non_blocking=True)
+        m.decode_step(cache, t_in, B, pos, next_tok=t_out)
+        nxt_h.copy_(t_out, non_blocking=True)
+        stream.synchronize()
+        tok_h.copy_(nxt_h)
+
+    base = T0 + args.warmup
+    host_step(base)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        host_step(base + i)
+    barrier()
+    e2e_s = replicas.max_over_ranks((time.perf_counter() - t0) / args.steps, dist, dev)
+    value = replicas.job_rate(world, B, ms * 1e-3)
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+        "prefill": {"ms": prefill_ms, "tokens_per_s": B * T0 / (prefill_ms * 1e-3)},
+        "device_flag": flag, "gpu_launches": int(launches), "roofline": roofline, "kernels": kernels,
+        "e2e": {"value": replicas.job_rate(world, B, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": B * 4,
+                "d2h_bytes_per_step": B * 4, "ms_per_step": 1000 * e2e_s},
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        Tc, t, cores = oracle_decode_time(w)
+        line["cpu_baseline"] = {"value": 1.0 / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample_line}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,6 +627,8 @@ def main():
         return kernel_workload(args)
     if args.workload == "eval":
         return eval_workload(args)
+    if args.workload == "decode":
+        return decode_workload(args)
     w = WORKLOADS[args.workload]
     from pretraining_step_03_b300 import replicas
     rank, world, local = replicas.rank_env()
@@ -534,7 +714,6 @@ def main():
     stream = torch.cuda.current_stream(dev)
     clocks = Clocks(gpu_id_for(torch, dev))
     time.sleep(0.4)
-    L.nc_profile(m.h, 1)
     launches0 = L.nc_launch_count()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -545,12 +724,12 @@ def main():
     barrier()
     launches = L.nc_launch_count() - launches0
     clk = clocks.stop()
-    L.nc_profile(m.h, 0)
     ms = replicas.max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
     loss = loss_d.cpu().numpy().mean(axis=0)
     flag = m.check_flag()
     pk = peaks()
-    kernels = kernel_table(L, m, args.steps, pk)
+    n_prof = profiled_pass(L, m, lambda i: step(args.warmup + args.steps + i), min(args.steps, 2), barrier)
+    kernels = kernel_table(L, m, n_prof, pk)
     g = kernels.get("gemm")
     roofline = None
     if g:

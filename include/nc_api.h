@@ -165,6 +165,40 @@ NC_API int nc_train_step(nc_model* m, const int32_t* tokens_host, const int32_t*
                   float weight_decay, int adam_step, float* loss_bpb_host);
 
 /*
+ * Inference with a KV cache (section 预搜检, on sampling from the base model: an
+ * Engine with a KV cache runs prefill and decode).  The cache is caller-owned
+ * device memory of nc_kv_cache_bytes(m, cache_B, cache_T) bytes, 16-byte
+ * aligned, laid out [layer][k | v][cache_B][cache_T][d_model] in the model's
+ * activation type, k after RoPE.  cache_T <= the model's max_T.  Both calls
+ * use the model's training activations as scratch (a training step in between
+ * is fine; the cache holds all state of the sequences) and are asynchronous.
+ */
+NC_API int nc_kv_cache_bytes(nc_model* m, int cache_B, int cache_T, size_t* out);
+
+/*
+ * Prefill: B prompts of T0 tokens (tokens: device int32 [B*T0], row b*T0 + t),
+ * 1 <= B <= cache_B, T0 <= cache_T, B*T0 <= max_B*max_T.  Writes k and v of
+ * positions 0 .. T0-1 of sequence b into cache row b, and for the last
+ * position of every prompt the logits (logits_out: device float [B*V] or
+ * NULL) and the greedy next token (next_out: device int32 [B] or NULL; the
+ * lowest id among equal maxima).
+ */
+NC_API int nc_prefill(nc_model* m, void* cache, int cache_B, int cache_T, const int32_t* tokens, int B,
+                      int T0, float* logits_out, int32_t* next_out);
+
+/*
+ * Decode: tokens (device int32 [B]) is the token at position pos of each of the
+ * sequences in cache rows 0 .. B-1, whose positions 0 .. pos-1 are cached.
+ * Appends its k and v at position pos and returns the logits of the next
+ * position and the greedy next token as nc_prefill does.  0 <= pos < cache_T.
+ * Errors: NC_ERR_ARG for a bad cache, B, pos or pointer; NC_ERR_UNSUPPORTED
+ * for head dims other than 128.  An out-of-range token sets
+ * NC_FLAG_TOKEN_RANGE (its row embeds as zeros).
+ */
+NC_API int nc_decode_step(nc_model* m, void* cache, int cache_B, int cache_T, const int32_t* tokens, int B,
+                          int pos, float* logits_out, int32_t* next_out);
+
+/*
  * Learning rates of optimizer step `step` (0-based) of an n_steps run (section
  * 预搜检: the rate scales as 1/sqrt(dim), and the multiplier lrm falls
  * linearly to 0 near the end of training).  Host arithmetic, no device work.

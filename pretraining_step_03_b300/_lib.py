@@ -42,6 +42,9 @@ SIGNATURES = {
     "nc_forward_backward": (_I, [_V, _V, _V, _V, _I, _I, _I, _F, _V]),
     "nc_eval_loss": (_I, [_V, _V, _V, _V, _I, _I, _I, _V, _V]),
     "nc_lr_schedule": (_I, [_I, _I, _F, _I, _I, ctypes.POINTER(_F), ctypes.POINTER(_F)]),
+    "nc_kv_cache_bytes": (_I, [_V, _I, _I, ctypes.POINTER(_SZ)]),
+    "nc_prefill": (_I, [_V, _V, _I, _I, _V, _I, _I, _V, _V]),
+    "nc_decode_step": (_I, [_V, _V, _I, _I, _V, _I, _I, _V, _V]),
     "nc_muon_step": (_I, [_V, _F, _F, _I, _I, ctypes.POINTER(_F)]),
     "nc_adamw_step": (_I, [_V, _F, _F, _F, _F, _F, _F, _I]),
     "nc_train_step": (_I, [_V, _V, _V, _V, _I, _I, _I, _F, _F, _I, ctypes.POINTER(_F), _F, _F, _F,
@@ -137,6 +140,20 @@ def nc_forward_backward(m, tokens, targets, token_bytes, B, T, accumulate, grad_
 
 def nc_eval_loss(m, tokens, targets, token_bytes, B, T, accumulate, sums, loss_bpb_out):
     _check(lib().nc_eval_loss(m, tokens, targets, token_bytes, B, T, accumulate, sums, loss_bpb_out))
+
+
+def nc_kv_cache_bytes(m, cache_B, cache_T):
+    n = ctypes.c_size_t()
+    _check(lib().nc_kv_cache_bytes(m, cache_B, cache_T, ctypes.byref(n)))
+    return n.value
+
+
+def nc_prefill(m, cache, cache_B, cache_T, tokens, B, T0, logits_out, next_out):
+    _check(lib().nc_prefill(m, cache, cache_B, cache_T, tokens, B, T0, logits_out, next_out))
+
+
+def nc_decode_step(m, cache, cache_B, cache_T, tokens, B, pos, logits_out, next_out):
+    _check(lib().nc_decode_step(m, cache, cache_B, cache_T, tokens, B, pos, logits_out, next_out))
 
 
 def nc_lr_schedule(step, n_steps, warmdown_frac, d_model, d_ref, base):

@@ -733,6 +733,220 @@ int nc_train_step(nc_model* m, const int32_t* tokens_host, const int32_t* target
     return NC_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// ---------------------------------------------------------------- inference with a KV cache
+// Cache layout: [layer][k | v][cache_B][cache_T][d] in the model's activation type.
+template <typename T>
+struct Cache {
+    T* base;
+    int B, T_, d;
+    T* k(int l) const { return base + (size_t)l * 2 * B * T_ * d; }
+    T* v(int l) const { return k(l) + (size_t)B * T_ * d; }
+};
+
+int round8(int b) { return (b + 7) & ~7; }
+
+// greedy token and (optionally) the logits of the Bp token rows in y [Bp][d]
+template <typename T>
+int lm_head_rows(nc_model* m, const void* y, int B, int Bp, float* logits_out, int32_t* next_out) {
+    const int d = m->d, V = m->V, iu = 1 + 6 * m->depth;
+    float* lt = reinterpret_cast<float*>(m->logits);   // logits^T [V][Bp]
+    NC_TRY(run_gemm(m, mk(m, V, Bp, d, W<T>(m, iu), d, false, y, d, false, lt, Bp, NC_FP32)));
+    Prof pr(m, NC_PROF_CE, 0, (double)V * Bp * 4);
+    // (the argmax partials use the attention-gradient scratch, idle outside the backward)
+    const size_t ws_bytes = (size_t)m->maxM * 3 * d * (m->dtype == NC_BF16 ? 2 : 4);
+    if (next_out) NC_TRY(decode_argmax(lt, V, B, Bp, next_out, m->dqkv, ws_bytes, m->flag, m->stream));
+    if (logits_out) NC_TRY(decode_logits_out(lt, V, B, Bp, logits_out, m->stream));
+    return NC_OK;
+}
+
+template <typename T>
+int prefill(nc_model* m, const Cache<T>& c, const int32_t* tok, int B, int T0, float* logits_out,
+            int32_t* next_out) {
+    const int d = m->d, H = m->H, Dh = m->Dh, F = m->F, V = m->V;
+    const int M = B * T0, act = m->dtype, Bp = round8(B);
+    const double ab = m->dtype == NC_BF16 ? 2.0 : 4.0;
+    const double Md = (double)M * d;
+    cudaStream_t s = m->stream;
+    const bool fuse_rope = m->dtype == NC_BF16 && Dh == 128;
+    const int rope_ld = m->maxT > 0 ? m->maxT : 1;
+    {
+        Prof pr(m, NC_PROF_EMBED, 0, Md * (ab + 4) + M * 4.0);
+        NC_TRY(embed_forward<T>(tok, W<T>(m, 0), m->x, M, d, V, m->flag, s));
+    }
+    for (int l = 0; l < m->depth; ++l) {
+        auto& Ly = m->L[l];
+        const int b0 = 1 + 6 * l;
+        {
+            Prof pr(m, NC_PROF_NORM, 0, Md * (4 + ab) + M * 4.0);
+            NC_TRY(rmsnorm_forward<T>(m->x, (T*)Ly.y1, Ly.r1, M, d, s));
+        }
+        {
+            Gemm g = mk(m, M, 3 * d, d, Ly.y1, d, false, W<T>(m, b0), d, false, Ly.qkv, 3 * d, act);
+            if (fuse_rope) {
+                g.epi = EPI_ROPE; g.rope = m->rope; g.rope_T = T0; g.rope_cols = 2 * d; g.rope_ld = rope_ld;
+            }
+            NC_TRY(run_gemm(m, g));
+            if (!fuse_rope) {
+                Prof pr(m, NC_PROF_ROPE, 0, 4.0 * Md * ab);
+                NC_TRY(rope_apply<T>((T*)Ly.qkv, 3 * d, M, T0, H, Dh, m->rope, rope_ld, 1.f, s));
+            }
+        }
+        T* q = (T*)Ly.qkv;
+        {
+            Prof pr(m, NC_PROF_ROPE, 0, 4.0 * Md * ab);
+            NC_TRY(prefill_kv_store<T>(q, B, T0, d, c.k(l), c.v(l), c.T_, s));
+        }
+        {
+            Prof pr(m, NC_PROF_ATTN_FWD, 4.0 * B * H * Dh * (0.5 * T0 * (T0 + 1.0)), 0);
+            NC_TRY(attention_forward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, d, Ly.lse, B, T0, H, Dh, s));
+        }
+        {
+            Gemm g = mk(m, M, d, d, Ly.o, d, false, W<T>(m, b0 + 3), d, false, m->x, d, NC_FP32);
+            g.aux = m->x; g.ldaux = d; g.aux_dtype = NC_FP32; g.beta = 1.f;
+            NC_TRY(run_gemm(m, g));
+        }
+        {
+            Prof pr(m, NC_PROF_NORM, 0, Md * (4 + ab) + M * 4.0);
+            NC_TRY(rmsnorm_forward<T>(m->x, (T*)Ly.y2, Ly.r2, M, d, s));
+        }
+        {
+            Gemm g = mk(m, M, F, d, Ly.y2, d, false, W<T>(m, b0 + 4), d, false, Ly.a, F, act);
+            g.epi = EPI_RELU2;
+            NC_TRY(run_gemm(m, g));
+        }
+        {
+            Gemm g = mk(m, M, d, F, Ly.a, F, false, W<T>(m, b0 + 5), F, false, m->x, d, NC_FP32);
+            g.aux = m->x; g.ldaux = d; g.aux_dtype = NC_FP32; g.beta = 1.f;
+            NC_TRY(run_gemm(m, g));
+        }
+    }
+    {
+        Prof pr(m, NC_PROF_NORM, 0, Md * (4 + ab) + M * 4.0);
+        NC_TRY(rmsnorm_forward<T>(m->x, (T*)m->yf, m->rf, M, d, s));
+        NC_TRY(prefill_gather_last<T>((const T*)m->yf, B, Bp, T0, d, (T*)m->dy, s));
+    }
+    return lm_head_rows<T>(m, m->dy, B, Bp, logits_out, next_out);
+}
+
+template <typename T>
+int decode_step(nc_model* m, const Cache<T>& c, const int32_t* tok, int B, int pos, float* logits_out,
+                int32_t* next_out) {
+    const int d = m->d, H = m->H, Dh = m->Dh, F = m->F, V = m->V;
+    const int Bp = round8(B), n = pos + 1, act = m->dtype;
+    const double ab = m->dtype == NC_BF16 ? 2.0 : 4.0;
+    cudaStream_t s = m->stream;
+    const int rope_ld = m->maxT > 0 ? m->maxT : 1;
+    // scratch in the training activations: x^T, the normed rows, [q|k|v]^T, q, the attention
+    // output, a^T (relu(h)^2), and the attention partials
+    float* xt = m->x;
+    T* y = (T*)m->yf;
+    T* cq = (T*)m->L[0].qkv;
+    T* q = (T*)m->L[0].o;
+    T* att = (T*)m->L[0].y2;
+    T* at = (T*)m->L[0].a;
+    void* ws = m->dqkv;
+    const size_t ws_bytes = (size_t)m->maxM * 3 * d * (size_t)ab;
+    {
+        Prof pr(m, NC_PROF_EMBED, 0, (double)B * d * (ab + 4));
+        NC_TRY(decode_embed_t<T>(tok, W<T>(m, 0), xt, B, Bp, d, V, m->flag, s));
+    }
+    auto norm = [&]() {
+        Prof pr(m, NC_PROF_NORM, 0, (double)Bp * d * (4 + ab));
+        return decode_rmsnorm_cols<T>(xt, y, Bp, d, s);
+    };
+    for (int l = 0; l < m->depth; ++l) {
+        const int b0 = 1 + 6 * l;
+        NC_TRY(norm());
+        NC_TRY(run_gemm(m, mk(m, 3 * d, Bp, d, W<T>(m, b0), d, false, y, d, false, cq, Bp, act)));
+        {
+            Prof pr(m, NC_PROF_ROPE, 0, (double)Bp * 3 * d * ab * 2);
+            NC_TRY(decode_qkv_post<T>(cq, B, Bp, d, H, Dh, pos, m->rope, rope_ld, q, c.k(l), c.v(l), c.T_, s));
+        }
+        {
+            Prof pr(m, NC_PROF_ATTN_FWD, 4.0 * B * H * Dh * n, 2.0 * B * n * d * ab);
+            NC_TRY(decode_attention<T>(q, c.k(l), c.v(l), B, Bp, d, H, Dh, c.T_, n, att, ws, ws_bytes, s));
+        }
+        {   // x^T += Wo att^T
+            Gemm g = mk(m, d, Bp, d, W<T>(m, b0 + 3), d, false, att, d, false, xt, Bp, NC_FP32);
+            g.aux = xt; g.ldaux = Bp; g.aux_dtype = NC_FP32; g.beta = 1.f;
+            NC_TRY(run_gemm(m, g));
+        }
+        NC_TRY(norm());
+        {   // a^T = relu(W1 y^T)^2
+            Gemm g = mk(m, F, Bp, d, W<T>(m, b0 + 4), d, false, y, d, false, at, Bp, act);
+            g.epi = EPI_RELU2;
+            NC_TRY(run_gemm(m, g));
+        }
+        {   // x^T += W2 a^T (a^T stored [F][Bp]: the K x N layout of the second operand)
+            Gemm g = mk(m, d, Bp, F, W<T>(m, b0 + 5), F, false, at, Bp, true, xt, Bp, NC_FP32);
+            g.aux = xt; g.ldaux = Bp; g.aux_dtype = NC_FP32; g.beta = 1.f;
+            NC_TRY(run_gemm(m, g));
+        }
+    }
+    NC_TRY(norm());
+    return lm_head_rows<T>(m, y, B, Bp, logits_out, next_out);
+}
+
+int check_cache(nc_model* m, const void* cache, int cache_B, int cache_T, int B) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    if (!cache) return set_error(NC_ERR_ARG, "null cache");
+    if ((uintptr_t)cache % 16) return set_error(NC_ERR_ARG, "cache must be 16-byte aligned");
+    if (cache_B < 1 || cache_T < 1) return set_error(NC_ERR_ARG, "cache_B %d, cache_T %d", cache_B, cache_T);
+    if (cache_T > m->maxT) return set_error(NC_ERR_ARG, "cache_T %d > the model's max_T %d", cache_T, m->maxT);
+    if (B < 1 || B > cache_B) return set_error(NC_ERR_ARG, "B = %d outside [1, cache_B = %d]", B, cache_B);
+    const long Bp = round8(B);
+    const double ab = m->dtype == NC_BF16 ? 2.0 : 4.0;
+    if (Bp > m->maxM || Bp * 4.0 > m->maxM * ab)
+        return set_error(NC_ERR_ARG, "B = %d too large for the arena (max_B*max_T = %ld)", B, m->maxM);
+    if (m->Dh != 128) return set_error(NC_ERR_UNSUPPORTED, "inference path: head dim %d (128 only)", m->Dh);
+    return NC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int nc_kv_cache_bytes(nc_model* m, int cache_B, int cache_T, size_t* out) {
+    if (!m || !out) return set_error(NC_ERR_ARG, "null argument");
+    if (cache_B < 1 || cache_T < 1) return set_error(NC_ERR_ARG, "cache_B %d, cache_T %d", cache_B, cache_T);
+    *out = (size_t)m->depth * 2 * cache_B * cache_T * m->d * (m->dtype == NC_BF16 ? 2 : 4);
+    return NC_OK;
+}
+
+int nc_prefill(nc_model* m, void* cache, int cache_B, int cache_T, const int32_t* tokens, int B, int T0,
+               float* logits_out, int32_t* next_out) {
+    NC_TRY(check_cache(m, cache, cache_B, cache_T, B));
+    if (!tokens) return set_error(NC_ERR_ARG, "null tokens");
+    if (T0 < 1 || T0 > cache_T || (long)B * T0 > m->maxM)
+        return set_error(NC_ERR_ARG, "T0 = %d: needs 1 <= T0 <= cache_T and B*T0 <= max_B*max_T", T0);
+    g_gemm_flag = m->flag;
+    g_attn_flag = m->flag;
+    if (m->dtype == NC_BF16)
+        return prefill<bf16>(m, Cache<bf16>{(bf16*)cache, cache_B, cache_T, m->d}, tokens, B, T0, logits_out, next_out);
+    return prefill<float>(m, Cache<float>{(float*)cache, cache_B, cache_T, m->d}, tokens, B, T0, logits_out,
+                          next_out);
+}
+
+int nc_decode_step(nc_model* m, void* cache, int cache_B, int cache_T, const int32_t* tokens, int B, int pos,
+                   float* logits_out, int32_t* next_out) {
+    NC_TRY(check_cache(m, cache, cache_B, cache_T, B));
+    if (!tokens) return set_error(NC_ERR_ARG, "null tokens");
+    if (pos < 0 || pos >= cache_T) return set_error(NC_ERR_ARG, "pos %d outside [0, cache_T = %d)", pos, cache_T);
+    if (decode_attention_ws_bytes(B, m->H, pos + 1) > (size_t)m->maxM * 3 * m->d * (m->dtype == NC_BF16 ? 2 : 4))
+        return set_error(NC_ERR_ARG, "decode workspace too small for B = %d", B);
+    g_gemm_flag = m->flag;
+    g_attn_flag = m->flag;
+    if (m->dtype == NC_BF16)
+        return decode_step<bf16>(m, Cache<bf16>{(bf16*)cache, cache_B, cache_T, m->d}, tokens, B, pos, logits_out,
+                                 next_out);
+    return decode_step<float>(m, Cache<float>{(float*)cache, cache_B, cache_T, m->d}, tokens, B, pos, logits_out,
+                              next_out);
+}
+
 int nc_lr_schedule(int step, int n_steps, float warmdown_frac, int d_model, int d_ref, const float base[3],
                    float out[3]) {
     if (!base || !out) return set_error(NC_ERR_ARG, "null pointer");

@@ -947,9 +947,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // C = alpha * sum_s ws[s] + beta * aux, fixed summation order.
+__device__ __forceinline__ float split_epi(float v, int epi) {
+    if (epi == EPI_RELU2) {
+        const float r = fmaxf(v, 0.f);
+        return r * r;
+    }
+    return v;
+}
+
 __global__ void splitk_reduce_kernel(const float* ws, int splits, int batch, int M, int N, void* C,
                                      long ldc, long sC, int c_dtype, const void* aux, long ldaux,
-                                     long sAux, int aux_dtype, float alpha, float beta) {
+                                     long sAux, int aux_dtype, float alpha, float beta, int epi) {
     const long total = (long)batch * M * N;
     const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= total) return;
@@ -957,8 +965,8 @@ __global__ void splitk_reduce_kernel(const float* ws, int splits, int batch, int
     float s = 0.f;
     for (int k = 0; k < splits; ++k) s += ws[(long)k * total + i];
     s *= alpha;
-    if (aux && beta != 0.f) s += beta * ld_elem(aux, b * sAux + m * ldaux + n, aux_dtype);
-    st_elem(C, b * sC + m * ldc + n, c_dtype, s);
+    if (epi == EPI_STORE && aux && beta != 0.f) s += beta * ld_elem(aux, b * sAux + m * ldaux + n, aux_dtype);
+    st_elem(C, b * sC + m * ldc + n, c_dtype, split_epi(s, epi));
 }
 
 // The same, four consecutive columns per thread (16-byte loads of every partial) and 32-bit
@@ -967,7 +975,8 @@ __global__ void splitk_reduce_kernel(const float* ws, int splits, int batch, int
 __global__ void __launch_bounds__(256) splitk_reduce4_kernel(const float* ws, int splits, int rows, int M,
                                                              int N, void* C, long ldc, long sC, int c_dtype,
                                                              const void* aux, long ldaux, long sAux,
-                                                             int aux_dtype, float alpha, float beta) {
+                                                             int aux_dtype, float alpha, float beta,
+                                                             int epi) {
     const int n4 = N / 4;
     const long total = (long)rows * N;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < rows * n4; i += gridDim.x * blockDim.x) {
@@ -980,7 +989,7 @@ __global__ void __launch_bounds__(256) splitk_reduce4_kernel(const float* ws, in
             acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
         }
         float o[4] = {acc.x * alpha, acc.y * alpha, acc.z * alpha, acc.w * alpha};
-        if (aux && beta != 0.f) {
+        if (epi == EPI_STORE && aux && beta != 0.f) {
             const long ai = (long)b * sAux + (long)m * ldaux + c;
             if (aux_dtype == NC_FP32) {
                 const float4 a = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(aux) + ai)[0];
@@ -990,6 +999,8 @@ __global__ void __launch_bounds__(256) splitk_reduce4_kernel(const float* ws, in
                 for (int e = 0; e < 4; ++e) o[e] += beta * ld_elem(aux, ai + e, aux_dtype);
             }
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = split_epi(o[e], epi);
         const long ci = (long)b * sC + (long)m * ldc + c;
         if (c_dtype == NC_FP32) {
             reinterpret_cast<float4*>(reinterpret_cast<float*>(C) + ci)[0] = make_float4(o[0], o[1], o[2], o[3]);
@@ -1053,21 +1064,29 @@ double wave_eff(long units, int slots) {
     return (double)units / ((double)waves * slots);
 }
 
-// Split K over CTAs when that fills the GPU's waves better.  Modelled time:
-// the MMA work at ~1.4 PFLOP/s divided by the wave efficiency, plus, for
-// s > 1, writing and re-reading s fp32 partials of the output at ~6 TB/s.
-// In practice this splits the long-K, small-output weight gradients only.
+// Split K over CTAs when that fills the GPU's waves better.  Modelled time: the
+// larger of the MMA work at ~1.4 PFLOP/s divided by the wave efficiency and the
+// operand bytes at ~50 GB/s per CTA (at most ~6 TB/s), plus, for s > 1, writing
+// and re-reading s fp32 partials of the output at ~6 TB/s.  This splits the
+// long-K, small-output weight gradients and, where the operand stream is the
+// bound (a few token rows against a weight matrix), the small-N products.
 int pick_splits(const Gemm& g, int tiles, int num_kb, int slots) {
-    if (g.epi != EPI_STORE || num_kb < 16) return 1;
+    if ((g.epi != EPI_STORE && g.epi != EPI_RELU2) || num_kb < 8) return 1;
     const long work = (long)tiles * g.batch;
     const double flops = 2.0 * g.M * g.N * (double)g.K * g.batch;
+    const double op_bytes = ((double)g.M + g.N) * g.K * g.batch * 2.0;
     const double out_bytes = (double)g.M * g.N * g.batch * 4.0;
     auto cost = [&](int s) {
-        return flops / 1.4e15 / wave_eff(work * s, slots) + (s > 1 ? 2.0 * s * out_bytes / 6.0e12 : 0.0);
+        const double mma = flops / 1.4e15 / wave_eff(work * s, slots);
+        const double mem = op_bytes / fmin(6.0e12, (double)fmin(work * s, (long)slots) * 5.0e10);
+        return fmax(mma, mem) + (s > 1 ? 2.0 * s * out_bytes / 6.0e12 : 0.0);
     };
+    const bool mem_bound = op_bytes / 6.0e12 > flops / 1.4e15;
+    const int min_kb = mem_bound ? 4 : 8;
+    if (num_kb < 2 * min_kb) return 1;
     int bs = 1;
     double best = cost(1);
-    for (int s = 2; s <= 16 && num_kb / s >= 8; ++s) {
+    for (int s = 2; s <= 16 && num_kb / s >= min_kb; ++s) {
         const double c = cost(s);
         if (c < 0.97 * best) {
             best = c;
@@ -1262,11 +1281,11 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
             const int blocks = (int)(quads / 256 < 8L * num_sms() ? ceil_div(quads, 256) : 8L * num_sms());
             splitk_reduce4_kernel<<<blocks, 256, 0, s>>>(p.ws, p.splits, g.batch * g.M, g.M, g.N, g.C, g.ldc,
                                                          g.sC, g.c_dtype, g.aux, g.ldaux, g.sAux, g.aux_dtype,
-                                                         g.alpha, g.beta);
+                                                         g.alpha, g.beta, g.epi);
         } else {
             splitk_reduce_kernel<<<ceil_div(total, 256), 256, 0, s>>>(
                 p.ws, p.splits, g.batch, g.M, g.N, g.C, g.ldc, g.sC, g.c_dtype, g.aux, g.ldaux, g.sAux,
-                g.aux_dtype, g.alpha, g.beta);
+                g.aux_dtype, g.alpha, g.beta, g.epi);
         }
         note_launch();
         NC_LAUNCH_CHECK("splitk_reduce");

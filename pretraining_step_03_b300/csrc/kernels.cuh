@@ -78,6 +78,33 @@ int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float
 // added to (accumulate = 1).  One CTA, fixed summation order.
 int loss_reduce(const float* nll, const int32_t* tgt, const int32_t* token_bytes, int M, int V,
                 float* out, uint32_t* flag, cudaStream_t s, double* sums = nullptr, int accumulate = 0);
+// ------------------------------------------------------------ inference (decode.cu)
+// Decode works on B sequences in a transposed layout with Bp = B rounded up to 8 columns:
+// residual x^T [d][Bp] fp32, projections [N][Bp] = W [N, K] x Y[Bp, K]^T.
+template <typename T>
+int decode_embed_t(const int32_t* tok, const T* wte, float* xt, int B, int Bp, int d, int V, uint32_t* flag,
+                   cudaStream_t s);
+template <typename T>
+int decode_rmsnorm_cols(const float* xt, T* y, int Bp, int d, cudaStream_t s);
+// [q|k|v]^T [3d][Bp] at position pos -> q [Bp][d] (RoPE), cache rows (b, pos) of k (RoPE) and v
+template <typename T>
+int decode_qkv_post(const T* c, int B, int Bp, int d, int H, int Dh, int pos, const float2* rope, int rope_ld,
+                    T* q, T* kc, T* vc, int cache_T, cudaStream_t s);
+// out [Bp][d] = softmax(q k^T / sqrt(Dh)) v over cache rows 0 .. n-1 of each of the B sequences
+// (rows B .. Bp-1 of out are zeroed); head dim 128
+size_t decode_attention_ws_bytes(int B, int H, int n);
+template <typename T>
+int decode_attention(const T* q, const T* kc, const T* vc, int B, int Bp, int d, int H, int Dh, int cache_T,
+                     int n, T* out, void* ws, size_t ws_bytes, cudaStream_t s);
+// next[b] = argmax_v logits^T[v][b] (lowest id on ties); ws >= B * 512 bytes
+int decode_argmax(const float* lt, int V, int B, int Bp, int32_t* next, void* ws, size_t ws_bytes, uint32_t* flag,
+                  cudaStream_t s);
+int decode_logits_out(const float* lt, int V, int B, int Bp, float* out, cudaStream_t s);
+template <typename T>
+int prefill_kv_store(const T* qkv, int B, int T0, int d, T* kc, T* vc, int cache_T, cudaStream_t s);
+template <typename T>
+int prefill_gather_last(const T* y, int B, int Bp, int T0, int d, T* out, cudaStream_t s);
+
 struct EmbedBwdWs {
     int* hist;       // [nchunks * V]
     int* rank;       // [M]

@@ -89,6 +89,34 @@ class Model:
                        accumulate, sums.data_ptr(), 0 if out is None else out.data_ptr())
         return sums
 
+    # ---------------------------------------------------------------- inference
+    def kv_cache(self, cache_B, cache_T):
+        """A device KV cache for cache_B sequences of up to cache_T positions."""
+        n = L.nc_kv_cache_bytes(self.h, cache_B, cache_T)
+        return KVCache(self.torch.empty(n, dtype=self.torch.uint8, device=self.device), cache_B, cache_T)
+
+    def prefill(self, cache, tokens, B, T0, logits=None, next_tok=None):
+        """tokens: device int32 [B*T0].  Fills positions 0..T0-1 of cache rows 0..B-1."""
+        L.nc_prefill(self.h, cache.buf.data_ptr(), cache.B, cache.T, tokens.data_ptr(), B, T0,
+                     0 if logits is None else logits.data_ptr(), 0 if next_tok is None else next_tok.data_ptr())
+
+    def decode_step(self, cache, tokens, B, pos, logits=None, next_tok=None):
+        """tokens: device int32 [B], the tokens at position pos."""
+        L.nc_decode_step(self.h, cache.buf.data_ptr(), cache.B, cache.T, tokens.data_ptr(), B, pos,
+                         0 if logits is None else logits.data_ptr(), 0 if next_tok is None else next_tok.data_ptr())
+
+    def generate(self, cache, prompt, n_new):
+        """Greedy continuation of B equal-length prompts (device int32 [B, T0]) by n_new
+        tokens; returns the device int32 [n_new, B] tokens (step-major: each step's
+        tokens are the next step's input, in place)."""
+        torch = self.torch
+        B, T0 = prompt.shape
+        out = torch.empty(n_new, B, dtype=torch.int32, device=self.device)
+        self.prefill(cache, prompt.reshape(-1).contiguous(), B, T0, next_tok=out[0])
+        for i in range(1, n_new):
+            self.decode_step(cache, out[i - 1], B, T0 + i - 1, next_tok=out[i])
+        return out
+
     def muon_step(self, lr, momentum=0.95, nesterov=True, ns_steps=5, coefs=NS_COEFS):
         L.nc_muon_step(self.h, lr, momentum, int(nesterov), ns_steps, coefs)
 
@@ -119,3 +147,11 @@ class Model:
             self.close()
         except Exception:
             pass
+
+
+class KVCache:
+    """Device buffer of a KV cache and its geometry (see nc_kv_cache_bytes)."""
+
+    def __init__(self, buf, B, T):
+        self.buf, self.B, self.T = buf, B, T
+
