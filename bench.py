@@ -517,7 +517,7 @@ def decode_workload(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    if T0 + args.warmup + 2 * args.steps + 1 > cT:
+    if T0 + args.warmup + 3 * args.steps + 3 > cT:
         raise SystemExit("decode: prompt + steps exceed the cache")
     prompt, _ = synth.zipf_rows(B, T0, V, seed=replicas.data_seed(rank) + 200)
     m = Model(L_, d, w["n_head"], V, B, cT, dtype="bf16", seed=0, device=dev)
@@ -540,8 +540,14 @@ def decode_workload(args):
     e1.record(stream)
     barrier()
     prefill_ms = e0.elapsed_time(e1)
+    # two fixed token buffers in turn: from the third step on every step replays a graph
+    buf = [toks[0].clone(), torch.empty_like(toks[0])]
+
+    def dstep(i):
+        m.decode_step(cache, buf[i % 2], B, T0 + i, next_tok=buf[(i + 1) % 2])
+
     for i in range(args.warmup):
-        m.decode_step(cache, toks[i], B, T0 + i, next_tok=toks[i + 1])
+        dstep(i)
     barrier()
     clocks = Clocks(gpu_id_for(torch, dev))
     time.sleep(0.4)
@@ -549,7 +555,7 @@ def decode_workload(args):
     barrier()
     e0.record(stream)
     for i in range(args.warmup, args.warmup + args.steps):
-        m.decode_step(cache, toks[i], B, T0 + i, next_tok=toks[i + 1])
+        dstep(i)
     e1.record(stream)
     barrier()
     launches = L.nc_launch_count() - launches0
@@ -557,8 +563,7 @@ def decode_workload(args):
     ms = replicas.max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
     pk = peaks()
     i0 = args.warmup + args.steps
-    n_prof = profiled_pass(L, m, lambda i: m.decode_step(cache, toks[i0 + i], B, T0 + i0 + i,
-                                                          next_tok=toks[i0 + i + 1]), args.steps, barrier)
+    n_prof = profiled_pass(L, m, lambda i: dstep(i0 + i), args.steps, barrier)   # (direct launches)
     kernels = kernel_table(L, m, n_prof, pk)
     flag = m.check_flag()
     # algorithmic bytes of one decode step: every weight once, the cache read up to the
@@ -572,7 +577,7 @@ def decode_workload(args):
                 "frac": achieved / pk["hbm"], "peak_kind": f"copy bandwidth ({pk['source']})",
                 "traffic": None, "bytes_per_step": wbytes + kvbytes}
     # end to end: this step's tokens from pinned host memory in, the next tokens out
-    tok_h = torch.from_numpy(toks[args.warmup].cpu().numpy().copy()).pin_memory()
+    tok_h = torch.from_numpy(buf[0].cpu().numpy().copy()).pin_memory()
     nxt_h = torch.zeros(B, dtype=torch.int32).pin_memory()
     t_in = torch.empty(B, dtype=torch.int32, device=dev)
     t_out = torch.empty(B, dtype=torch.int32, device=dev)
@@ -584,12 +589,13 @@ def decode_workload(args):
         stream.synchronize()
         tok_h.copy_(nxt_h)
 
-    base = T0 + args.warmup
+    base = T0 + args.warmup + 2 * args.steps    # (every position up to here has been written)
+    host_step(base)
     host_step(base)
     barrier()
     t0 = time.perf_counter()
     for i in range(args.steps):
-        host_step(base + i)
+        host_step(base + 1 + i)
     barrier()
     e2e_s = replicas.max_over_ranks((time.perf_counter() - t0) / args.steps, dist, dev)
     value = replicas.job_rate(world, B, ms * 1e-3)

@@ -199,6 +199,15 @@ NC_API int nc_decode_step(nc_model* m, void* cache, int cache_B, int cache_T, co
                           int pos, float* logits_out, int32_t* next_out);
 
 /*
+ * Decode steps as CUDA graphs (default on): the second nc_decode_step call with the
+ * same cache, B and token/logit/next-token buffers records the step once; later
+ * calls set the position and replay it, with results bit-identical to direct
+ * launches.  enable = 0 launches every kernel directly (as does every call while
+ * the profiler is on).  New weights need no re-recording.
+ */
+NC_API int nc_decode_graphs(nc_model* m, int enable);
+
+/*
  * Learning rates of optimizer step `step` (0-based) of an n_steps run (section
  * 预搜检: the rate scales as 1/sqrt(dim), and the multiplier lrm falls
  * linearly to 0 near the end of training).  Host arithmetic, no device work.

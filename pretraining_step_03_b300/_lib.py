@@ -45,6 +45,7 @@ SIGNATURES = {
     "nc_kv_cache_bytes": (_I, [_V, _I, _I, ctypes.POINTER(_SZ)]),
     "nc_prefill": (_I, [_V, _V, _I, _I, _V, _I, _I, _V, _V]),
     "nc_decode_step": (_I, [_V, _V, _I, _I, _V, _I, _I, _V, _V]),
+    "nc_decode_graphs": (_I, [_V, _I]),
     "nc_muon_step": (_I, [_V, _F, _F, _I, _I, ctypes.POINTER(_F)]),
     "nc_adamw_step": (_I, [_V, _F, _F, _F, _F, _F, _F, _I]),
     "nc_train_step": (_I, [_V, _V, _V, _V, _I, _I, _I, _F, _F, _I, ctypes.POINTER(_F), _F, _F, _F,
@@ -154,6 +155,10 @@ def nc_prefill(m, cache, cache_B, cache_T, tokens, B, T0, logits_out, next_out):
 
 def nc_decode_step(m, cache, cache_B, cache_T, tokens, B, pos, logits_out, next_out):
     _check(lib().nc_decode_step(m, cache, cache_B, cache_T, tokens, B, pos, logits_out, next_out))
+
+
+def nc_decode_graphs(m, enable):
+    _check(lib().nc_decode_graphs(m, enable))
 
 
 def nc_lr_schedule(step, n_steps, warmdown_frac, d_model, d_ref, base):

@@ -66,8 +66,10 @@ __global__ void rmsnorm_cols_kernel(const float* xt, T* y, int Bp, int d) {
 // c = [q | k | v]^T [3d][Bp] of position pos -> q [Bp][d] with RoPE, and k (with RoPE), v
 // appended to the cache at row (b, pos).  One thread per (b, head, rotation pair).
 template <typename T>
-__global__ void qkv_post_kernel(const T* c, int B, int Bp, int d, int H, int Dh, int pos, const float2* rope,
-                                int rope_ld, T* q, T* kc, T* vc, int cache_T) {
+__global__ void qkv_post_kernel(const T* c, int B, int Bp, int d, int H, int Dh, int pos_arg,
+                                const int* pos_dev, const float2* rope, int rope_ld, T* q, T* kc, T* vc,
+                                int cache_T) {
+    const int pos = pos_dev ? *pos_dev : pos_arg;   // (a replayed step reads its position)
     const int half = Dh / 2;
     const long idx = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long)Bp * H * half) return;
@@ -128,8 +130,12 @@ template <> struct Vec8<float> {
 
 template <typename T>
 __global__ void __launch_bounds__(DA_THREADS) decode_attn_kernel(const T* q, const T* kc, const T* vc, int d,
-                                                                 int cache_T, int n, int kchunk, float scale,
-                                                                 float* part_o, float2* part_ml) {
+                                                                 int cache_T, int n_arg, const int* pos_dev,
+                                                                 int kchunk, float scale, float* part_o,
+                                                                 float2* part_ml) {
+    // a replayed step reads its position; the grid then covers the whole cache and the
+    // chunks past the last key leave an empty partial (max -inf, sum 0)
+    const int n = pos_dev ? *pos_dev + 1 : n_arg;
     __shared__ float s_o[DA_GROUPS][DA_HD];
     __shared__ float s_m[DA_GROUPS], s_l[DA_GROUPS];
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, H = gridDim.y, nchunk = gridDim.x;
@@ -334,11 +340,11 @@ int decode_rmsnorm_cols(const float* xt, T* y, int Bp, int d, cudaStream_t s) {
 }
 
 template <typename T>
-int decode_qkv_post(const T* c, int B, int Bp, int d, int H, int Dh, int pos, const float2* rope, int rope_ld,
-                    T* q, T* kc, T* vc, int cache_T, cudaStream_t s) {
+int decode_qkv_post(const T* c, int B, int Bp, int d, int H, int Dh, int pos, const int* pos_dev,
+                    const float2* rope, int rope_ld, T* q, T* kc, T* vc, int cache_T, cudaStream_t s) {
     const long total = (long)Bp * H * (Dh / 2);
-    qkv_post_kernel<T><<<ceil_div(total, 256), 256, 0, s>>>(c, B, Bp, d, H, Dh, pos, rope, rope_ld, q, kc, vc,
-                                                           cache_T);
+    qkv_post_kernel<T><<<ceil_div(total, 256), 256, 0, s>>>(c, B, Bp, d, H, Dh, pos, pos_dev, rope, rope_ld, q,
+                                                           kc, vc, cache_T);
     note_launch();
     NC_LAUNCH_CHECK("decode_qkv_post");
     return NC_OK;
@@ -361,15 +367,17 @@ size_t decode_attention_ws_bytes(int B, int H, int n) {
 
 template <typename T>
 int decode_attention(const T* q, const T* kc, const T* vc, int B, int Bp, int d, int H, int Dh, int cache_T,
-                     int n, T* out, void* ws, size_t ws_bytes, cudaStream_t s) {
+                     int n, const int* pos_dev, T* out, void* ws, size_t ws_bytes, cudaStream_t s) {
     if (Dh != DA_HD) return set_error(NC_ERR_UNSUPPORTED, "decode attention: head dim %d (128 only)", Dh);
-    const int kch = decode_attention_chunks(B, H, n);
-    const int nchunk = ceil_div(n, kch);
+    // chunk boundaries from the cache length, so a replayed step (grid over the whole cache,
+    // the chunks past the last key empty) adds up exactly as a direct one
+    const int kch = decode_attention_chunks(B, H, cache_T);
+    const int nchunk = ceil_div(pos_dev ? cache_T : n, kch);
     const long parts = (long)B * H * nchunk;
-    if (decode_attention_ws_bytes(B, H, n) > ws_bytes) return set_error(NC_ERR_ARG, "decode attention workspace");
+    if (decode_attention_ws_bytes(B, H, cache_T) > ws_bytes) return set_error(NC_ERR_ARG, "decode attention workspace");
     float* po = reinterpret_cast<float*>(ws);
     float2* pml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) + (((size_t)parts * DA_HD * 4 + 255) & ~(size_t)255));
-    decode_attn_kernel<T><<<dim3(nchunk, H, B), DA_THREADS, 0, s>>>(q, kc, vc, d, cache_T, n, kch,
+    decode_attn_kernel<T><<<dim3(nchunk, H, B), DA_THREADS, 0, s>>>(q, kc, vc, d, cache_T, n, pos_dev, kch,
                                                                    1.0f / sqrtf((float)Dh), po, pml);
     decode_combine_kernel<T><<<dim3(H, Bp), DA_HD, 0, s>>>(po, pml, nchunk, B, d, out);
     note_launch(2);
@@ -414,14 +422,23 @@ int prefill_gather_last(const T* y, int B, int Bp, int T0, int d, T* out, cudaSt
     return NC_OK;
 }
 
+__global__ void set_int_kernel(int* p, int v) { *p = v; }
+
+int decode_set_pos(int* pos_dev, int pos, cudaStream_t s) {
+    set_int_kernel<<<1, 1, 0, s>>>(pos_dev, pos);
+    note_launch();
+    NC_LAUNCH_CHECK("decode_set_pos");
+    return NC_OK;
+}
+
 #define NC_DEC_INST(T)                                                                                       \
     template int decode_embed_t<T>(const int32_t*, const T*, float*, int, int, int, int, uint32_t*,         \
                                    cudaStream_t);                                                            \
     template int decode_rmsnorm_cols<T>(const float*, T*, int, int, cudaStream_t);                           \
-    template int decode_qkv_post<T>(const T*, int, int, int, int, int, int, const float2*, int, T*, T*, T*, \
-                                    int, cudaStream_t);                                                      \
-    template int decode_attention<T>(const T*, const T*, const T*, int, int, int, int, int, int, int, T*,   \
-                                     void*, size_t, cudaStream_t);                                           \
+    template int decode_qkv_post<T>(const T*, int, int, int, int, int, int, const int*, const float2*, int, \
+                                    T*, T*, T*, int, cudaStream_t);                                          \
+    template int decode_attention<T>(const T*, const T*, const T*, int, int, int, int, int, int, int,       \
+                                     const int*, T*, void*, size_t, cudaStream_t);                           \
     template int prefill_kv_store<T>(const T*, int, int, int, T*, T*, int, cudaStream_t);                    \
     template int prefill_gather_last<T>(const T*, int, int, int, int, T*, cudaStream_t);
 NC_DEC_INST(float)

@@ -82,6 +82,15 @@ struct nc_model {
     size_t ebws_bytes;
     void* splitk;
     size_t splitk_bytes;
+    // decode steps replayed as CUDA graphs, one per (cache, batch, token/output buffers)
+    struct DecGraph {
+        const void* cache; int cache_B, cache_T, B; const void* tok; const void* logits; const void* next;
+        int uses; cudaGraphExec_t exec; int kernels;
+    };
+    std::vector<DecGraph> dec_graphs;
+    bool dec_graph_on = true;
+    int* pos_dev = nullptr;
+    cudaStream_t cap_stream = nullptr;   // recording needs a stream of its own (not the legacy one)
     // measurement: CUDA event pairs around kernel classes
     struct ProfRec { cudaEvent_t a, b; int cat; double flops, bytes; };
     bool prof_on = false;
@@ -142,6 +151,7 @@ void layout(nc_model* m, char* base, size_t* total) {
     m->rope = (float2*)c.take((size_t)(m->maxT > 0 ? m->maxT : 1) * (m->Dh / 2) * 8);
     m->loss = (float*)c.take(128 * 4);
     m->flag = (uint32_t*)c.take(16);
+    m->pos_dev = (int*)c.take(16);
     const long M = m->maxM;
     m->L.assign(Ld, nc_model::Layer{});
     m->tok_stage = nullptr;
@@ -594,6 +604,8 @@ int nc_init_model(int depth, int d_model, int n_head, int vocab, uint64_t seed, 
 
 int nc_free(nc_model* m) {
     if (m) for (auto e : m->ev_pool) cudaEventDestroy(e);
+    if (m) for (auto& g : m->dec_graphs) if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (m && m->cap_stream) cudaStreamDestroy(m->cap_stream);
     delete m;
     return NC_OK;
 }
@@ -832,9 +844,11 @@ int prefill(nc_model* m, const Cache<T>& c, const int32_t* tok, int B, int T0, f
     return lm_head_rows<T>(m, m->dy, B, Bp, logits_out, next_out);
 }
 
+// pos_dev (a step recorded for replay): the position is read from device memory by the
+// kernels that need it, and pos is only its upper bound (cache_T - 1)
 template <typename T>
 int decode_step(nc_model* m, const Cache<T>& c, const int32_t* tok, int B, int pos, float* logits_out,
-                int32_t* next_out) {
+                int32_t* next_out, const int* pos_dev = nullptr) {
     const int d = m->d, H = m->H, Dh = m->Dh, F = m->F, V = m->V;
     const int Bp = round8(B), n = pos + 1, act = m->dtype;
     const double ab = m->dtype == NC_BF16 ? 2.0 : 4.0;
@@ -864,11 +878,12 @@ int decode_step(nc_model* m, const Cache<T>& c, const int32_t* tok, int B, int p
         NC_TRY(run_gemm(m, mk(m, 3 * d, Bp, d, W<T>(m, b0), d, false, y, d, false, cq, Bp, act)));
         {
             Prof pr(m, NC_PROF_ROPE, 0, (double)Bp * 3 * d * ab * 2);
-            NC_TRY(decode_qkv_post<T>(cq, B, Bp, d, H, Dh, pos, m->rope, rope_ld, q, c.k(l), c.v(l), c.T_, s));
+            NC_TRY(decode_qkv_post<T>(cq, B, Bp, d, H, Dh, pos, pos_dev, m->rope, rope_ld, q, c.k(l), c.v(l), c.T_,
+                                      s));
         }
         {
             Prof pr(m, NC_PROF_ATTN_FWD, 4.0 * B * H * Dh * n, 2.0 * B * n * d * ab);
-            NC_TRY(decode_attention<T>(q, c.k(l), c.v(l), B, Bp, d, H, Dh, c.T_, n, att, ws, ws_bytes, s));
+            NC_TRY(decode_attention<T>(q, c.k(l), c.v(l), B, Bp, d, H, Dh, c.T_, n, pos_dev, att, ws, ws_bytes, s));
         }
         {   // x^T += Wo att^T
             Gemm g = mk(m, d, Bp, d, W<T>(m, b0 + 3), d, false, att, d, false, xt, Bp, NC_FP32);
@@ -936,15 +951,68 @@ int nc_decode_step(nc_model* m, void* cache, int cache_B, int cache_T, const int
     NC_TRY(check_cache(m, cache, cache_B, cache_T, B));
     if (!tokens) return set_error(NC_ERR_ARG, "null tokens");
     if (pos < 0 || pos >= cache_T) return set_error(NC_ERR_ARG, "pos %d outside [0, cache_T = %d)", pos, cache_T);
-    if (decode_attention_ws_bytes(B, m->H, pos + 1) > (size_t)m->maxM * 3 * m->d * (m->dtype == NC_BF16 ? 2 : 4))
+    if (decode_attention_ws_bytes(B, m->H, cache_T) > (size_t)m->maxM * 3 * m->d * (m->dtype == NC_BF16 ? 2 : 4))
         return set_error(NC_ERR_ARG, "decode workspace too small for B = %d", B);
     g_gemm_flag = m->flag;
     g_attn_flag = m->flag;
-    if (m->dtype == NC_BF16)
-        return decode_step<bf16>(m, Cache<bf16>{(bf16*)cache, cache_B, cache_T, m->d}, tokens, B, pos, logits_out,
-                                 next_out);
-    return decode_step<float>(m, Cache<float>{(float*)cache, cache_B, cache_T, m->d}, tokens, B, pos, logits_out,
-                              next_out);
+    auto run = [&](int p, const int* pd) {
+        if (m->dtype == NC_BF16)
+            return decode_step<bf16>(m, Cache<bf16>{(bf16*)cache, cache_B, cache_T, m->d}, tokens, B, p, logits_out,
+                                     next_out, pd);
+        return decode_step<float>(m, Cache<float>{(float*)cache, cache_B, cache_T, m->d}, tokens, B, p,
+                                  logits_out, next_out, pd);
+    };
+    if (!m->dec_graph_on || m->prof_on) return run(pos, nullptr);
+    // The second call with the same buffers records the step (the position read from device
+    // memory, the attention grid sized for the whole cache) as a CUDA graph; later calls set
+    // the position and replay it: ~13 launches per layer become one.
+    nc_model::DecGraph* gr = nullptr;
+    for (auto& g : m->dec_graphs)
+        if (g.cache == cache && g.cache_B == cache_B && g.cache_T == cache_T && g.B == B && g.tok == tokens &&
+            g.logits == logits_out && g.next == next_out)
+            gr = &g;
+    if (!gr) {
+        if (m->dec_graphs.size() >= 8) {
+            if (m->dec_graphs.front().exec) cudaGraphExecDestroy(m->dec_graphs.front().exec);
+            m->dec_graphs.erase(m->dec_graphs.begin());
+        }
+        m->dec_graphs.push_back({cache, cache_B, cache_T, B, tokens, logits_out, next_out, 0, nullptr, 0});
+        gr = &m->dec_graphs.back();
+    }
+    if (gr->exec == nullptr && gr->uses++ == 0) return run(pos, nullptr);   // the first call runs directly
+    if (gr->exec == nullptr) {
+        if (!m->cap_stream)
+            NC_TRY(cuda_check(cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking), "capture stream"));
+        cudaStream_t s = m->cap_stream, user = m->stream;
+        NC_TRY(cuda_check(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal), "decode capture"));
+        const uint64_t l0 = nc_launch_count();
+        m->stream = s;   // the step's launches go to the recording stream
+        const int rc = run(cache_T - 1, m->pos_dev);
+        m->stream = user;
+        cudaGraph_t graph = nullptr;
+        const cudaError_t e = cudaStreamEndCapture(s, &graph);
+        const int k = (int)(nc_launch_count() - l0);
+        note_launch(-k);   // recorded, not launched
+        if (rc != NC_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            return rc;
+        }
+        NC_TRY(cuda_check(e, "decode capture end"));
+        const cudaError_t e2 = cudaGraphInstantiate(&gr->exec, graph, 0);
+        cudaGraphDestroy(graph);
+        NC_TRY(cuda_check(e2, "decode graph instantiate"));
+        gr->kernels = k;
+    }
+    NC_TRY(decode_set_pos(m->pos_dev, pos, m->stream));
+    NC_TRY(cuda_check(cudaGraphLaunch(gr->exec, m->stream), "decode graph launch"));
+    note_launch(gr->kernels);
+    return NC_OK;
+}
+
+int nc_decode_graphs(nc_model* m, int enable) {
+    if (!m) return set_error(NC_ERR_ARG, "null model");
+    m->dec_graph_on = enable != 0;
+    return NC_OK;
 }
 
 int nc_lr_schedule(int step, int n_steps, float warmdown_frac, int d_model, int d_ref, const float base[3],

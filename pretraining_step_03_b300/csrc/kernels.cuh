@@ -86,16 +86,20 @@ int decode_embed_t(const int32_t* tok, const T* wte, float* xt, int B, int Bp, i
                    cudaStream_t s);
 template <typename T>
 int decode_rmsnorm_cols(const float* xt, T* y, int Bp, int d, cudaStream_t s);
-// [q|k|v]^T [3d][Bp] at position pos -> q [Bp][d] (RoPE), cache rows (b, pos) of k (RoPE) and v
+// [q|k|v]^T [3d][Bp] at position pos -> q [Bp][d] (RoPE), cache rows (b, pos) of k (RoPE) and v.
+// pos_dev (optional): the position is read from device memory instead (a replayed graph).
 template <typename T>
-int decode_qkv_post(const T* c, int B, int Bp, int d, int H, int Dh, int pos, const float2* rope, int rope_ld,
-                    T* q, T* kc, T* vc, int cache_T, cudaStream_t s);
+int decode_qkv_post(const T* c, int B, int Bp, int d, int H, int Dh, int pos, const int* pos_dev,
+                    const float2* rope, int rope_ld, T* q, T* kc, T* vc, int cache_T, cudaStream_t s);
 // out [Bp][d] = softmax(q k^T / sqrt(Dh)) v over cache rows 0 .. n-1 of each of the B sequences
-// (rows B .. Bp-1 of out are zeroed); head dim 128
+// (rows B .. Bp-1 of out are zeroed); head dim 128.  Key chunks are sized from cache_T, so the
+// sums do not depend on n's grid.  pos_dev (optional): n = *pos_dev + 1 at run time, the grid
+// covering the whole cache.
 size_t decode_attention_ws_bytes(int B, int H, int n);
 template <typename T>
 int decode_attention(const T* q, const T* kc, const T* vc, int B, int Bp, int d, int H, int Dh, int cache_T,
-                     int n, T* out, void* ws, size_t ws_bytes, cudaStream_t s);
+                     int n, const int* pos_dev, T* out, void* ws, size_t ws_bytes, cudaStream_t s);
+int decode_set_pos(int* pos_dev, int pos, cudaStream_t s);
 // next[b] = argmax_v logits^T[v][b] (lowest id on ties); ws >= B * 512 bytes
 int decode_argmax(const float* lt, int V, int B, int Bp, int32_t* next, void* ws, size_t ws_bytes, uint32_t* flag,
                   cudaStream_t s);

@@ -107,15 +107,22 @@ class Model:
 
     def generate(self, cache, prompt, n_new):
         """Greedy continuation of B equal-length prompts (device int32 [B, T0]) by n_new
-        tokens; returns the device int32 [n_new, B] tokens (step-major: each step's
-        tokens are the next step's input, in place)."""
+        tokens; returns the device int32 [n_new, B] tokens (step-major).  The steps take
+        their input from and write their output to two fixed buffers in turn, so from the
+        third token on each step is a replay of a recorded graph."""
         torch = self.torch
         B, T0 = prompt.shape
         out = torch.empty(n_new, B, dtype=torch.int32, device=self.device)
-        self.prefill(cache, prompt.reshape(-1).contiguous(), B, T0, next_tok=out[0])
+        buf = [torch.empty(B, dtype=torch.int32, device=self.device) for _ in range(2)]
+        self.prefill(cache, prompt.reshape(-1).contiguous(), B, T0, next_tok=buf[0])
+        out[0].copy_(buf[0])
         for i in range(1, n_new):
-            self.decode_step(cache, out[i - 1], B, T0 + i - 1, next_tok=out[i])
+            self.decode_step(cache, buf[(i - 1) % 2], B, T0 + i - 1, next_tok=buf[i % 2])
+            out[i].copy_(buf[i % 2])
         return out
+
+    def decode_graphs(self, enable):
+        L.nc_decode_graphs(self.h, int(enable))
 
     def muon_step(self, lr, momentum=0.95, nesterov=True, ns_steps=5, coefs=NS_COEFS):
         L.nc_muon_step(self.h, lr, momentum, int(nesterov), ns_steps, coefs)

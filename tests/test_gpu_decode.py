@@ -145,3 +145,33 @@ def test_d20_full_size_identical_prompts():
     for i in range(n_new):
         assert_close(z_gpu[0, i], z_ref[0, i], 0.999, 2e-2, f"d20 step {i} logits")
     _check_tokens(tok[:1], z_gpu[:1], z_ref, 2e-2)
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16"])
+def test_replayed_steps_equal_direct_launches(mode):
+    """Decode steps replayed from a recorded CUDA graph give the same bits as direct
+    launches (two fixed token buffers in turn; 10 steps, so 8 are replays)."""
+    import torch
+    from pretraining_step_03_b300.model import Model
+    depth, d, H, V, B, T0, steps = 2, 256, 2, 512, 3, 9, 10
+    params = [p * 4.0 for p in synth.init_params(depth, d, H, V, seed=0)]
+    prompt = np.random.default_rng(8).integers(0, V, (B, T0))
+    results = []
+    for graphs in (True, False):
+        m = Model(depth, d, H, V, 4, 64, dtype=mode)
+        m.set_params(params)
+        m.decode_graphs(graphs)
+        cache = m.kv_cache(4, 64)
+        buf = [torch.zeros(B, dtype=torch.int32, device=m.device) for _ in range(2)]
+        logits = torch.zeros(B, V, dtype=torch.float32, device=m.device)
+        m.prefill(cache, m.device_i32(prompt), B, T0, next_tok=buf[0])
+        seen = []
+        for i in range(steps):
+            m.decode_step(cache, buf[i % 2], B, T0 + i, logits=logits, next_tok=buf[(i + 1) % 2])
+            seen.append((logits.cpu().numpy().copy(), buf[(i + 1) % 2].cpu().numpy().copy()))
+        assert m.check_flag() == 0
+        results.append(seen)
+        m.close()
+    for i, ((za, ta), (zb, tb)) in enumerate(zip(*results)):
+        assert np.array_equal(za, zb), f"{mode} step {i}: logits differ"
+        assert np.array_equal(ta, tb), f"{mode} step {i}: tokens differ"
