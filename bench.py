@@ -71,7 +71,7 @@ ROOF = {"gemm": "tensor", "attn_fwd": "tensor", "attn_bwd": "tensor", "muon_ns":
 # dram read+write bytes per launch site of the dominant kernel class (the step's
 # GEMMs, each with its split-K reduce when it has one) from the last ncu capture
 # of the current GEMM code (profiles/d20_step_launches.md), None when not measured.
-GEMM_TRAFFIC_PER_LAUNCH = 1.220e9
+GEMM_TRAFFIC_PER_LAUNCH = 1.286e9
 CPU_SAMPLE_T = 256
 
 
