@@ -7,7 +7,9 @@
  * per byte; full backward; Muon (Newton-Schulz orthogonalised momentum) for
  * the 2-D block matrices and AdamW for the embedding and unembedding.  The
  * section 该你了 (depth scaling) adds gradient accumulation when the device
- * batch is smaller than the optimizer batch.
+ * batch is smaller than the optimizer batch.  Around the step: an evaluation
+ * pass (loss and bits per byte, no backward), the run's learning-rate
+ * schedule, and inference with a KV cache (prefill and greedy decode).
  *
  * Conventions for every entry point:
  *  - Every function returns an int status: NC_OK (0) or one of NC_ERR_*.
@@ -18,9 +20,13 @@
  *    pointers are ordinary (or pinned) host memory owned by the caller.
  *  - Calls on a model enqueue work on the model's stream and return without
  *    waiting, unless the comment says the call synchronises.
- *  - The library allocates no device memory: the caller passes one arena
- *    (e.g. a torch uint8 tensor) of nc_arena_bytes() bytes and the library
- *    lays every parameter, optimizer state and activation out inside it.
+ *  - The library allocates no device memory for data: the caller passes one
+ *    arena (e.g. a torch uint8 tensor) of nc_arena_bytes() bytes and the
+ *    library lays every parameter, optimizer state and activation out inside
+ *    it (a KV cache is a second caller-owned buffer).  The one exception is
+ *    the CUDA graphs (and their recording stream) that nc_decode_step keeps,
+ *    which the CUDA runtime backs with its own memory; nc_decode_graphs(m, 0)
+ *    turns them off.
  *  - Conditions found on the device (a token id >= vocab, a non-finite loss,
  *    a bounded wait that ran out) set bits of a device flag word instead of
  *    trapping; nc_check_device_flag() reads and clears it.
