@@ -29,7 +29,9 @@
  *    turns them off.
  *  - Conditions found on the device (a token id >= vocab, a non-finite loss,
  *    a bounded wait that ran out) set bits of a device flag word instead of
- *    trapping; nc_check_device_flag() reads and clears it.
+ *    trapping; nc_check_device_flag() reads and clears a model's word, and
+ *    nc_check_kernel_flag() the per-device word of the kernel-level entry
+ *    points (attention, GEMM), which belong to no model.
  */
 #ifndef NC_API_H
 #define NC_API_H
@@ -248,6 +250,14 @@ NC_API int nc_check_device_flag(nc_model* m, uint32_t* flags);
 /* ------------------------------------------------------------------ */
 /* Kernel-level entry points (the same kernels the step runs).         */
 /* ------------------------------------------------------------------ */
+
+/* Reads and clears the flag word (NC_FLAG_*) that the kernels of the
+ * kernel-level entry points below set on the current device (one word per
+ * device in the library's own memory; a kernel that gave up a bounded wait,
+ * or found its shared memory misaligned, leaves its outputs unwritten and
+ * sets a bit here).  Synchronises `stream`, which should be the stream the
+ * calls were made on.  Returns NC_ERR_DEVICE_FLAG when any bit was set. */
+NC_API int nc_check_kernel_flag(void* stream, uint32_t* flags);
 
 /*
  * Causal multi-head attention forward (section 预搜检: 10 heads of dim 128):

@@ -57,6 +57,7 @@ SIGNATURES = {
     "nc_get_state": (_I, [_V, _I, _I, _V, _SZ]),
     "nc_set_state": (_I, [_V, _I, _I, _V, _SZ]),
     "nc_check_device_flag": (_I, [_V, ctypes.POINTER(ctypes.c_uint32)]),
+    "nc_check_kernel_flag": (_I, [_V, ctypes.POINTER(ctypes.c_uint32)]),
     "nc_attention_forward": (_I, [_V, _V, _V, _I, _V, _I, _V, _I, _I, _I, _I, _I, _V]),
     "nc_attention_workspace_bytes": (_SZ, [_I, _I, _I]),
     "nc_attention_backward": (_I, [_V, _V, _V, _I, _V, _V, _I, _V, _V, _V, _V, _I, _V, _I, _I, _I,
@@ -217,6 +218,15 @@ def nc_check_device_flag(m):
     """Returns the flag bits (0 when clean); never raises for a set flag."""
     f = ctypes.c_uint32(0)
     rc = lib().nc_check_device_flag(m, ctypes.byref(f))
+    if rc not in (NC_OK, NC_ERR_DEVICE_FLAG):
+        _check(rc)
+    return f.value
+
+
+def nc_check_kernel_flag(stream):
+    """Flag bits of the kernel-level entry points on the current device (0 when clean)."""
+    f = ctypes.c_uint32(0)
+    rc = lib().nc_check_kernel_flag(stream, ctypes.byref(f))
     if rc not in (NC_OK, NC_ERR_DEVICE_FLAG):
         _check(rc)
     return f.value

@@ -68,12 +68,14 @@ extern "C" int nc_attention_backward_noalloc(const void* q, const void* k, const
     if (dtype != NC_BF16 && dtype != NC_FP32) return set_error(NC_ERR_ARG, "dtype %d", dtype);
     float* delta = nullptr;
     NC_TRY(scratch_address(&delta));
+    uint32_t* flag = nullptr;
+    NC_TRY(kernel_flag(&flag));
     cudaStream_t s = (cudaStream_t)stream;
     if (dtype == NC_BF16)
         return attention_backward<bf16>((const bf16*)q, (const bf16*)k, (const bf16*)v, ld_qkv,
                                         (const bf16*)o, (const bf16*)dout, ld_o, lse, (bf16*)dq,
-                                        (bf16*)dk, (bf16*)dv, ld_dqkv, delta, B, T, H, D, s);
+                                        (bf16*)dk, (bf16*)dv, ld_dqkv, delta, B, T, H, D, s, flag);
     return attention_backward<float>((const float*)q, (const float*)k, (const float*)v, ld_qkv,
                                      (const float*)o, (const float*)dout, ld_o, lse, (float*)dq,
-                                     (float*)dk, (float*)dv, ld_dqkv, delta, B, T, H, D, s);
+                                     (float*)dk, (float*)dv, ld_dqkv, delta, B, T, H, D, s, flag);
 }

@@ -905,8 +905,6 @@ int maps(CUtensorMap* m, const void* ptr, long rows, long ld, int H) {
 
 }  // namespace
 
-uint32_t* g_attn_flag = nullptr;
-
 // Grids are (blocks of a sequence, batch x heads): the x index runs fastest, so the
 // CTAs of one batch-head are resident together and share its K/V (forward, dQ) or
 // Q/dO (dK/dV) tiles through L2 instead of re-reading them from HBM.
@@ -921,13 +919,10 @@ bool attention_tc_supported(long ld, long ldo, long ldd, const void* q, const vo
 }
 
 int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, bf16* o, long ldo,
-                         float* lse, int B, int T, int H, cudaStream_t s) {
+                         float* lse, int B, int T, int H, cudaStream_t s, uint32_t* flag) {
     if ((long)B * H > MAX_GRID_Y) return set_error(NC_ERR_UNSUPPORTED, "attention: B*H = %ld > %ld", (long)B * H, MAX_GRID_Y);
-    static bool init = false;
-    if (!init) {
-        NC_TRY(set_smem(attn_fwd_kernel, smem_bytes(FWD_TILES)));
-        init = true;
-    }
+    static DeviceOnce init;
+    NC_TRY(init.run([] { return set_smem(attn_fwd_kernel, smem_bytes(FWD_TILES)); }));
     CUtensorMap mq, mk, mv;
     const long rows = (long)B * T;
     NC_TRY(maps(&mq, q, rows, ld, H));
@@ -935,7 +930,7 @@ int attention_forward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, b
     NC_TRY(maps(&mv, v, rows, ld, H));
     AttnParams p{};
     p.T = T; p.H = H; p.nblk = ceil_div(T, BR); p.ldo = ldo; p.o = o; p.lse = lse;
-    p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
+    p.scale = 1.0f / sqrtf((float)HD); p.flag = flag;
     attn_fwd_kernel<<<dim3((p.nblk + 1) / 2, H * B), NT, smem_bytes(FWD_TILES), s>>>(mq, mk, mv, p);
     note_launch();
     NC_LAUNCH_CHECK("attn_fwd_kernel");
@@ -951,15 +946,14 @@ size_t attention_tc_ds_bytes(int B, int T, int H) {
 int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, const bf16* dout,
                           long ldo, const float* lse, const float* delta, bf16* dq, bf16* dk, bf16* dv,
                           long ldd, int B, int T, int H, const float2* rope, int rope_ld, bf16* ds,
-                          cudaStream_t s) {
+                          cudaStream_t s, uint32_t* flag) {
     if ((long)B * H > MAX_GRID_Y) return set_error(NC_ERR_UNSUPPORTED, "attention: B*H = %ld > %ld", (long)B * H, MAX_GRID_Y);
-    static bool init = false;
-    if (!init) {
+    static DeviceOnce init;
+    NC_TRY(init.run([] {
         NC_TRY(set_smem(attn_dq_kernel, smem_bytes(DQ_TILES)));
         NC_TRY(set_smem(attn_dkdv_kernel, smem_bytes(DKV_TILES)));
-        NC_TRY(set_smem(attn_dq_ds_kernel, smem_bytes(DQS_ST)));
-        init = true;
-    }
+        return set_smem(attn_dq_ds_kernel, smem_bytes(DQS_ST));
+    }));
     if ((uintptr_t)ds % 16) ds = nullptr;
     CUtensorMap mq, mk, mv, mdo;
     const long rows = (long)B * T;
@@ -971,7 +965,7 @@ int attention_backward_tc(const bf16* q, const bf16* k, const bf16* v, long ld, 
     p.T = T; p.H = H; p.nblk = ceil_div(T, BR); p.ldo = ldo; p.ldd = ldd;
     p.lse = const_cast<float*>(lse); p.delta = delta; p.dq = dq; p.dk = dk; p.dv = dv; p.rope = rope;
     p.rope_ld = rope_ld;
-    p.scale = 1.0f / sqrtf((float)HD); p.flag = g_attn_flag;
+    p.scale = 1.0f / sqrtf((float)HD); p.flag = flag;
     p.ds = ds; p.ds_bh = (long)p.nblk * (p.nblk + 1) / 2;
     attn_dkdv_kernel<<<dim3(p.nblk, H * B), DKV_NT, smem_bytes(DKV_TILES), s>>>(mq, mk, mv, mdo, p);
     if (ds) {

@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <atomic>
+
 #include "../../include/nc_api.h"
 
 typedef __nv_bfloat16 bf16;
@@ -48,5 +50,32 @@ int cuda_check(cudaError_t e, const char* what);
 #define NC_LAUNCH_CHECK(what) NC_TRY(::nc::cuda_check(cudaGetLastError(), what))
 
 inline int ceil_div(long a, long b) { return (int)((a + b - 1) / b); }
+
+// Runs a set-up once per device ordinal.  Kernel attributes (the dynamic
+// shared-memory limit) are kept per device, so a process-wide "done" switch
+// would skip the set-up on a second GPU.  Threads that race may both run it,
+// so the set-up must be idempotent (setting an attribute is).
+class DeviceOnce {
+  public:
+    template <typename F>
+    int run(F&& setup) {
+        int dev = 0;
+        NC_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
+        const uint64_t bit = dev >= 0 && dev < 64 ? 1ull << dev : 0;
+        if (bit && (done_.load(std::memory_order_acquire) & bit)) return NC_OK;
+        NC_TRY(setup());
+        if (bit) done_.fetch_or(bit, std::memory_order_acq_rel);
+        return NC_OK;
+    }
+
+  private:
+    std::atomic<uint64_t> done_{0};
+};
+
+// Device flag word for kernels launched by the kernel-level entry points,
+// which have no model (and so no model flag): a word in the library's own
+// device memory of the current device, read and cleared by
+// nc_check_kernel_flag.  Looked up once per device.
+int kernel_flag(uint32_t** out);
 
 }  // namespace nc

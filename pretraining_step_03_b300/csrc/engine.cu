@@ -19,11 +19,6 @@
 
 #include "kernels.cuh"
 
-namespace nc {
-extern uint32_t* g_gemm_flag;
-extern uint32_t* g_attn_flag;
-}
-
 using namespace nc;
 
 struct nc_model {
@@ -253,6 +248,7 @@ Gemm mk(nc_model* m, int M, int N, int K, const void* A, long lda, bool a_t, con
     g.B = B; g.ldb = ldb; g.b_t = b_t;
     g.in_dtype = m->dtype;
     g.C = C; g.ldc = ldc; g.c_dtype = c_dtype;
+    g.flag = m->flag;
     return g;
 }
 
@@ -317,7 +313,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         T* q = (T*)Ly.qkv;
         {
             Prof pr(m, NC_PROF_ATTN_FWD, attn_fl, 0);
-            NC_TRY(attention_forward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, d, Ly.lse, B, T_, H, Dh, s));
+            NC_TRY(attention_forward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, d, Ly.lse, B, T_, H, Dh, s, m->flag));
         }
         {   // x += o Wo^T
             Gemm g = mk(m, M, d, d, Ly.o, d, false, W<T>(m, b0 + 3), d, false, m->x, d, NC_FP32);
@@ -392,7 +388,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         {
             Prof pr(m, NC_PROF_ATTN_BWD, 2.5 * attn_fl, 0);
             NC_TRY(attention_backward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, (T*)m->dO, d, Ly.lse, dq,
-                                         dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s, m->rope,
+                                         dq + d, dq + 2 * d, 3 * d, m->delta, B, T_, H, Dh, s, m->flag, m->rope,
                                          rope_ld, &unroped, fuse_rope,
                                          attention_ds_bytes(B, T_, H, Dh) <= m->ds_bytes ? m->ds : nullptr));
         }
@@ -664,8 +660,6 @@ int nc_forward_backward(nc_model* m, const int32_t* tokens, const int32_t* targe
         return set_error(NC_ERR_ARG, "B=%d T=%d exceeds the arena's max_B*max_T=%ld / max_T=%d", B, T,
                          m->maxM, m->maxT);
     if (accumulate != 0 && accumulate != 1) return set_error(NC_ERR_ARG, "accumulate must be 0 or 1");
-    g_gemm_flag = m->flag;
-    g_attn_flag = m->flag;
     if (m->dtype == NC_BF16)
         return forward_backward<bf16>(m, tokens, targets, token_bytes, B, T, accumulate, grad_scale, loss_bpb_out);
     return forward_backward<float>(m, tokens, targets, token_bytes, B, T, accumulate, grad_scale, loss_bpb_out);
@@ -679,8 +673,6 @@ int nc_eval_loss(nc_model* m, const int32_t* tokens, const int32_t* targets, con
         return set_error(NC_ERR_ARG, "B=%d T=%d exceeds the arena's max_B*max_T=%ld / max_T=%d", B, T,
                          m->maxM, m->maxT);
     if (accumulate != 0 && accumulate != 1) return set_error(NC_ERR_ARG, "accumulate must be 0 or 1");
-    g_gemm_flag = m->flag;
-    g_attn_flag = m->flag;
     if (m->dtype == NC_BF16)
         return forward_backward<bf16>(m, tokens, targets, token_bytes, B, T, 0, 1.f, loss_bpb_out, false,
                                       sums, accumulate);
@@ -691,7 +683,6 @@ int nc_eval_loss(nc_model* m, const int32_t* tokens, const int32_t* targets, con
 int nc_muon_step(nc_model* m, float lr, float momentum, int nesterov, int ns_steps, const float ns_coef[3]) {
     if (!m || !ns_coef) return set_error(NC_ERR_ARG, "null argument");
     if (ns_steps < 0 || ns_steps > 100) return set_error(NC_ERR_ARG, "ns_steps %d", ns_steps);
-    g_gemm_flag = m->flag;
     if (m->dtype == NC_BF16) return muon<bf16>(m, lr, momentum, nesterov, ns_steps, ns_coef);
     return muon<float>(m, lr, momentum, nesterov, ns_steps, ns_coef);
 }
@@ -814,7 +805,7 @@ int prefill(nc_model* m, const Cache<T>& c, const int32_t* tok, int B, int T0, f
         }
         {
             Prof pr(m, NC_PROF_ATTN_FWD, 4.0 * B * H * Dh * (0.5 * T0 * (T0 + 1.0)), 0);
-            NC_TRY(attention_forward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, d, Ly.lse, B, T0, H, Dh, s));
+            NC_TRY(attention_forward<T>(q, q + d, q + 2 * d, 3 * d, (T*)Ly.o, d, Ly.lse, B, T0, H, Dh, s, m->flag));
         }
         {
             Gemm g = mk(m, M, d, d, Ly.o, d, false, W<T>(m, b0 + 3), d, false, m->x, d, NC_FP32);
@@ -938,8 +929,6 @@ int nc_prefill(nc_model* m, void* cache, int cache_B, int cache_T, const int32_t
     if (!tokens) return set_error(NC_ERR_ARG, "null tokens");
     if (T0 < 1 || T0 > cache_T || (long)B * T0 > m->maxM)
         return set_error(NC_ERR_ARG, "T0 = %d: needs 1 <= T0 <= cache_T and B*T0 <= max_B*max_T", T0);
-    g_gemm_flag = m->flag;
-    g_attn_flag = m->flag;
     if (m->dtype == NC_BF16)
         return prefill<bf16>(m, Cache<bf16>{(bf16*)cache, cache_B, cache_T, m->d}, tokens, B, T0, logits_out, next_out);
     return prefill<float>(m, Cache<float>{(float*)cache, cache_B, cache_T, m->d}, tokens, B, T0, logits_out,
@@ -953,8 +942,6 @@ int nc_decode_step(nc_model* m, void* cache, int cache_B, int cache_T, const int
     if (pos < 0 || pos >= cache_T) return set_error(NC_ERR_ARG, "pos %d outside [0, cache_T = %d)", pos, cache_T);
     if (decode_attention_ws_bytes(B, m->H, cache_T) > (size_t)m->maxM * 3 * m->d * (m->dtype == NC_BF16 ? 2 : 4))
         return set_error(NC_ERR_ARG, "decode workspace too small for B = %d", B);
-    g_gemm_flag = m->flag;
-    g_attn_flag = m->flag;
     auto run = [&](int p, const int* pd) {
         if (m->dtype == NC_BF16)
             return decode_step<bf16>(m, Cache<bf16>{(bf16*)cache, cache_B, cache_T, m->d}, tokens, B, p, logits_out,
@@ -1102,12 +1089,14 @@ int nc_attention_forward(const void* q, const void* k, const void* v, int ld_qkv
     if (B < 0 || T < 0 || H < 1 || D < 2 || D > 128 || D % 2 || ld_qkv < H * D || ld_o < H * D)
         return set_error(NC_ERR_ARG, "bad attention shape");
     cudaStream_t s = (cudaStream_t)stream;
+    uint32_t* flag = nullptr;
+    NC_TRY(kernel_flag(&flag));
     if (dtype == NC_BF16)
         return attention_forward<bf16>((const bf16*)q, (const bf16*)k, (const bf16*)v, ld_qkv, (bf16*)o,
-                                       ld_o, lse, B, T, H, D, s);
+                                       ld_o, lse, B, T, H, D, s, flag);
     if (dtype == NC_FP32)
         return attention_forward<float>((const float*)q, (const float*)k, (const float*)v, ld_qkv,
-                                        (float*)o, ld_o, lse, B, T, H, D, s);
+                                        (float*)o, ld_o, lse, B, T, H, D, s, flag);
     return set_error(NC_ERR_ARG, "dtype %d", dtype);
 }
 
@@ -1127,17 +1116,19 @@ int nc_attention_backward(const void* q, const void* k, const void* v, int ld_qk
         ld_dqkv < H * D)
         return set_error(NC_ERR_ARG, "bad attention shape");
     cudaStream_t s = (cudaStream_t)stream;
+    uint32_t* flag = nullptr;
+    NC_TRY(kernel_flag(&flag));
     if (dtype == NC_BF16)
         return attention_backward<bf16>((const bf16*)q, (const bf16*)k, (const bf16*)v, ld_qkv,
                                         (const bf16*)o, (const bf16*)dout, ld_o, lse, (bf16*)dq,
                                         (bf16*)dk, (bf16*)dv, ld_dqkv, (float*)workspace, B, T, H, D, s,
-                                        nullptr, 0, nullptr, false,
+                                        flag, nullptr, 0, nullptr, false,
                                         (char*)workspace + al((size_t)B * T * H * 4));
     if (dtype == NC_FP32)
         return attention_backward<float>((const float*)q, (const float*)k, (const float*)v, ld_qkv,
                                          (const float*)o, (const float*)dout, ld_o, lse, (float*)dq,
                                          (float*)dk, (float*)dv, ld_dqkv, (float*)workspace, B, T, H, D,
-                                         s);
+                                         s, flag);
     return set_error(NC_ERR_ARG, "dtype %d", dtype);
 }
 
@@ -1160,7 +1151,7 @@ int nc_gemm_bf16(int M, int N, int K, int batch, const void* A, long lda, long s
     if (beta != 0.f) { g.aux = C; g.ldaux = ldc; g.sAux = stride_c; g.aux_dtype = c_dtype; }
     if (!gemm_tc_supported(g))
         return set_error(NC_ERR_UNSUPPORTED, "operands must be 16-byte aligned with leading dims % 8 == 0");
-    g_gemm_flag = nullptr;
+    NC_TRY(kernel_flag(&g.flag));
     return gemm_tc(g, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 

@@ -1015,13 +1015,12 @@ template <int BN, bool A_MN, bool B_MN>
 int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, const TcParams& p,
            cudaStream_t s) {
     using C = Cfg<BN>;
-    static bool attr = false;
-    if (!attr) {
-        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>,
+    static DeviceOnce attr;
+    NC_TRY(attr.run([] {
+        return cuda_check(cudaFuncSetAttribute(gemm_tc_kernel<BN, A_MN, B_MN>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM),
-                          "gemm_tc smem attribute"));
-        attr = true;
-    }
+                          "gemm_tc smem attribute");
+    }));
     const long grid = p.units < num_sms() ? p.units : num_sms();
     gemm_tc_kernel<BN, A_MN, B_MN><<<(int)grid, NTHREADS, C::SMEM, s>>>(ma, mb, mx, p);
     note_launch();
@@ -1032,13 +1031,12 @@ int launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, 
 template <bool A_MN, bool B_MN, bool SYM = false, int EF = EF_GEN>
 int launch2(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mx, const TcParams& p,
             cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        NC_TRY(cuda_check(cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN, SYM, EF>,
+    static DeviceOnce attr;
+    NC_TRY(attr.run([] {
+        return cuda_check(cudaFuncSetAttribute(gemm_tc2_kernel<A_MN, B_MN, SYM, EF>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM),
-                          "gemm_tc2 smem attribute"));
-        attr = true;
-    }
+                          "gemm_tc2 smem attribute");
+    }));
     long clusters = p.units < num_sms() / 2 ? p.units : num_sms() / 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
@@ -1166,8 +1164,6 @@ int num_sms() {
 }
 
 
-uint32_t* g_gemm_flag = nullptr;  // device flag word of the current model (set by the engine)
-
 bool gemm_tc_supported(const Gemm& g) {
     if (g.in_dtype != NC_BF16) return false;
     if (g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
@@ -1226,7 +1222,7 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     p.aux = g.aux; p.ldaux = g.ldaux; p.sAux = g.sAux; p.aux_dtype = g.aux_dtype;
     p.alpha = g.alpha; p.beta = g.beta; p.epi = g.epi;
     p.ws = p.splits > 1 ? reinterpret_cast<float*>(ws) : nullptr;
-    p.flag = g_gemm_flag;
+    p.flag = g.flag;
     p.rope = g.rope; p.rope_T = g.rope_T; p.rope_cols = g.rope_cols; p.rope_ld = g.rope_ld; p.delta = g.delta;
     p.lse_part = g.lse_part;
 

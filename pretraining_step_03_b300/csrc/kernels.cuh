@@ -38,6 +38,7 @@ struct Gemm {
     // transposed.  Ignored (full computation) where the pair path does not apply.
     bool sym = false;
     float2* lse_part = nullptr;    // EPI_LSE: [M][N/128]
+    uint32_t* flag = nullptr;      // device flag word for aborted waits (may be null)
 };
 // Fraction of the 2*M*N*K products gemm_tc executes for g (below 1 for symmetric C).
 double gemm_tc_work_fraction(const Gemm& g);
@@ -123,9 +124,10 @@ int embed_backward(const int32_t* tok, const float* g, float* dwte, int M, int d
                    int accumulate, const EmbedBwdWs& ws, cudaStream_t s);
 
 // ------------------------------------------------------------ attention
+// flag: device flag word that an aborted wait or misaligned shared memory sets (may be null).
 template <typename T>
 int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ldo, float* lse,
-                      int B, int T_, int H, int D, cudaStream_t s);
+                      int B, int T_, int H, int D, cudaStream_t s, uint32_t* flag);
 // rope: optional RoPE table ((cos, sin) of pair j at position t at rope[j * rope_ld + t]);
 // when the kernel can rotate dq, dk back itself it does so and sets *rope_done = 1
 // (else the caller applies the inverse RoPE).
@@ -136,7 +138,8 @@ int attention_forward(const T* q, const T* k, const T* v, long ld, T* o, long ld
 template <typename T>
 int attention_backward(const T* q, const T* k, const T* v, long ld, const T* o, const T* dout,
                        long ldo, const float* lse, T* dq, T* dk, T* dv, long ldd, float* delta,
-                       int B, int T_, int H, int D, cudaStream_t s, const float2* rope = nullptr,
+                       int B, int T_, int H, int D, cudaStream_t s, uint32_t* flag,
+                       const float2* rope = nullptr,
                        int rope_ld = 0, int* rope_done = nullptr, bool delta_ready = false,
                        void* ds = nullptr);
 // bytes of the dS scratch above (0 where it would not be used)
