@@ -72,7 +72,12 @@ ROOF = {"gemm": "tensor", "attn_fwd": "tensor", "attn_bwd": "tensor", "muon_ns":
 # GEMMs, each with its split-K reduce when it has one) from the last ncu capture
 # of the current GEMM code (profiles/d20_step_launches.md), None when not measured.
 GEMM_TRAFFIC_PER_LAUNCH = 1.286e9
-CPU_SAMPLE_T = 256
+# The reference arm times one bounded oracle sample per step (the driver runs
+# --steps 20 --warmup 5): a 512-token row and a sixteenth of the embedding's AdamW
+# keep each near ten seconds on the host.  The cpu_baseline of our own arm is one
+# sample of a whole 2048-token row and the whole embedding.
+REF_SAMPLE_T, REF_ADAM_ROWS = 512, 4096
+CPU_SAMPLE_T = 256   # the decode baseline's prompt
 
 
 def peaks():
@@ -138,8 +143,19 @@ def gpu_id_for(torch, dev):
 
 
 # ---------------------------------------------------------------- oracle timing
-def cpu_baseline(w, steps=1, forward_only=False):
-    """The fp64 oracle as it stands, on a bounded sample, in a fresh process."""
+def cpu_baseline(w, steps=1, forward_only=False, T=None, adam_rows=None):
+    """The fp64 oracle as it stands, timed on a bounded sample of one step of workload w
+    in a fresh process on the host cores, and scaled to the whole step.
+
+    Per sample: the forward+backward of one 1 x T row at full widths and depth
+    (forward and loss only for the evaluation pass), then the optimizer on that
+    row's gradients: Muon on one square d x d matrix and on one d x 4d matrix, AdamW
+    on adam_rows rows of the embedding.  The step's time is estimated as
+        t_fb * (B * T_step * n_micro) / T + t_sq * 4L + t_rect * 2L + t_adam * 2V / adam_rows
+    (the optimizer runs once per step).  Returns (tokens/s of the estimate, the
+    per-sample estimated step times, cores, a description of the sample)."""
+    Ts = min(T or w["T"], w["T"])
+    ar = min(adam_rows or w["vocab"], w["vocab"])
     code = (
         "import sys, time, json, os\n"
         f"sys.path.insert(0, {ROOT!r})\n"
@@ -148,26 +164,50 @@ def cpu_baseline(w, steps=1, forward_only=False):
         "from oracle.model import Config\n"
         "from pretraining_step_03_b300 import synth\n"
         f"w = json.loads({json.dumps(json.dumps(w))})\n"
-        f"T = min({CPU_SAMPLE_T}, w['T'])\n"
+        f"T, AR, FWD = {Ts}, {ar}, {bool(forward_only)}\n"
         "cfg = Config(w['depth'], w['d_model'], w['n_head'], w['vocab'])\n"
         "params = synth.init_params(w['depth'], w['d_model'], w['n_head'], w['vocab'], seed=0)\n"
         "tok, tgt = synth.zipf_rows(1, T, w['vocab'], seed=1)\n"
         "tb = synth.token_bytes_binomial(w['vocab'], seed=2)\n"
-        "ts = []\n"
+        "out = []\n"
         f"for _ in range({steps}):\n"
         "    t0 = time.perf_counter()\n"
-        + ("    oracle.eval_sums(params, cfg, tok, tgt, tb)\n" if forward_only else
-           "    oracle.loss_and_grads(params, cfg, tok, tgt, tb)\n") +
-        "    ts.append(time.perf_counter() - t0)\n"
-        "print(json.dumps({'T': T, 'times': ts}))\n")
+        "    if FWD:\n"
+        "        oracle.eval_sums(params, cfg, tok, tgt, tb)\n"
+        "        out.append([time.perf_counter() - t0, 0.0, 0.0, 0.0])\n"
+        "        continue\n"
+        "    _, _, g = oracle.loss_and_grads(params, cfg, tok, tgt, tb)\n"
+        "    t1 = time.perf_counter()\n"
+        "    oracle.muon_step(params[1], g[1], np.zeros_like(g[1]), 0.02)\n"
+        "    t2 = time.perf_counter()\n"
+        "    oracle.muon_step(params[6], g[6], np.zeros_like(g[6]), 0.02)\n"
+        "    t3 = time.perf_counter()\n"
+        "    z = np.zeros((AR, w['d_model']))\n"
+        "    oracle.adamw_step(params[0][:AR], g[0][:AR], z, z, 0.2, 0.8, 0.95, 1e-10, 0.0, 1)\n"
+        "    out.append([t1 - t0, t2 - t1, t3 - t2, time.perf_counter() - t3])\n"
+        "print(json.dumps(out))\n")
     cores = len(os.sched_getaffinity(0))
     env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores),
                MKL_NUM_THREADS=str(cores), CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
     if r.returncode != 0:
         raise RuntimeError("oracle timing failed:\n" + r.stderr[-2000:])
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    return d["T"], d["times"], cores
+    parts = json.loads(r.stdout.strip().splitlines()[-1])
+    L_, n_tok = w["depth"], w["B"] * w["T"] * w.get("n_micro", 1)
+    est = [fb * n_tok / Ts + (0.0 if forward_only else sq * 4 * L_ + rect * 2 * L_ + ad * 2 * w["vocab"] / ar)
+           for fb, sq, rect, ad in parts]
+    if forward_only:
+        sample = (f"forward and loss of 1x{Ts} tokens at full widths (fp64 NumPy), scaled linearly to "
+                  f"{n_tok} tokens")
+    else:
+        sample = (f"forward+backward of 1x{Ts} tokens at full widths, Muon on one {w['d_model']}^2 and one "
+                  f"{w['d_model']}x{4 * w['d_model']} matrix, AdamW on {ar} of the {w['vocab']} embedding rows "
+                  f"(fp64 NumPy); scaled to the step: fwd+bwd x {n_tok}/{Ts} tokens, Muon x {4 * L_} square "
+                  f"+ {2 * L_} rectangular matrices, AdamW x {2 * w['vocab']}/{ar} rows")
+        if Ts < w["T"]:
+            sample += (f"; the {Ts}-token row undercounts attention, whose cost per token grows with the "
+                       f"row length ({w['T']} in the step)")
+    return n_tok / (sum(est) / len(est)), est, cores, sample
 
 
 # ---------------------------------------------------------------- kernel workloads
@@ -334,15 +374,16 @@ def eval_workload(args):
     if args.impl == "reference":
         if rank != 0:
             return
-        Tc, times, cores = cpu_baseline(w, steps=args.warmup + args.steps, forward_only=True)
-        t = times[args.warmup:] if len(times) > args.warmup else times
-        v = Tc / (sum(t) / len(t))
+        _, est, cores, sample = cpu_baseline(w, steps=args.warmup + args.steps, forward_only=True,
+                                             T=REF_SAMPLE_T)
+        t = est[args.warmup:] if len(est) > args.warmup else est
+        v = B * T / (sum(t) / len(t))
         print(json.dumps({"metric": EVAL_METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
                           "steps": len(t), "warmup": args.warmup, "ms_per_step": 1000 * sum(t) / len(t),
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                           "data": "synthetic", "config": config, "impl": "reference",
                           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                           "sample": f"forward and loss of 1x{Tc} tokens at full widths"},
+                                           "sample": sample},
                           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                                   "d2h_bytes_per_step": 0}}), flush=True)
         return
@@ -441,9 +482,9 @@ def eval_workload(args):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        Tc, times, cores = cpu_baseline(w, steps=1, forward_only=True)
-        line["cpu_baseline"] = {"value": Tc / times[0], "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                "sample": f"forward and loss of 1x{Tc} tokens at full widths (fp64 NumPy)"}
+        v, _, cores, sample = cpu_baseline(w, steps=1, forward_only=True)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -654,16 +695,16 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        T, times, cores = cpu_baseline(w, steps=args.warmup + args.steps)
-        t = times[args.warmup:] if len(times) > args.warmup else times
-        v = T / (sum(t) / len(t))
+        _, est, cores, sample = cpu_baseline(w, steps=args.warmup + args.steps, T=REF_SAMPLE_T,
+                                             adam_rows=REF_ADAM_ROWS)
+        t = est[args.warmup:] if len(est) > args.warmup else est
+        v = tokens_per_step / (sum(t) / len(t))
         line = {"metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world, "steps": len(t),
                 "warmup": args.warmup, "ms_per_step": 1000 * sum(t) / len(t), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": config, "impl": "reference",
                 "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                 "sample": f"forward+backward of 1x{T} tokens at full widths (fp64 NumPy); "
-                                           "optimizer excluded"},
+                                 "sample": sample},
                 "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -787,10 +828,9 @@ def main():
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        Tc, times, cores = cpu_baseline(w, steps=1)
-        line["cpu_baseline"] = {"value": Tc / times[0], "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                "sample": f"forward+backward of 1x{Tc} tokens at full widths (fp64 NumPy); "
-                                          "optimizer excluded"}
+        v, _, cores, sample = cpu_baseline(w, steps=1)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
