@@ -16,8 +16,9 @@ Checks, with the GPU's own greedy tokens fed to the oracle (teacher forcing):
   * the cached k (after RoPE) and v against the oracle's;
   * an identity model (zero blocks, orthonormal tied embeddings) repeats the
     prompt's last token exactly;
-  * the d20 model at full size, 32 identical prompts of 512 tokens: every row
-    generates the same tokens and matches the oracle's single row.
+  * the d20 model at full size, 32 prompts of 512 tokens made of three
+    distinct prompts in a non-periodic row order: rows with the same prompt
+    generate the same tokens, and each prompt's logits match the oracle's.
 """
 
 import numpy as np
@@ -27,6 +28,7 @@ import oracle
 from oracle import generate as og
 from oracle.model import Config
 from pretraining_step_03_b300 import synth
+from tests import _mix
 from tests._util import assert_close, bf16_round
 
 pytestmark = pytest.mark.gpu
@@ -127,24 +129,30 @@ def test_argument_checks():
     assert m.check_flag() == 0
 
 
-def test_d20_full_size_identical_prompts():
+def test_d20_full_size_distinct_prompts():
+    """d20 at full size: 32 prompts of 512 tokens, three distinct Zipf prompts in a
+    non-periodic row order (tests/_mix.py).  Rows that hold the same prompt must
+    generate the same tokens, and each of the three against the oracle."""
     import torch
     from pretraining_step_03_b300.model import Model
     depth, d, H, V, B, T0, n_new = 20, 1280, 10, 65536, 32, 512, 8
     params = synth.init_params(depth, d, H, V, seed=0)
-    row, _ = synth.zipf_rows(1, T0, V, seed=1)
-    prompt = np.repeat(row, B, axis=0)
+    mix = _mix.mixed((9, 13, 10), T0, V, seq_seed=1, order_seed=2)
     m = Model(depth, d, H, V, B, 2048, dtype="bf16")
     m.set_params(params)
-    cache, z_gpu, tok = _run(m, None, prompt, n_new, B, 1024)
+    cache, z_gpu, tok = _run(m, None, mix.tokens, n_new, B, 1024)
     m.close()
     del m, cache
     torch.cuda.empty_cache()
-    assert np.all(tok == tok[:1]), "identical prompts generated different tokens"
-    z_ref = og.teacher_forced_logits([bf16_round(p) for p in params], Config(depth, d, H, V), row, tok[:1])
-    for i in range(n_new):
-        assert_close(z_gpu[0, i], z_ref[0, i], 0.999, 2e-2, f"d20 step {i} logits")
-    _check_tokens(tok[:1], z_gpu[:1], z_ref, 2e-2)
+    first = [int(np.flatnonzero(mix.order == j)[0]) for j in range(3)]
+    for b in range(B):
+        assert np.array_equal(tok[b], tok[first[mix.order[b]]]), f"row {b} differs from its prompt's first row"
+    z_ref = og.teacher_forced_logits([bf16_round(p) for p in params], Config(depth, d, H, V), mix.seq_tok,
+                                     tok[first])
+    for j, b in enumerate(first):
+        for i in range(n_new):
+            assert_close(z_gpu[b, i], z_ref[j, i], 0.999, 2e-2, f"d20 prompt {j} (row {b}) step {i} logits")
+    _check_tokens(tok[first], z_gpu[first], z_ref, 2e-2)
 
 
 @pytest.mark.parametrize("mode", ["fp32", "bf16"])

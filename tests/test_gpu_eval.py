@@ -9,8 +9,9 @@ Checks: the sums over two batches against the oracle's (relative error
 <= 1e-5 in fp32 mode, 1e-3 in bf16 mode, as the loss); the batch's
 {loss, bpb} bit-identical to what the training pass reports for the same
 batch and weights; gradients and weights untouched (bit for bit).  At the
-benchmark's d20 size, 32 identical copies of one Zipf row make the sums 32
-times the oracle's single-row sums.
+benchmark's d20 size (32 x 2048) the batch holds three distinct Zipf
+sequences in a non-periodic row order, and the expected sums are the
+count-weighted sums of the oracle's per-sequence sums.
 """
 
 import math
@@ -21,6 +22,7 @@ import pytest
 import oracle
 from oracle.model import Config
 from pretraining_step_03_b300 import synth
+from tests import _mix
 from tests._util import bf16_round
 
 pytestmark = pytest.mark.gpu
@@ -72,31 +74,34 @@ def test_tiny_eval_sums_and_no_side_effects(mode):
     assert np.array_equal(fb.cpu().numpy(), batch), (fb.cpu().numpy(), batch)
 
 
-def test_d20_eval_full_size_identical_rows():
+def test_d20_eval_full_size_distinct_rows():
+    """The d20 evaluation pass at 32 x 2048: three distinct Zipf sequences over the
+    32 rows (tests/_mix.py), so the sums are exact count-weighted sums of the
+    oracle's per-sequence sums."""
     import torch
     from pretraining_step_03_b300.model import Model
     depth, d, h, v, Bf, Tf = 20, 1280, 10, 65536, 32, 2048
+    mix = _mix.d20_mix(Tf)
     params = synth.init_params(depth, d, h, v, seed=0)
-    tok1, tgt1 = synth.zipf_rows(1, Tf, v, seed=1)
     tb = synth.token_bytes_binomial(v, seed=2)
-    tok = np.repeat(tok1, Bf, axis=0)
-    tgt = np.repeat(tgt1, Bf, axis=0)
     m = Model(depth, d, h, v, Bf, Tf, dtype="bf16")
     m.set_params(params)
     dt = m.device_i32
+    tok, tgt = dt(mix.tokens), dt(mix.targets)
     out = torch.zeros(2, dtype=torch.float32, device=m.device)
-    sums = m.eval_loss(dt(tok), dt(tgt), dt(tb), Bf, Tf, out=out)
+    sums = m.eval_loss(tok, tgt, dt(tb), Bf, Tf, out=out)
     torch.cuda.synchronize()
     got = sums.cpu().numpy()
     batch = out.cpu().numpy().copy()
-    fb = m.forward_backward(dt(tok), dt(tgt), dt(tb), Bf, Tf)
+    fb = m.forward_backward(tok, tgt, dt(tb), Bf, Tf)
     torch.cuda.synchronize()
     assert np.array_equal(fb.cpu().numpy(), batch)
     assert m.check_flag() == 0
     m.close()
     del m
     torch.cuda.empty_cache()
-    ref = oracle.eval_sums([bf16_round(p) for p in params], Config(depth, d, h, v), tok1, tgt1, tb)
-    assert got[2] == Bf * ref[2]
+    _, ref_bpb, ref, _ = _mix.oracle_expectation(_mix.d20_config(), mix, keep=_mix.D20_KEEP)
+    assert got[2] == ref[2]                    # integer byte count: exact
     for k in range(2):
-        assert abs(got[k] - Bf * ref[k]) / abs(Bf * ref[k]) <= 1e-3, (k, got[k], Bf * ref[k])
+        assert abs(got[k] - ref[k]) / abs(ref[k]) <= 1e-3, (k, got[k], ref[k])
+    assert abs(batch[1] - ref_bpb) / ref_bpb <= 1e-3, (batch[1], ref_bpb)

@@ -11,10 +11,12 @@ arithmetic is fp32 against fp64, so gradients must agree to max-rel 1e-4
 (cosine >= 0.99999) and updates, which Newton-Schulz amplifies up to
 3.4445^5 ~ 490x on the smallest singular values, to max-rel 1e-3.
 Muon's orthogonalised update alone is also checked; in bf16 mode its five
-Newton-Schulz iterations round X, A and B to bf16 (2^-9) fifteen times and
-the same ~490x gain applies to the smallest singular directions, so it is
-held to cosine >= 0.998 and to the stated singular-value band (see the
-test) rather than element by element.
+Newton-Schulz iterations store X, A and B in bf16 fifteen times and the
+same ~490x gain applies to the smallest singular directions, so it is held
+to the stated singular-value band (see the test) rather than element by
+element, and to cosine >= 0.999 wherever bf16 storage allows that on the
+gradient's spectrum, else to 1 - 2 (1 - c) with c the cosine of a bf16
+storage model of the iteration (tests/_util.py, ns_bf16_model).
 """
 
 import numpy as np
@@ -23,7 +25,7 @@ import pytest
 import oracle
 from oracle.model import Config
 from pretraining_step_03_b300 import synth
-from tests._util import assert_close, bf16_round, cmp
+from tests._util import assert_close, bf16_round, cmp, muon_update_cos_min
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +33,7 @@ DEPTH, D, H, V, B, T = 2, 128, 2, 512, 4, 64
 CFG = Config(DEPTH, D, H, V)
 TOL = {
     "fp32": dict(loss=1e-5, gcos=0.99999, grel=1e-4, ucos=0.9999, urel=1e-3, dcos=0.9999),
-    "bf16": dict(loss=1e-3, gcos=0.999, grel=2e-2, ucos=0.999, urel=2e-2, dcos=0.998),
+    "bf16": dict(loss=1e-3, gcos=0.999, grel=2e-2, ucos=0.999, urel=2e-2, dcos=None),
 }
 HP = dict(muon_lr=0.02, momentum=0.95, lr_emb=0.2, lr_unemb=0.004, beta1=0.8, beta2=0.95, eps=1e-10,
           wd=0.0)
@@ -82,7 +84,7 @@ def test_tiny_optimizer_step_given_gradients(mode, inputs):
     singular basis: with X_ref = U diag(s) V^T (fp64), u_i^T X v_i must stay
     within 0.1 of s_i and inside the stated bf16 band [0.6, 1.3] wherever
     s_i >= 0.68 (inputs with sigma/|G| >= 1e-2 map there), and cos(X, X_ref)
-    >= 0.998 (bf16) / 0.9999 (fp32).
+    >= 0.9999 (fp32) / the bf16 bound of the module docstring.
     """
     params, tok, tgt, tb = inputs
     m = _model(mode, params)
@@ -116,7 +118,12 @@ def test_tiny_optimizer_step_given_gradients(mode, inputs):
                 r, c = got.shape
                 x = (prev[i] - got) / (HP["muon_lr"] * np.sqrt(max(1.0, r / c)))
                 cos, _ = cmp(x, xref[i])
-                assert cos >= tol["dcos"], f"{mode} step {step} Muon update {i}: cos {cos}"
+                if tol["dcos"] is None:   # bf16: the bound bf16 storage allows on this spectrum
+                    geff = grads[i] + HP["momentum"] * buf[i]
+                    cmin, cmodel = muon_update_cos_min(geff, xref[i])
+                else:
+                    cmin, cmodel = tol["dcos"], None
+                assert cos >= cmin, f"{mode} step {step} Muon update {i}: cos {cos} (min {cmin}, model {cmodel})"
                 u, sv, vt = np.linalg.svd(xref[i], full_matrices=False)
                 proj = np.einsum("ki,kl,il->i", u, x, vt)
                 sel = sv >= 0.68
