@@ -117,6 +117,7 @@ struct EmbedBwdWs {
     int* sorted;     // [M]
     float* head;     // [npieces * d]
     float* tail;     // [npieces * d]
+    int* bsum;       // [ceil(V / 256)] token counts per 256 ids
 };
 size_t embed_backward_ws_bytes(int M, int d, int V);
 EmbedBwdWs embed_backward_ws(void* base, int M, int d, int V);

@@ -399,40 +399,73 @@ __global__ void __launch_bounds__(EB_CHUNK) eb_hist_rank_kernel(const int32_t* t
     atomicAdd(&hist[(long)c * V + t], 1);
 }
 
-__global__ void eb_colscan_kernel(int* hist, int* counts, int nchunks, int V) {
-    int v = blockIdx.x * blockDim.x + threadIdx.x;
-    if (v >= V) return;
+// Per token id v (one thread each): the column scan of the per-chunk counts, which
+// turns hist[c][v] into the number of rows of token v in chunks before c; then the
+// exclusive scan of the token counts within this CTA's 256 ids (offsets[v], local to
+// the CTA) and the CTA's total (bsum[blockIdx.x]).
+constexpr int EB_SCAN_T = 256;
+
+__global__ void __launch_bounds__(EB_SCAN_T) eb_colscan_kernel(int* hist, int* offsets, int* bsum, int nchunks,
+                                                               int V) {
+    __shared__ int wsum[EB_SCAN_T / 32];
+    const int v = blockIdx.x * EB_SCAN_T + threadIdx.x;
     int run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-        int h = hist[(long)c * V + v];
-        hist[(long)c * V + v] = run;
-        run += h;
+    if (v < V) {
+        // 16 chunks' counts in flight at a time (the loads do not wait on the stores)
+        for (int c0 = 0; c0 < nchunks; c0 += 16) {
+            int h[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) h[k] = c0 + k < nchunks ? __ldcs(hist + (long)(c0 + k) * V + v) : 0;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                if (c0 + k < nchunks) hist[(long)(c0 + k) * V + v] = run;
+                run += h[k];
+            }
+        }
     }
-    counts[v] = run;
+    // exclusive scan of run over the CTA: warp shuffles, then the warp totals
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    int before = 0;
+#pragma unroll
+    for (int k = 0; k < EB_SCAN_T / 32; ++k) before += k < w ? wsum[k] : 0;
+    if (v < V) offsets[v] = before + x - run;
+    if (threadIdx.x == EB_SCAN_T - 1) bsum[blockIdx.x] = before + x;
 }
 
-// exclusive scan of counts[0..V) in place, offsets[V] = total; one CTA of 1024
-__global__ void __launch_bounds__(1024) eb_scan_kernel(int* offsets, int V) {
-    __shared__ int part[1024];
-    const int per = (V + 1023) / 1024;
-    const int b = threadIdx.x * per, e = min(V, b + per);
-    int s = 0;
-    for (int i = b; i < e; ++i) s += offsets[i];
-    part[threadIdx.x] = s;
+// offsets[v] += the exclusive prefix of the CTA totals of eb_colscan_kernel;
+// offsets[V] = the number of rows.  One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) eb_scan_kernel(int* offsets, const int* bsum, int nb, int V) {
+    __shared__ int pre[1024];
+    __shared__ int carry;
+    if (threadIdx.x == 0) carry = 0;
     __syncthreads();
-    for (int o = 1; o < 1024; o <<= 1) {
-        int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+    // the CTA totals (nb <= a few thousand), scanned 1024 at a time
+    extern __shared__ int boff[];
+    for (int b0 = 0; b0 < nb; b0 += 1024) {
+        const int i = b0 + threadIdx.x;
+        pre[threadIdx.x] = i < nb ? bsum[i] : 0;
         __syncthreads();
-        part[threadIdx.x] += v;
+        for (int o = 1; o < 1024; o <<= 1) {
+            const int y = threadIdx.x >= o ? pre[threadIdx.x - o] : 0;
+            __syncthreads();
+            pre[threadIdx.x] += y;
+            __syncthreads();
+        }
+        if (i < nb) boff[i] = carry + pre[threadIdx.x] - (i < nb ? bsum[i] : 0);
+        __syncthreads();
+        if (threadIdx.x == 1023) carry += pre[1023];
         __syncthreads();
     }
-    int run = part[threadIdx.x] - s;
-    for (int i = b; i < e; ++i) {
-        int c = offsets[i];
-        offsets[i] = run;
-        run += c;
-    }
-    if (threadIdx.x == 1023) offsets[V] = part[1023];
+    for (int v = threadIdx.x; v < V; v += 1024) offsets[v] += boff[v / EB_SCAN_T];
+    if (threadIdx.x == 0) offsets[V] = carry;
 }
 
 __global__ void eb_scatter_kernel(const int32_t* tok, const int* hist, const int* rank,
@@ -477,18 +510,25 @@ __global__ void __launch_bounds__(EB_COLS) eb_piece_kernel(const int32_t* tok, c
     }
 }
 
-__global__ void eb_fixup_kernel(const int* offsets, const float* head, const float* tail,
-                                float* dwte, int d, int accumulate) {
-    const int id = blockIdx.x;
+// Tokens whose run of sorted rows crosses a piece border: the piece where the run
+// starts adds its own part (head or tail) and the heads of the pieces it runs into,
+// in order.  One CTA per piece.
+__global__ void eb_fixup_kernel(const int32_t* tok, const int* sorted, const int* offsets, const float* head,
+                                const float* tail, float* dwte, int d, int V, int accumulate) {
+    const int pa = blockIdx.x;
+    const int Mv = offsets[V];
+    const int p0 = pa * EB_PIECE, p1 = min(p0 + EB_PIECE, Mv);
+    if (p0 >= Mv) return;
+    const int id = tok[sorted[p1 - 1]];   // the last run of this piece
     const int off = offsets[id], cnt = offsets[id + 1] - off;
-    if (cnt == 0) return;
-    const int pa = off / EB_PIECE, pb = (off + cnt - 1) / EB_PIECE;
-    if (pa == pb) return;
+    if (off + cnt <= p1) return;          // ends inside this piece: written by eb_piece_kernel
+    if (off < p0) return;                 // started in an earlier piece, which sums it
+    const int pb = (off + cnt - 1) / EB_PIECE;
     for (int col = threadIdx.x; col < d; col += blockDim.x) {
-        float s = (off == pa * EB_PIECE) ? head[(long)pa * d + col] : tail[(long)pa * d + col];
-        for (int p = pa + 1; p <= pb; ++p) s += head[(long)p * d + col];
+        float sum = (off == p0) ? head[(long)pa * d + col] : tail[(long)pa * d + col];
+        for (int p = pa + 1; p <= pb; ++p) sum += head[(long)p * d + col];
         float* dst = dwte + (long)id * d + col;
-        *dst = accumulate ? *dst + s : s;
+        *dst = accumulate ? *dst + sum : sum;
     }
 }
 
@@ -581,7 +621,7 @@ static size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
 size_t embed_backward_ws_bytes(int M, int d, int V) {
     long nchunks = ceil_div(M, EB_CHUNK), npieces = ceil_div(M, EB_PIECE);
     return al256(nchunks * V * 4) + al256((size_t)M * 4) + al256(((size_t)V + 1) * 4) +
-           al256((size_t)M * 4) + 2 * al256((size_t)npieces * d * 4);
+           al256((size_t)M * 4) + 2 * al256((size_t)npieces * d * 4) + al256((size_t)ceil_div(V, EB_SCAN_T) * 4);
 }
 
 EmbedBwdWs embed_backward_ws(void* base, int M, int d, int V) {
@@ -593,7 +633,8 @@ EmbedBwdWs embed_backward_ws(void* base, int M, int d, int V) {
     w.offsets = (int*)p; p += al256(((size_t)V + 1) * 4);
     w.sorted = (int*)p;  p += al256((size_t)M * 4);
     w.head = (float*)p;  p += al256((size_t)npieces * d * 4);
-    w.tail = (float*)p;
+    w.tail = (float*)p;  p += al256((size_t)npieces * d * 4);
+    w.bsum = (int*)p;
     return w;
 }
 
@@ -603,13 +644,15 @@ int embed_backward(const int32_t* tok, const float* g, float* dwte, int M, int d
     if (!accumulate) NC_TRY(cuda_check(cudaMemsetAsync(dwte, 0, (size_t)V * d * 4, s), "memset dwte"));
     if (M <= 0) return NC_OK;
     NC_TRY(cuda_check(cudaMemsetAsync(ws.hist, 0, (size_t)nchunks * V * 4, s), "memset hist"));
+    const int nb = ceil_div(V, EB_SCAN_T);
+    if ((size_t)nb * 4 > 48 * 1024) return set_error(NC_ERR_UNSUPPORTED, "embedding backward: vocab %d too large", V);
     eb_hist_rank_kernel<<<nchunks, EB_CHUNK, 0, s>>>(tok, ws.hist, ws.rank, M, V);
-    eb_colscan_kernel<<<ceil_div(V, 256), 256, 0, s>>>(ws.hist, ws.offsets, nchunks, V);
-    eb_scan_kernel<<<1, 1024, 0, s>>>(ws.offsets, V);
+    eb_colscan_kernel<<<nb, EB_SCAN_T, 0, s>>>(ws.hist, ws.offsets, ws.bsum, nchunks, V);
+    eb_scan_kernel<<<1, 1024, (size_t)nb * 4, s>>>(ws.offsets, ws.bsum, nb, V);
     eb_scatter_kernel<<<ceil_div(M, 256), 256, 0, s>>>(tok, ws.hist, ws.rank, ws.offsets, ws.sorted, M, V);
     eb_piece_kernel<<<dim3(npieces, ceil_div(d, EB_COLS)), EB_COLS, 0, s>>>(
         tok, ws.sorted, ws.offsets, g, dwte, ws.head, ws.tail, d, V, accumulate);
-    eb_fixup_kernel<<<V, 256, 0, s>>>(ws.offsets, ws.head, ws.tail, dwte, d, accumulate);
+    eb_fixup_kernel<<<npieces, 256, 0, s>>>(tok, ws.sorted, ws.offsets, ws.head, ws.tail, dwte, d, V, accumulate);
     note_launch(6);
     NC_LAUNCH_CHECK("embed_backward");
     return NC_OK;
