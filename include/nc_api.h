@@ -89,8 +89,9 @@ NC_API int nc_arena_bytes(int depth, int d_model, int n_head, int vocab, int max
 /*
  * Create a model (section 预搜检: depth layers of width d_model with n_head
  * heads; section 该你了: depth is the one size knob).  Weights are drawn
- * N(0, 0.02) from a host generator seeded by `seed` (splitmix64 feeding a
- * Box-Muller transform) and copied into the arena; optimizer state is zero.
+ * N(0, 0.02) on the device: value pair k (parameters in index order) is the
+ * Box-Muller transform of outputs 2k and 2k+1 of the splitmix64 stream
+ * seeded by `seed`; optimizer state is zero.
  * arena: device pointer, 256-byte aligned, arena_bytes >= nc_arena_bytes().
  * stream: a cudaStream_t (NULL = legacy default stream) all work is put on.
  * Synchronises the stream before returning.  *out receives the handle.

@@ -466,11 +466,29 @@ int download_f32(nc_model* m, float* host, const float* src, size_t n) {
     return cuda_check(cudaStreamSynchronize(m->stream), "sync");
 }
 
-uint64_t splitmix(uint64_t& s) {
-    uint64_t z = (s += 0x9E3779B97F4A7C15ull);
+// splitmix64 is counter-based: output i (0-based) of the stream seeded with s is
+// mix(s + (i + 1) * golden), so any element of the weight stream can be drawn on its own.
+__host__ __device__ __forceinline__ uint64_t splitmix_at(uint64_t seed, uint64_t i) {
+    uint64_t z = seed + (i + 1) * 0x9E3779B97F4A7C15ull;
     z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
     z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
     return z ^ (z >> 31);
+}
+
+// Weights N(0, std): value pair k of the model (parameters in index order, pairs
+// numbered from pair0 for this tensor) is the Box-Muller transform of outputs 2k and
+// 2k + 1 of the splitmix64 stream seeded with `seed`.
+__global__ void init_normal_kernel(float* w, long n, uint64_t seed, long pair0, double std) {
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (2 * i >= n) return;
+    const uint64_t k = (uint64_t)(pair0 + i);
+    const double u1 = ((splitmix_at(seed, 2 * k) >> 11) + 1.0) * (1.0 / 9007199254740993.0);
+    const double u2 = (splitmix_at(seed, 2 * k + 1) >> 11) * (1.0 / 9007199254740992.0);
+    const double rr = sqrt(-2.0 * log(u1)) * std;
+    double sn, cs;
+    sincospi(2.0 * u2, &sn, &cs);
+    w[2 * i] = (float)(rr * cs);
+    if (2 * i + 1 < n) w[2 * i + 1] = (float)(rr * sn);
 }
 
 int check_param(nc_model* m, int index, size_t n) {
@@ -539,20 +557,14 @@ int nc_init_model(int depth, int d_model, int n_head, int vocab, uint64_t seed, 
     int rc = NC_OK;
     do {
         cudaStream_t s = m->stream;
-        // weights N(0, 0.02): splitmix64 -> Box-Muller, one tensor at a time
-        uint64_t st = seed;
-        std::vector<float> h;
+        // weights N(0, 0.02) drawn on the device, one tensor at a time (init_normal_kernel)
+        long pair0 = 0;
         for (int i = 0; i < m->nparams && rc == NC_OK; ++i) {
-            const size_t n = (size_t)(m->prows[i] * m->pcols[i]);
-            h.resize(n);
-            for (size_t j = 0; j < n; j += 2) {
-                double u1 = ((splitmix(st) >> 11) + 1.0) * (1.0 / 9007199254740993.0);
-                double u2 = (splitmix(st) >> 11) * (1.0 / 9007199254740992.0);
-                double rr = sqrt(-2.0 * log(u1)) * 0.02;
-                h[j] = (float)(rr * cos(6.283185307179586 * u2));
-                if (j + 1 < n) h[j + 1] = (float)(rr * sin(6.283185307179586 * u2));
-            }
-            rc = upload_f32(m, m->master + m->poff[i], h.data(), n);
+            const long n = m->prows[i] * m->pcols[i];
+            init_normal_kernel<<<ceil_div((n + 1) / 2, 256), 256, 0, s>>>(m->master + m->poff[i], n, seed, pair0, 0.02);
+            note_launch();
+            rc = cuda_check(cudaGetLastError(), "init_normal_kernel");
+            pair0 += (n + 1) / 2;
         }
         if (rc) break;
         if (m->shadow && (rc = cast_f32_bf16(m->master, m->shadow, m->P, s))) break;
