@@ -478,41 +478,62 @@ __global__ void eb_scatter_kernel(const int32_t* tok, const int* hist, const int
     sorted[offsets[t] + hist[c * V + t] + rank[r]] = (int)r;
 }
 
+// One CTA per (piece of EB_PIECE sorted rows, EB_COLS columns).  The piece's row
+// indices and token ids are staged in shared memory first, so the gradient rows are
+// read eight at a time with their loads in flight together; they are still added in
+// sorted order.
 __global__ void __launch_bounds__(EB_COLS) eb_piece_kernel(const int32_t* tok, const int* sorted,
                                                            const int* offsets, const float* g,
                                                            float* dwte, float* head, float* tail,
                                                            int d, int V, int accumulate) {
-    const int piece = blockIdx.x, col = blockIdx.y * EB_COLS + threadIdx.x;
+    __shared__ int s_row[EB_PIECE];
+    __shared__ int s_id[EB_PIECE + 1];
+    const int piece = blockIdx.x;
     const int Mv = offsets[V];
     const int p0 = piece * EB_PIECE, p1 = min(p0 + EB_PIECE, Mv);
-    if (p0 >= Mv || col >= d) return;
+    if (p0 >= Mv) return;
+    const int n = p1 - p0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int r = sorted[p0 + i];
+        s_row[i] = r;
+        s_id[i] = tok[r];
+    }
+    if (threadIdx.x == 0) s_id[n] = -1;
+    __syncthreads();
+    const int col = blockIdx.y * EB_COLS + threadIdx.x;
+    if (col >= d) return;
     float acc = 0.f;
-    int run_start = p0;
-    int id = tok[sorted[p0]];
-    for (int p = p0; p < p1; ++p) {
-        const int r = sorted[p];
-        acc += g[(long)r * d + col];
-        const int next = (p + 1 < p1) ? tok[sorted[p + 1]] : -1;
-        if (next != id) {
-            const int off = offsets[id], cnt = offsets[id + 1] - off;
-            if (off >= p0 && off + cnt <= p1) {
-                float* dst = dwte + (long)id * d + col;
-                *dst = accumulate ? *dst + acc : acc;
-            } else if (run_start == p0) {
-                head[(long)piece * d + col] = acc;
-            } else {
-                tail[(long)piece * d + col] = acc;
+    int run_start = 0;   // relative to p0
+    for (int i0 = 0; i0 < n; i0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = i0 + u < n ? __ldcs(g + (long)s_row[i0 + u] * d + col) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u;
+            if (i >= n) break;
+            acc += v[u];
+            const int id = s_id[i];
+            if (s_id[i + 1] != id) {   // the run of token id ends at sorted position p0 + i
+                const int off = offsets[id], cnt = offsets[id + 1] - off;
+                if (off >= p0 && off + cnt <= p1) {
+                    float* dst = dwte + (long)id * d + col;
+                    *dst = accumulate ? *dst + acc : acc;
+                } else if (run_start == 0) {
+                    head[(long)piece * d + col] = acc;
+                } else {
+                    tail[(long)piece * d + col] = acc;
+                }
+                acc = 0.f;
+                run_start = i + 1;
             }
-            acc = 0.f;
-            run_start = p + 1;
-            id = next;
         }
     }
 }
 
 // Tokens whose run of sorted rows crosses a piece border: the piece where the run
 // starts adds its own part (head or tail) and the heads of the pieces it runs into,
-// in order.  One CTA per piece.
+// in order.  One CTA per (piece, 256 columns).
 __global__ void eb_fixup_kernel(const int32_t* tok, const int* sorted, const int* offsets, const float* head,
                                 const float* tail, float* dwte, int d, int V, int accumulate) {
     const int pa = blockIdx.x;
@@ -524,7 +545,7 @@ __global__ void eb_fixup_kernel(const int32_t* tok, const int* sorted, const int
     if (off + cnt <= p1) return;          // ends inside this piece: written by eb_piece_kernel
     if (off < p0) return;                 // started in an earlier piece, which sums it
     const int pb = (off + cnt - 1) / EB_PIECE;
-    for (int col = threadIdx.x; col < d; col += blockDim.x) {
+    for (int col = blockIdx.y * blockDim.x + threadIdx.x; col < d; col += gridDim.y * blockDim.x) {
         float sum = (off == p0) ? head[(long)pa * d + col] : tail[(long)pa * d + col];
         for (int p = pa + 1; p <= pb; ++p) sum += head[(long)p * d + col];
         float* dst = dwte + (long)id * d + col;
@@ -652,7 +673,7 @@ int embed_backward(const int32_t* tok, const float* g, float* dwte, int M, int d
     eb_scatter_kernel<<<ceil_div(M, 256), 256, 0, s>>>(tok, ws.hist, ws.rank, ws.offsets, ws.sorted, M, V);
     eb_piece_kernel<<<dim3(npieces, ceil_div(d, EB_COLS)), EB_COLS, 0, s>>>(
         tok, ws.sorted, ws.offsets, g, dwte, ws.head, ws.tail, d, V, accumulate);
-    eb_fixup_kernel<<<npieces, 256, 0, s>>>(tok, ws.sorted, ws.offsets, ws.head, ws.tail, dwte, d, V, accumulate);
+    eb_fixup_kernel<<<dim3(npieces, ceil_div(d, 256)), 256, 0, s>>>(tok, ws.sorted, ws.offsets, ws.head, ws.tail, dwte, d, V, accumulate);
     note_launch(6);
     NC_LAUNCH_CHECK("embed_backward");
     return NC_OK;
