@@ -14,6 +14,7 @@
 // k and v to the cache, attention of one query over the cached keys (split over key
 // chunks, then combined), and the greedy next token.
 #include "kernels.cuh"
+#include "tc_ptx.cuh"
 
 namespace nc {
 namespace {
@@ -208,6 +209,138 @@ __global__ void __launch_bounds__(DA_THREADS) decode_attn_kernel(const T* q, con
     if (dim == 0) part_ml[pc] = make_float2(mm, ll);
 }
 
+// The same chunked one-query attention for bf16 caches with the cache rows brought in
+// by TMA: tiles of 32 keys x 128 dims of k and of v (two 64-dim atoms each, 128-byte
+// swizzle) in a ring of DT_ST stages, so the copies run ahead of the arithmetic instead
+// of each group waiting on its own loads.  Group g (16 lanes, 8 dims each) takes keys
+// g, g+8, g+16 and g+24 of every tile, four at a time.
+constexpr int DT_KEYS = 32;
+constexpr int DT_ST = 4;
+constexpr int DT_TILE = DT_KEYS * DA_HD * 2;          // 8 KB
+// tiles | barriers (64 B) | group merge [DA_GROUPS][DA_HD] + m, l | abort word
+constexpr int DT_SMEM = DT_ST * 2 * DT_TILE + 64 + (DA_GROUPS * DA_HD + 2 * DA_GROUPS + 4) * 4;
+
+// this lane's 8 dims of key row r of a swizzled tile (atom = dims 64a .. 64a+63)
+__device__ __forceinline__ const uint8_t* dt_addr(const uint8_t* tile, int r, int lane16) {
+    const int a = lane16 >> 3, c = lane16 & 7;
+    return tile + a * (DT_KEYS * 128) + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(DA_THREADS) decode_attn_tma_kernel(
+    const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, const bf16* q, int d,
+    int cache_T, int n_arg, const int* pos_dev, int kchunk, float scale, float* part_o, float2* part_ml) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(dsm + DT_ST * 2 * DT_TILE);
+    float (*s_o)[DA_HD] = reinterpret_cast<float (*)[DA_HD]>(dsm + DT_ST * 2 * DT_TILE + 64);
+    float* s_m = &s_o[DA_GROUPS][0];
+    float* s_l = s_m + DA_GROUPS;
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_l + DA_GROUPS);
+    // the swizzled tiles need a 1024-byte aligned base; without it the chunk reports NaN
+    const bool bad = (tc::smem_u32(dsm) & 1023u) != 0;
+    const int n = pos_dev ? *pos_dev + 1 : n_arg;
+    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, H = gridDim.y, nchunk = gridDim.x;
+    const int g = threadIdx.x / 16, lane = threadIdx.x % 16;
+    const int k0 = chunk * kchunk, k1 = min(n, k0 + kchunk);
+    const int ntile = bad ? 0 : k1 > k0 ? (k1 - k0 + DT_KEYS - 1) / DT_KEYS : 0;
+    const int row0 = b * cache_T + k0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < DT_ST; ++i) tc::mbar_init(&full[i], 1);
+        *s_abort = 0;
+        tc::fence_barrier_init();
+    }
+    __syncthreads();
+    auto issue = [&](int i) {
+        uint8_t* kt = dsm + (i % DT_ST) * 2 * DT_TILE;
+        uint64_t* bar = &full[i % DT_ST];
+        tc::mbar_expect_tx(bar, 2 * DT_TILE);
+        const int y = row0 + i * DT_KEYS;
+        tc::tma_load_3d(kt, &mk, bar, h * DA_HD, y, 0);
+        tc::tma_load_3d(kt + DT_TILE / 2, &mk, bar, h * DA_HD + 64, y, 0);
+        tc::tma_load_3d(kt + DT_TILE, &mv, bar, h * DA_HD, y, 0);
+        tc::tma_load_3d(kt + DT_TILE + DT_TILE / 2, &mv, bar, h * DA_HD + 64, y, 0);
+    };
+    if (threadIdx.x == 0)
+        for (int i = 0; i < DT_ST && i < ntile; ++i) issue(i);
+    float qf[8];
+    Vec8<bf16>::load(q + (long)b * d + h * DA_HD + lane * 8, qf);
+    const float c2 = scale * LOG2E_D;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qf[e] *= c2;
+    float m = bad ? NAN : -INFINITY, l = 0.f, o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = 0.f;
+    for (int i = 0; i < ntile; ++i) {
+        if (!tc::mbar_wait(&full[i % DT_ST], (i / DT_ST) & 1, s_abort)) {
+            m = NAN;   // a copy that never landed: the step's logits come out NaN (flagged)
+            break;
+        }
+        const uint8_t* kt = dsm + (i % DT_ST) * 2 * DT_TILE;
+        const uint8_t* vt = kt + DT_TILE;
+        const int kbase = k0 + i * DT_KEYS;
+        float sc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float kf[8];
+            Vec8<bf16>::load(reinterpret_cast<const bf16*>(dt_addr(kt, g + 8 * u, lane)), kf);
+            float x = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x = fmaf(qf[e], kf[e], x);
+            sc[u] = x;
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1)   // sums over the group's 16 lanes
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
+        float mn = m;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (kbase + g + 8 * u >= k1) sc[u] = -INFINITY;
+            mn = fmaxf(mn, sc[u]);
+        }
+        if (mn != -INFINITY) {
+            const float corr = exp2f(m - mn);   // m = -inf before the first key: 0
+            l *= corr;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] *= corr;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (sc[u] == -INFINITY) continue;   // past the chunk's end: the row is not read
+                const float pr = exp2f(sc[u] - mn);
+                float vf[8];
+                Vec8<bf16>::load(reinterpret_cast<const bf16*>(dt_addr(vt, g + 8 * u, lane)), vf);
+                l += pr;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = fmaf(pr, vf[e], o[e]);
+            }
+            m = mn;
+        }
+        __syncthreads();   // every thread is done with this stage
+        if (threadIdx.x == 0 && i + DT_ST < ntile) {
+            tc::fence_async_smem();
+            issue(i + DT_ST);
+        }
+    }
+    // merge the groups
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s_o[g][lane * 8 + e] = o[e];
+    if (lane == 0) { s_m[g] = m; s_l[g] = l; }
+    __syncthreads();
+    float mm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < DA_GROUPS; ++i) mm = fmaxf(mm, s_m[i]);
+    const int dim = threadIdx.x;   // DA_THREADS == DA_HD
+    float acc = 0.f, ll = 0.f;
+#pragma unroll
+    for (int i = 0; i < DA_GROUPS; ++i) {
+        const float w = s_m[i] == -INFINITY ? 0.f : exp2f(s_m[i] - mm);
+        acc = fmaf(s_o[i][dim], w, acc);
+        ll = fmaf(s_l[i], w, ll);
+    }
+    const long pc = ((long)b * H + h) * nchunk + chunk;
+    part_o[pc * DA_HD + dim] = acc;
+    if (dim == 0) part_ml[pc] = make_float2(mm, ll);
+}
+
 // out[b][h*128 + dim] = sum_c o_c 2^(m_c - M) / sum_c l_c 2^(m_c - M); zero rows b >= B
 template <typename T>
 __global__ void __launch_bounds__(DA_HD) decode_combine_kernel(const float* part_o, const float2* part_ml,
@@ -377,8 +510,23 @@ int decode_attention(const T* q, const T* kc, const T* vc, int B, int Bp, int d,
     if (decode_attention_ws_bytes(B, H, cache_T) > ws_bytes) return set_error(NC_ERR_ARG, "decode attention workspace");
     float* po = reinterpret_cast<float*>(ws);
     float2* pml = reinterpret_cast<float2*>(reinterpret_cast<char*>(ws) + (((size_t)parts * DA_HD * 4 + 255) & ~(size_t)255));
-    decode_attn_kernel<T><<<dim3(nchunk, H, B), DA_THREADS, 0, s>>>(q, kc, vc, d, cache_T, n, pos_dev, kch,
-                                                                   1.0f / sqrtf((float)Dh), po, pml);
+    if constexpr (sizeof(T) == 2) {
+        // bf16: the cache rows come in by TMA (d and the cache base allow the copies)
+        static DeviceOnce init;
+        NC_TRY(init.run([] {
+            return cuda_check(cudaFuncSetAttribute(decode_attn_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   DT_SMEM), "decode attention smem attribute");
+        }));
+        CUtensorMap mk, mv;
+        const long rows = (long)B * cache_T;   // the sequences in use (rows past them read as zeros)
+        NC_TRY(make_map(&mk, kc, d, rows, 1, d, 0, 64, DT_KEYS));
+        NC_TRY(make_map(&mv, vc, d, rows, 1, d, 0, 64, DT_KEYS));
+        decode_attn_tma_kernel<<<dim3(nchunk, H, B), DA_THREADS, DT_SMEM, s>>>(
+            mk, mv, q, d, cache_T, n, pos_dev, kch, 1.0f / sqrtf((float)Dh), po, pml);
+    } else {
+        decode_attn_kernel<T><<<dim3(nchunk, H, B), DA_THREADS, 0, s>>>(q, kc, vc, d, cache_T, n, pos_dev, kch,
+                                                                       1.0f / sqrtf((float)Dh), po, pml);
+    }
     decode_combine_kernel<T><<<dim3(H, Bp), DA_HD, 0, s>>>(po, pml, nchunk, B, d, out);
     note_launch(2);
     NC_LAUNCH_CHECK("decode_attention");
