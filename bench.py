@@ -558,12 +558,15 @@ def decode_workload(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    if T0 + args.warmup + 3 * args.steps + 3 > cT:
+    # the first four steps record the two alternating buffer pairs' CUDA graphs (a step is
+    # recorded on its second use); they run before the W warm-up steps, untimed
+    REC = 4
+    if T0 + REC + args.warmup + 3 * args.steps + 3 > cT:
         raise SystemExit("decode: prompt + steps exceed the cache")
     prompt, _ = synth.zipf_rows(B, T0, V, seed=replicas.data_seed(rank) + 200)
     m = Model(L_, d, w["n_head"], V, B, cT, dtype="bf16", seed=0, device=dev)
     cache = m.kv_cache(B, cT)
-    toks = torch.zeros(1 + args.warmup + 2 * args.steps + 1, B, dtype=torch.int32, device=dev)
+    toks = torch.zeros(1 + REC + args.warmup + 2 * args.steps + 1, B, dtype=torch.int32, device=dev)
     p_d = torch.from_numpy(prompt.reshape(-1)).to(dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -587,7 +590,7 @@ def decode_workload(args):
     def dstep(i):
         m.decode_step(cache, buf[i % 2], B, T0 + i, next_tok=buf[(i + 1) % 2])
 
-    for i in range(args.warmup):
+    for i in range(REC + args.warmup):
         dstep(i)
     barrier()
     clocks = Clocks(gpu_id_for(torch, dev))
@@ -595,7 +598,7 @@ def decode_workload(args):
     launches0 = L.nc_launch_count()
     barrier()
     e0.record(stream)
-    for i in range(args.warmup, args.warmup + args.steps):
+    for i in range(REC + args.warmup, REC + args.warmup + args.steps):
         dstep(i)
     e1.record(stream)
     barrier()
@@ -603,18 +606,18 @@ def decode_workload(args):
     clk = clocks.stop()
     ms = replicas.max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
     pk = peaks()
-    i0 = args.warmup + args.steps
+    i0 = REC + args.warmup + args.steps
     n_prof = profiled_pass(L, m, lambda i: dstep(i0 + i), args.steps, barrier)   # (direct launches)
     kernels = kernel_table(L, m, n_prof, pk)
     flag = m.check_flag()
     # algorithmic bytes of one decode step: every weight once, the cache read up to the
     # step's position (mean over the timed steps) and the new k, v written
-    n_mean = T0 + args.warmup + (args.steps + 1) / 2.0
+    n_mean = T0 + REC + args.warmup + (args.steps + 1) / 2.0
     wbytes = (12 * d * d * L_ + V * d) * 2
     kvbytes = 2 * L_ * B * n_mean * d * 2 + 2 * L_ * B * d * 2
     achieved = (wbytes + kvbytes) / (ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": "the decode step (weights by the swapped tcgen05 GEMMs, cache by "
-                "decode_attn_kernel)", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "the TMA-fed decode attention)", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
                 "frac": achieved / pk["hbm"], "peak_kind": f"copy bandwidth ({pk['source']})",
                 "traffic": None, "bytes_per_step": wbytes + kvbytes}
     # end to end: this step's tokens from pinned host memory in, the next tokens out
@@ -630,7 +633,7 @@ def decode_workload(args):
         stream.synchronize()
         tok_h.copy_(nxt_h)
 
-    base = T0 + args.warmup + 2 * args.steps    # (every position up to here has been written)
+    base = T0 + REC + args.warmup + 2 * args.steps    # (every position up to here has been written)
     host_step(base)
     host_step(base)
     barrier()
@@ -645,6 +648,7 @@ def decode_workload(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
         "prefill": {"ms": prefill_ms, "tokens_per_s": B * T0 / (prefill_ms * 1e-3)},
+        "graph_recording_steps": REC,
         "device_flag": flag, "gpu_launches": int(launches), "roofline": roofline, "kernels": kernels,
         "e2e": {"value": replicas.job_rate(world, B, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": B * 4,
                 "d2h_bytes_per_step": B * 4, "ms_per_step": 1000 * e2e_s},
@@ -668,15 +672,21 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="d20", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batch", type=int, default=32, help="batch of the attn workload")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="batch: of the attn / gemm workloads (default 32), or the micro-batch rows of a "
+                         "training workload (a smaller case than the named configuration, for profiling)")
     args = ap.parse_args()
     if args.workload in ("attn", "optim", "gemm"):
+        if args.batch is None:
+            args.batch = 32
         return kernel_workload(args)
     if args.workload == "eval":
         return eval_workload(args)
     if args.workload == "decode":
         return decode_workload(args)
-    w = WORKLOADS[args.workload]
+    w = dict(WORKLOADS[args.workload])
+    if args.batch is not None:
+        w["B"] = args.batch
     from pretraining_step_03_b300 import replicas
     rank, world, local = replicas.rank_env()
     tokens_per_step = w["B"] * w["T"] * w["n_micro"]
