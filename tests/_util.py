@@ -27,7 +27,7 @@ def bf16_round(x):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).to(torch.float32).numpy()
 
 
-def ns_bf16_model(g, steps=5, coefs=(3.4445, -4.7750, 2.0315)):
+def ns_bf16_model(g, steps=5, coefs=(3.4445, -4.7750, 2.0315), store_bf16=True):
     """Newton-Schulz with bf16 storage: a model of where the bf16 kernels round.
 
     Not the oracle (that is oracle.newton_schulz, fp64): this rounds to bf16
@@ -47,7 +47,7 @@ def ns_bf16_model(g, steps=5, coefs=(3.4445, -4.7750, 2.0315)):
     t = torch.from_numpy(np.ascontiguousarray(x.T if tall else x))
 
     def r(v):
-        return v.to(torch.bfloat16).to(torch.float32)
+        return v.to(torch.bfloat16).to(torch.float32) if store_bf16 else v
 
     t = r(t)
     for _ in range(steps):
@@ -58,7 +58,7 @@ def ns_bf16_model(g, steps=5, coefs=(3.4445, -4.7750, 2.0315)):
     return out.T if tall else out
 
 
-def muon_update_cos_min(geff, x_ref, cap=0.999):
+def muon_update_cos_min(geff, x_ref, cap=0.999, cos=None):
     """Smallest cosine accepted between a bf16 Muon update and the fp64 one.
 
     cap (0.999) wherever bf16 storage allows it; where the input's spectrum
@@ -66,5 +66,7 @@ def muon_update_cos_min(geff, x_ref, cap=0.999):
     ~0.9995), the bound is 1 - 2 (1 - c_model): the kernel's rounding has the
     model's size, and the factor 2 leaves room for its other summation order.
     """
+    if cos is not None and cos >= cap:   # the cap holds: no need for the model
+        return cap, None
     cm, _ = cmp(ns_bf16_model(geff), x_ref)
     return min(cap, 1.0 - 2.0 * (1.0 - cm)), cm

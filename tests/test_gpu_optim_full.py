@@ -35,7 +35,7 @@ def _muon_update_checks(prev, got, xref, geff, what):
     r, c = got.shape
     x = (prev - got) / (HP["muon_lr"] * np.sqrt(max(1.0, r / c)))
     cos, _ = cmp(x, xref)
-    cmin, cmodel = muon_update_cos_min(geff, xref)
+    cmin, cmodel = muon_update_cos_min(geff, xref, cos=cos)
     assert cos >= cmin, f"{what}: Muon update cos {cos} (min {cmin}, bf16 storage model {cmodel})"
     u, sv, vt = np.linalg.svd(xref, full_matrices=False)
     proj = np.einsum("ki,kl,il->i", u, x, vt)

@@ -120,7 +120,7 @@ def test_tiny_optimizer_step_given_gradients(mode, inputs):
                 cos, _ = cmp(x, xref[i])
                 if tol["dcos"] is None:   # bf16: the bound bf16 storage allows on this spectrum
                     geff = grads[i] + HP["momentum"] * buf[i]
-                    cmin, cmodel = muon_update_cos_min(geff, xref[i])
+                    cmin, cmodel = muon_update_cos_min(geff, xref[i], cos=cos)
                 else:
                     cmin, cmodel = tol["dcos"], None
                 assert cos >= cmin, f"{mode} step {step} Muon update {i}: cos {cos} (min {cmin}, model {cmodel})"
