@@ -276,6 +276,26 @@ __device__ __forceinline__ void x_issue(XPipe& x, const CUtensorMap* m, int n0, 
     }
 }
 
+// The tile this epilogue warp handles next.  A warp's aux blocks are fetched in one
+// sequence, this tile's chunks and then the next tile's, keeping the ring full: so the
+// next tile's first blocks come in while this tile's last chunks are processed, instead
+// of being waited for at the start of the next epilogue.
+struct NextTile {
+    bool on;       // there is a next tile and the aux matrix comes by TMA
+    int tn, row, b;
+    int next;      // index in that sequence of the next block to fetch (this tile: 0 .. n-1)
+};
+
+// A ring slot has just been freed: fetch the next block of the sequence, if any.
+__device__ __forceinline__ void x_ahead(XPipe& x, const CUtensorMap* m, int cstart, int cend, int BN, int tn,
+                                        int row, int b, NextTile& nt) {
+    const int lane = threadIdx.x & 31, n = cend - cstart, j = nt.next;
+    if (j < n) x_issue(x, m, tn * BN + (cstart + j) * 32, row - lane, b);
+    else if (nt.on && j - n < n) x_issue(x, m, nt.tn * BN + (cstart + j - n) * 32, nt.row - lane, nt.b);
+    else return;
+    nt.next = j + 1;
+}
+
 // The oldest outstanding block, once it has landed (null if the CTA aborted).
 __device__ __forceinline__ uint8_t* x_wait(XPipe& x, volatile int* abort) {
     const int k = (x.st >> 2) & 3;
@@ -460,7 +480,8 @@ constexpr int epi_family(int epi) {
 template <int BN, bool MIRROR, int EF = EF_ANY>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int split, int row, int tn,
                                               uint32_t tbase, int g, uint8_t* stg, XPipe& x,
-                                              const CUtensorMap* mx, volatile int* abort, bool mirror) {
+                                              const CUtensorMap* mx, volatile int* abort, bool mirror,
+                                              NextTile& nt) {
     const int lane = threadIdx.x & 31;
     const bool rows_ok = __all_sync(0xffffffffu, row < p.M);
     const int cend = (g + 1) * (BN / 64);
@@ -587,7 +608,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
                     dot = 0.f;
                 }
             }
-            if (p.aux_tma && c + x.slots() < cend) x_issue(x, mx, n0 + 32 * x.slots(), row - lane, b);
+            if (p.aux_tma) x_ahead(x, mx, g * (BN / 64), cend, BN, tn, row, b, nt);
         }
     } else
 #pragma unroll 1
@@ -610,7 +631,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
             if (mirror && n0 < p.N)   // symmetric C: the transposed copy of this chunk (warp-uniform)
                 mirror32(p, xb ? const_cast<uint8_t*>(xb) : stg, b, row, n0, v, rows_ok && n0 + 32 <= p.N);
         }
-        if (p.aux_tma && c + x.slots() < cend) x_issue(x, mx, n0 + 32 * x.slots(), row - lane, b);
+        if (p.aux_tma) x_ahead(x, mx, g * (BN / 64), cend, BN, tn, row, b, nt);
     }
 }
 
@@ -747,17 +768,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         XPipe x = x_make(epi_smem + (warp - 2) * EPI_STG, xbar + XSLOTS_MAX * (warp - 2), xf32);
         int acc = 0;
         uint32_t aph = 0;
+        int carried = 0;   // aux blocks of this tile fetched during the last epilogue
         for (long u = blockIdx.x; u < p.units; u += gridDim.x) {
             int b, split, tm, tn;
             decode(p, u, b, split, tm, tn);
             const int row = tm * BM + q * 32 + lane;
-            if (p.aux_tma)   // this tile's first blocks come in while its MMAs run
-                for (int k = 0; k < x.slots() && k < BN / 64; ++k)
-                    x_issue(x, &tmX, tn * BN + g * (BN / 2) + 32 * k, row - lane, b);
+            NextTile nt{false, 0, 0, 0, 0};
+            if (p.aux_tma && u + gridDim.x < p.units) {
+                int s2, tm2;
+                decode(p, u + gridDim.x, nt.b, s2, tm2, nt.tn);
+                nt.row = tm2 * BM + q * 32 + lane;
+                nt.on = true;
+            }
+            if (p.aux_tma) {   // this tile's first blocks come in while its MMAs run
+                const int first = min(x.slots(), BN / 64);
+                for (int k = carried; k < first; ++k) x_issue(x, &tmX, tn * BN + g * (BN / 2) + 32 * k, row - lane, b);
+                nt.next = max(carried, first);
+            }
             if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            epilogue_tile<BN, false>(p, b, split, row, tn, tbase, g, x.bufp(0), x, &tmX, abort_flag, false);
+            epilogue_tile<BN, false>(p, b, split, row, tn, tbase, g, x.bufp(0), x, &tmX, abort_flag, false, nt);
+            carried = max(0, nt.next - BN / 64);
             tc::fence_before();
             tc::mbar_arrive(&tempty[acc]);
             acc ^= 1;
@@ -915,18 +947,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t tempty_leader = tc::mapa(tc::smem_u32(&tempty[0]), 0);
         int acc = 0;
         uint32_t aph = 0;
+        int carried = 0;   // aux blocks of this tile fetched during the last epilogue
         for (long u = cluster; u < p.units; u += nclusters) {
             int b, split, tm, tn;
             decode(p, u, b, split, tm, tn);
             const int row = tm * 256 + (int)rank * 128 + q * 32 + lane;
-            if (p.aux_tma)   // this tile's first blocks come in while its MMAs run
-                for (int k = 0; k < x.slots() && k < P_BN / 64; ++k)
+            NextTile nt{false, 0, 0, 0, 0};
+            if (p.aux_tma && u + nclusters < p.units) {
+                int s2, tm2;
+                decode(p, u + nclusters, nt.b, s2, tm2, nt.tn);
+                nt.row = tm2 * 256 + (int)rank * 128 + q * 32 + lane;
+                nt.on = true;
+            }
+            if (p.aux_tma) {   // this tile's first blocks come in while its MMAs run
+                const int first = min(x.slots(), P_BN / 64);
+                for (int k = carried; k < first; ++k)
                     x_issue(x, &tmX, tn * P_BN + g * (P_BN / 2) + 32 * k, row - lane, b);
+                nt.next = max(carried, first);
+            }
             if (!tc::mbar_wait_warp(&tfull[acc], aph, abort_flag)) break;
             tc::fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * P_BN);
             epilogue_tile<P_BN, SYM, EF>(p, b, split, row, tn, tbase, g, x.bufp(0), x, &tmX, abort_flag,
-                                     SYM && tm != tn);
+                                     SYM && tm != tn, nt);
+            carried = max(0, nt.next - P_BN / 64);
             tc::fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(tempty_leader + acc * 8);
