@@ -67,6 +67,8 @@ struct nc_model {
     float* g;          // residual gradient fp32 [M, d]
     void* gT;          // its act-type copy (bf16 mode)
     void* dy;          // gradient at a norm output [M, d] (act type)
+    float* nb_dot;     // bf16 mode: <dlogits, logits> per row [M] (the final norm's row dot)
+    float* nb_part;    // bf16 mode: <dh, relu(h)> per row and 128 columns [M, 4d/128]
     void* dqkv;
     void* dO;
     void* dh;
@@ -172,6 +174,8 @@ void layout(nc_model* m, char* base, size_t* total) {
         m->g = (float*)c.take(M * d * 4);
         m->gT = m->dtype == NC_BF16 ? c.take(M * d * act) : nullptr;
         m->dy = c.take(M * d * act);
+        m->nb_dot = m->dtype == NC_BF16 ? (float*)c.take(M * 4) : nullptr;
+        m->nb_part = m->dtype == NC_BF16 ? (float*)c.take(M * ceil_div(4 * d, 128) * 4) : nullptr;
         m->dqkv = c.take(M * 3 * d * act);
         m->dO = c.take(M * d * act);
         m->dh = c.take(M * 4 * d * act);
@@ -287,6 +291,21 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
         Prof pr(m, NC_PROF_NORM, 0, Md * (ab + ab + (gin ? 4 : 0) + 4 + (gT ? ab : 0)) + M * 4.0);
         return rmsnorm_backward<T>((const T*)m->dy, (T*)y, r, gin, m->g, gT, M, d, s);
     };
+    // dy = (the product g0) and then the norm's backward; in bf16 mode, given each row's
+    // <dy, y> as partials (part, nparts per row), the product's epilogue finishes the norm
+    // and dy is never stored
+    auto dx_norm_b = [&](Gemm g0, void* y, float* r, const float* gin, const float* part, int nparts) {
+        if (part && gT) {
+            Gemm g = g0;
+            g.epi = EPI_NORMB; g.C = m->g; g.ldc = d; g.c_dtype = NC_FP32;
+            g.aux = y; g.ldaux = d; g.aux_dtype = act;
+            g.nb_r = r; g.nb_part = part; g.nb_nparts = nparts; g.nb_inv_d = 1.f / (float)d;
+            g.nb_gin = gin; g.nb_gt = (bf16*)gT;
+            if (gemm_tc_supported(g)) return run_gemm(m, g);
+        }
+        NC_TRY(run_gemm(m, g0));
+        return norm_b(y, r, gin);
+    };
     auto rope = [&](void* qkv, float sign) {
         Prof pr(m, NC_PROF_ROPE, 0, 4.0 * Md * ab);
         return rope_apply<T>((T*)qkv, 3 * d, M, T_, H, Dh, m->rope, rope_ld, sign, s);
@@ -349,7 +368,7 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
                                          : (lse_part ? M * (V / 128) * 8.0 : (double)M * V * ab);
         Prof pr(m, NC_PROF_CE, 0, ce_bytes + M * 16.0);
         NC_TRY(cross_entropy<T>((T*)m->logits, tgt, m->nll, M, V, grad_scale / (float)M, m->flag, s,
-                                lse_part, backward));
+                                lse_part, backward, m->nb_dot));
         NC_TRY(loss_reduce(m->nll, tgt, tb, M, V, out, m->flag, s, sums, sum_acc));
     }
     if (!backward) return NC_OK;
@@ -357,21 +376,27 @@ int forward_backward(nc_model* m, const int32_t* tok, const int32_t* tgt, const 
     // ------------------------------------------------ backward
     float* G = m->grads;
     NC_TRY(weight_grad(m, G + m->poff[iu], V, d, m->logits, V, m->yf, d, M, accumulate));
-    NC_TRY(run_gemm(m, mk(m, M, d, V, m->logits, V, false, W<T>(m, iu), d, true, m->dy, d, act)));
-    NC_TRY(norm_b(m->yf, m->rf, nullptr));
+    NC_TRY(dx_norm_b(mk(m, M, d, V, m->logits, V, false, W<T>(m, iu), d, true, m->dy, d, act), m->yf, m->rf,
+                     nullptr, m->nb_dot, 1));
     for (int l = m->depth - 1; l >= 0; --l) {
         auto& Ly = m->L[l];
         const int b0 = 1 + 6 * l;
         // MLP block
         NC_TRY(weight_grad(m, G + m->poff[b0 + 5], d, F, gop, d, Ly.a, F, M, accumulate));
-        {   // dh = (g W2) * 2 relu(h)
+        bool dots = false;
+        {   // dh = (g W2) * 2 relu(h); in bf16 mode also <dh, relu(h)> per row and 128 columns
             Gemm g = mk(m, M, F, d, gop, d, false, W<T>(m, b0 + 5), F, true, m->dh, F, act);
             g.epi = EPI_RELU2_BWD; g.aux = Ly.a; g.ldaux = F; g.aux_dtype = act;
+            if (m->nb_part) {
+                g.dot_out = m->nb_part;
+                dots = gemm_tc_supported(g);
+                if (!dots) g.dot_out = nullptr;
+            }
             NC_TRY(run_gemm(m, g));
         }
         NC_TRY(weight_grad(m, G + m->poff[b0 + 4], F, d, m->dh, F, Ly.y2, d, M, accumulate));
-        NC_TRY(run_gemm(m, mk(m, M, d, F, m->dh, F, false, W<T>(m, b0 + 4), d, true, m->dy, d, act)));
-        NC_TRY(norm_b(Ly.y2, Ly.r2, m->g));
+        NC_TRY(dx_norm_b(mk(m, M, d, F, m->dh, F, false, W<T>(m, b0 + 4), d, true, m->dy, d, act), Ly.y2, Ly.r2,
+                         m->g, dots ? m->nb_part : nullptr, F / 128));
         // attention block
         NC_TRY(weight_grad(m, G + m->poff[b0 + 3], d, d, gop, d, Ly.o, d, M, accumulate));
         {   // dO = g Wo; with head dim 128 the epilogue also leaves D_t = dO_t . O_t per head

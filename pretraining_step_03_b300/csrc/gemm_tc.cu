@@ -58,6 +58,13 @@ struct TcParams {
     int aux_tma;      // the auxiliary matrix comes through the per-warp TMA buffers
     int sym;          // symmetric C: upper-triangle tiles only, mirrored (tiles_m == tiles_n)
     float2* lse_part; // EPI_LSE: [M][N/128] (max, sum exp) partials
+    float* dot_out;       // EPI_RELU2_BWD: [M][N/128] <dh, relu(h)> partials (may be null)
+    const float* nb_r;    // EPI_NORMB: rstd [M], row-dot partials [M][nb_nparts], 1/d,
+    const float* nb_part; //   residual gradient in (fp32, C's layout; may alias C), bf16 copy out
+    int nb_nparts;
+    float nb_inv_d;
+    const float* nb_gin;
+    bf16* nb_gt;
 };
 
 template <int BN> struct Cfg {
@@ -240,6 +247,26 @@ __device__ __forceinline__ void st16_bf16(bf16* dst, const float* v) {
         }
         reinterpret_cast<uint4*>(dst)[c] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+}
+
+// fp32 rows out through a 2 KB staging block, 16 columns at a time (64-byte rows laid
+// out as the bf16 blocks above): lane i's 16 values of row r0 + i, rows ld elements
+// apart, lane 0's first element at off0.
+__device__ __forceinline__ void wst16_f32(uint8_t* stg, float* base, long off0, long ld, const float* v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<float4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+            make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    __syncwarp();
+    float* out = base + off0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 8 * i + (lane >> 2), c = lane & 3;
+        *reinterpret_cast<float4*>(out + (long)r * ld + 4 * c) =
+            *reinterpret_cast<const float4*>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+    }
+    __syncwarp();
 }
 
 // The auxiliary-matrix pipeline of one epilogue warp: 32 x 32 blocks come in by TMA
@@ -470,9 +497,12 @@ __device__ __forceinline__ void mirror32(const TcParams& p, uint8_t* stg, int b,
 // once a chunk is done, the block x.slots chunks ahead goes into its slot.
 // Epilogue families a kernel instance is compiled for (each instance carries only its
 // own epilogue code, which keeps the register budget of the others).
-enum EpiFamily { EF_ANY = 0, EF_GEN = 1, EF_ROPE = 2, EF_DELTA = 3, EF_LSE = 4 };
-constexpr int epi_family(int epi) {
-    return epi == EPI_ROPE ? EF_ROPE : epi == EPI_DELTA ? EF_DELTA : epi == EPI_LSE ? EF_LSE : EF_GEN;
+// The RMSNorm-backward pair: EF_DOT, the dh product that also leaves the row dots
+// (EPI_RELU2_BWD with dot_out), and EF_NB, the dX product that finishes the norm (EPI_NORMB).
+enum EpiFamily { EF_ANY = 0, EF_GEN = 1, EF_ROPE = 2, EF_DELTA = 3, EF_LSE = 4, EF_NB = 5, EF_DOT = 6 };
+constexpr int epi_family(int epi, bool dot_out = false) {
+    return epi == EPI_ROPE ? EF_ROPE : epi == EPI_DELTA ? EF_DELTA : epi == EPI_LSE ? EF_LSE
+         : epi == EPI_NORMB ? EF_NB : (epi == EPI_RELU2_BWD && dot_out) ? EF_DOT : EF_GEN;
 }
 
 // MIRROR (compile time, symmetric products only): also write the transposed copy of
@@ -610,7 +640,111 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
             }
             if (p.aux_tma) x_ahead(x, mx, g * (BN / 64), cend, BN, tn, row, b, nt);
         }
-    } else
+    } else if (EF == EF_NB) {
+        // RMSNorm backward, dy = alpha acc never stored: this row's D = <dy, y> from the
+        // partials its producers left, then per chunk g = gin + r (dy - y D / d) in fp32
+        // and its bf16 copy.  N is a multiple of 128, so a chunk is whole or absent.  The
+        // residual gradient in (fp32, read per lane) is fetched one chunk ahead.
+        const bool live = row < p.M;
+        float rr = 0.f, dm = 0.f;
+        if (live) {
+            rr = p.nb_r[row];
+            const float* pp = p.nb_part + (long)row * p.nb_nparts;
+            float sd = 0.f;
+            if ((p.nb_nparts & 3) == 0) {
+#pragma unroll 4
+                for (int k = 0; k < p.nb_nparts; k += 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(pp + k);
+                    sd = (((sd + f.x) + f.y) + f.z) + f.w;
+                }
+            } else {
+                for (int k = 0; k < p.nb_nparts; ++k) sd += pp[k];
+            }
+            dm = sd * p.nb_inv_d;
+        }
+        float* C = reinterpret_cast<float*>(p.C);
+        const int cstart = g * (BN / 64);
+        float gi[32];
+        auto fetch_gin = [&](int c) {
+            const int n0 = tn * BN + c * 32;
+            if (p.nb_gin && live && n0 < p.N) ld32(p.nb_gin, (long)row * p.ldc + n0, NC_FP32, gi);
+            else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gi[j] = 0.f;
+            }
+        };
+        fetch_gin(cstart);
+#pragma unroll 1
+        for (int c = cstart; c < cend; ++c) {
+            float v[32];
+            tc::tmem_ld32(tbase + c * 32, reinterpret_cast<uint32_t*>(v));
+            tc::tmem_wait_ld();
+            const int n0 = tn * BN + c * 32;
+            const uint8_t* xb = nullptr;
+            {
+                float y[32];
+                if (p.aux_tma) {
+                    if (!(xb = x_wait(x, abort))) break;
+                    x_row(xb, NC_BF16, y);
+                } else if (live && n0 < p.N) {
+                    ld32(p.aux, (long)row * p.ldaux + n0, NC_BF16, y);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[j] = 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = gi[j] + rr * (p.alpha * v[j] - y[j] * dm);
+            }
+            if (c + 1 < cend) fetch_gin(c + 1);
+            if (n0 < p.N) {   // warp-uniform
+                const long ci = (long)row * p.ldc + n0;
+                if (rows_ok) {
+                    uint8_t* sb = xb ? const_cast<uint8_t*>(xb) : stg;
+                    const long c0 = ci - (long)lane * p.ldc;
+                    wst16_f32(sb, C, c0, p.ldc, v);
+                    wst16_f32(sb, C, c0 + 16, p.ldc, v + 16);
+                    wst32(sb, p.nb_gt, c0, p.ldc, NC_BF16, v);
+                } else if (live) {
+                    st32(C, ci, NC_FP32, v);
+                    st32(p.nb_gt, ci, NC_BF16, v);
+                }
+            }
+            if (p.aux_tma) x_ahead(x, mx, g * (BN / 64), cend, BN, tn, row, b, nt);
+        }
+    } else if (EF == EF_DOT) {
+        // dh = alpha acc * 2 relu(h) = alpha acc * 2 sqrt(a), and per 128-column group the
+        // row dot <dh, relu(h)> over the stored (rounded) dh: the dot product <dy, y> the
+        // RMSNorm backward after the next product needs (dy = dh W1, h = W1 y)
+        float dot = 0.f;
+#pragma unroll 1
+        for (int c = g * (BN / 64); c < cend; ++c) {
+            float v[32];
+            tc::tmem_ld32(tbase + c * 32, reinterpret_cast<uint32_t*>(v));
+            tc::tmem_wait_ld();
+            const int n0 = tn * BN + c * 32;
+            const uint8_t* xb = nullptr;
+            float a[32];
+            if (p.aux_tma) {
+                if (!(xb = x_wait(x, abort))) break;
+                x_row(xb, NC_BF16, a);
+            }
+            if (n0 < p.N) {   // warp-uniform
+                const long ci = (long)row * p.ldc + n0;
+                if (!xb && row < p.M) ld32(p.aux, (long)row * p.ldaux + n0, NC_BF16, a);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float sq = a[j] > 0.f ? a[j] * rsqrtf(a[j]) : 0.f;
+                    v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * p.alpha * (2.f * sq)));
+                    dot = fmaf(v[j], sq, dot);
+                }
+                if (rows_ok) wst32(xb ? const_cast<uint8_t*>(xb) : stg, p.C, ci - (long)lane * p.ldc, p.ldc, NC_BF16, v);
+                else if (row < p.M) st32(p.C, ci, NC_BF16, v);
+            }
+            if (p.aux_tma) x_ahead(x, mx, g * (BN / 64), cend, BN, tn, row, b, nt);
+        }
+        const int grp = (tn * BN + g * (BN / 2)) / 128;
+        if (row < p.M && grp * 128 < p.N) p.dot_out[(long)row * (p.N / 128) + grp] = dot;
+    } else if (EF != EF_NB && EF != EF_DOT)
 #pragma unroll 1
     for (int c = g * (BN / 64); c < (g + 1) * (BN / 64); ++c) {
         float v[32];
@@ -1226,6 +1360,16 @@ bool gemm_tc_supported(const Gemm& g) {
     if (g.epi == EPI_DELTA && (g.N % 128 || g.N < 256 || !g.delta || !g.aux || g.rope_T <= 0 || g.c_dtype != NC_BF16 ||
                                g.aux_dtype != NC_BF16 || g.batch != 1))
         return false;
+    // the RMSNorm-backward pair: CTA-pair tiles (two 128-column groups per tile), A K-major,
+    // B MN-major (the dX and dh products of the backward), one matrix
+    const bool nb_shape = g.M >= 256 && g.N >= 256 && g.N % 128 == 0 && !g.a_t && g.b_t && g.batch == 1;
+    if (g.dot_out && (g.epi != EPI_RELU2_BWD || !nb_shape || !g.aux || g.aux_dtype != NC_BF16 ||
+                      g.c_dtype != NC_BF16))
+        return false;
+    if (g.epi == EPI_NORMB &&
+        (!nb_shape || !g.aux || g.aux_dtype != NC_BF16 || g.c_dtype != NC_FP32 || !g.nb_r || !g.nb_part ||
+         g.nb_nparts <= 0 || !g.nb_gt || (uintptr_t)g.nb_gt % 16 || (uintptr_t)g.nb_gin % 16))
+        return false;
     return true;
 }
 
@@ -1269,12 +1413,15 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
     p.flag = g.flag;
     p.rope = g.rope; p.rope_T = g.rope_T; p.rope_cols = g.rope_cols; p.rope_ld = g.rope_ld; p.delta = g.delta;
     p.lse_part = g.lse_part;
+    p.dot_out = g.dot_out;
+    p.nb_r = g.nb_r; p.nb_part = g.nb_part; p.nb_nparts = g.nb_nparts; p.nb_inv_d = g.nb_inv_d;
+    p.nb_gin = g.nb_gin; p.nb_gt = g.nb_gt;
 
     // the auxiliary matrix by TMA (32 x 32 blocks, 128 / 64-byte swizzle) when the
     // epilogue reads one and its layout allows the copy
     CUtensorMap ma, mb, mx;
     const bool reads_aux = (g.epi == EPI_STORE && g.aux && g.beta != 0.f) || g.epi == EPI_RELU2_BWD ||
-                           g.epi == EPI_DELTA;
+                           g.epi == EPI_DELTA || g.epi == EPI_NORMB;
     const int xes = g.aux_dtype == NC_FP32 ? 4 : 2;
     if (reads_aux && p.splits == 1 && (g.ldaux * xes) % 16 == 0 && (g.batch <= 1 || (g.sAux * xes) % 16 == 0)) {
         NC_TRY(make_map_x(&mx, g.aux, g.aux_dtype, g.N, g.M, g.batch, g.ldaux, g.sAux));
@@ -1288,12 +1435,14 @@ int gemm_tc(const Gemm& g, void* ws, size_t ws_bytes, cudaStream_t s) {
 
     int rc;
     if (pair) {
-        const int ef = epi_family(g.epi);
+        const int ef = epi_family(g.epi, g.dot_out != nullptr);
         if (p.sym && !g.a_t) rc = g.b_t ? launch2<false, true, true>(ma, mb, mx, p, s)
                                         : launch2<false, false, true>(ma, mb, mx, p, s);
         else if (ef == EF_ROPE) rc = launch2<false, false, false, EF_ROPE>(ma, mb, mx, p, s);
         else if (ef == EF_LSE) rc = launch2<false, false, false, EF_LSE>(ma, mb, mx, p, s);
         else if (ef == EF_DELTA) rc = launch2<false, true, false, EF_DELTA>(ma, mb, mx, p, s);
+        else if (ef == EF_NB) rc = launch2<false, true, false, EF_NB>(ma, mb, mx, p, s);
+        else if (ef == EF_DOT) rc = launch2<false, true, false, EF_DOT>(ma, mb, mx, p, s);
         else if (!g.a_t && !g.b_t) rc = launch2<false, false>(ma, mb, mx, p, s);
         else if (!g.a_t && g.b_t) rc = launch2<false, true>(ma, mb, mx, p, s);
         else if (g.a_t && !g.b_t) rc = launch2<true, false>(ma, mb, mx, p, s);

@@ -18,6 +18,9 @@ enum EpiKind {
     EPI_DELTA = 4,      // C = alpha*acc (bf16) and delta[b, h, t] = sum over head h of bf16(C) * aux
     EPI_LSE = 5,        // C = alpha*acc (bf16) and, per row and 128-column group k, lse_part[row][k] =
                         //   (max z, sum exp(z - max)) over the stored (rounded) values z
+    EPI_NORMB = 6,      // the RMSNorm backward finished in the dX product: with dy = alpha*acc,
+                        //   y = aux (bf16), r = nb_r[row], D = sum of nb_part[row][0 .. nb_nparts):
+                        //   C (fp32) = nb_gin + r (dy - y D nb_inv_d), nb_gt = bf16(C)
 };
 
 struct Gemm {
@@ -39,6 +42,16 @@ struct Gemm {
     bool sym = false;
     float2* lse_part = nullptr;    // EPI_LSE: [M][N/128]
     uint32_t* flag = nullptr;      // device flag word for aborted waits (may be null)
+    // EPI_RELU2_BWD (optional): per row and 128-column group k, dot_out[row][k] = sum of
+    // bf16(C) * sqrt(aux), i.e. <dh, relu(h)> (the row dot of the next RMSNorm's backward)
+    float* dot_out = nullptr;
+    // EPI_NORMB (see above); nb_gin may alias C (the residual gradient updated in place)
+    const float* nb_r = nullptr;
+    const float* nb_part = nullptr;
+    int nb_nparts = 0;
+    float nb_inv_d = 0.f;
+    const float* nb_gin = nullptr;
+    bf16* nb_gt = nullptr;
 };
 // Fraction of the 2*M*N*K products gemm_tc executes for g (below 1 for symmetric C).
 double gemm_tc_work_fraction(const Gemm& g);
@@ -70,10 +83,14 @@ int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* tabl
 // logits [M, V] -> dlogits in place; nll [M].  lse_part (bf16 only, optional): the
 // per-row (max, sum exp) partials of every 128-column group, left by the LM-head GEMM
 // (EPI_LSE); with them the logits are read once instead of twice.  grad = false: nll
-// only, the logits are left untouched.
+// only, the logits are left untouched.  zdot (optional, with grad): per row <dz, z> =
+// scale * sum of (softmax - onehot) * logits (dz before its bf16 rounding), the row dot
+// <dy, y> of the final RMSNorm's backward by the adjoint identity
+// <dz W, y> = <dz, y W^T> = <dz, z>.
 template <typename T>
 int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float scale,
-                  uint32_t* flag, cudaStream_t s, const float2* lse_part = nullptr, bool grad = true);
+                  uint32_t* flag, cudaStream_t s, const float2* lse_part = nullptr, bool grad = true,
+                  float* zdot = nullptr);
 // out (optional): {mean nll, bpb of this batch}; sums (optional): device double[3]
 // {sum nll, sum nll over targets with bytes > 0, sum bytes}, set (accumulate = 0) or
 // added to (accumulate = 1).  One CTA, fixed summation order.

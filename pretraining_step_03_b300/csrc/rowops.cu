@@ -148,7 +148,7 @@ __device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
 // z <- scale * (softmax(z) - onehot(target)) in place.
 template <typename T>
 __global__ void __launch_bounds__(CE_THREADS) ce_kernel(T* z, const int32_t* tgt, float* nll, int V,
-                                                        float scale, int grad, uint32_t* flag) {
+                                                        float scale, int grad, uint32_t* flag, float* zdot) {
     __shared__ float sh[32];
     __shared__ float zt_s;
     const long row = blockIdx.x;
@@ -169,10 +169,17 @@ __global__ void __launch_bounds__(CE_THREADS) ce_kernel(T* z, const int32_t* tgt
     __syncthreads();  // zt_s was read before any thread overwrites z
     if (threadIdx.x == 0) nll[row] = ok ? lse - zt_s : 0.f;
     if (!grad) return;   // (loss only: the logits stay as they are)
+    float zd = 0.f;   // sum over the row of (softmax - onehot) * z; times scale: <dz, z>
     for (int j = threadIdx.x; j < V; j += blockDim.x) {
-        float p = expf(to_f<T>(zr[j]) - lse);
+        const float zj = to_f<T>(zr[j]);
+        float p = expf(zj - lse);
         if (j == t) p -= 1.f;
+        zd = fmaf(p, zj, zd);
         zr[j] = from_f<T>(p * scale);
+    }
+    if (zdot) {
+        const float v = block_reduce(zd, sh, false);
+        if (threadIdx.x == 0) zdot[row] = v * scale;
     }
 }
 
@@ -192,7 +199,8 @@ __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s
 }
 
 __global__ void __launch_bounds__(CE2_THREADS) ce_online_kernel(bf16* z, const int32_t* tgt, float* nll,
-                                                                int V, float scale, int grad, uint32_t* flag) {
+                                                                int V, float scale, int grad, uint32_t* flag,
+                                                                float* zdot) {
     __shared__ float shm[32], shs[32];
     __shared__ float zt_s, lse_s;
     const long row = blockIdx.x;
@@ -252,6 +260,7 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_online_kernel(bf16* z, const i
     __syncthreads();   // zt_s was read before any thread overwrites z
     if (!grad) return;   // (loss only: the logits stay as they are)
     const float lsel = lse_s * CE_LOG2E;
+    float zd = 0.f;   // sum over the row of (softmax - onehot) * z; times scale: <dz, z>
 #pragma unroll 4
     for (int k = 0; k < nv; ++k) {
         const int base = (threadIdx.x + k * CE2_THREADS) * 8;
@@ -263,10 +272,15 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_online_kernel(bf16* z, const i
             float p0 = exp2f(fmaf(f.x, CE_LOG2E, -lsel)), p1 = exp2f(fmaf(f.y, CE_LOG2E, -lsel));
             if (base + 2 * e == t) p0 -= 1.f;
             if (base + 2 * e + 1 == t) p1 -= 1.f;
+            zd = fmaf(p0, f.x, fmaf(p1, f.y, zd));
             __nv_bfloat162 h = __floats2bfloat162_rn(p0 * scale, p1 * scale);
             w[e] = *reinterpret_cast<uint32_t*>(&h);
         }
         zr[threadIdx.x + k * CE2_THREADS] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (zdot) {
+        const float v = block_reduce(zd, shm, false);
+        if (threadIdx.x == 0) zdot[row] = v * scale;
     }
 }
 
@@ -275,7 +289,7 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_online_kernel(bf16* z, const i
 // writes dlogits = scale * (softmax - onehot) over the logits in place.
 __global__ void __launch_bounds__(CE2_THREADS) ce_stats_kernel(bf16* z, const float2* part, const int32_t* tgt,
                                                                float* nll, int V, float scale, int grad,
-                                                               uint32_t* flag) {
+                                                               uint32_t* flag, float* zdot) {
     __shared__ float shm[32], shs[32];
     __shared__ float zt_s, lse_s;
     const long row = blockIdx.x;
@@ -317,6 +331,7 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_stats_kernel(bf16* z, const fl
     __syncthreads();   // zt_s was read before any thread overwrites z
     if (!grad) return;   // (loss only: the logits stay as they are)
     const float lsel = lse_s * CE_LOG2E;
+    float zd = 0.f;   // sum over the row of (softmax - onehot) * z; times scale: <dz, z>
 #pragma unroll 4
     for (int k = 0; k < nv; ++k) {
         const int base = (threadIdx.x + k * CE2_THREADS) * 8;
@@ -328,10 +343,15 @@ __global__ void __launch_bounds__(CE2_THREADS) ce_stats_kernel(bf16* z, const fl
             float p0 = exp2f(fmaf(f.x, CE_LOG2E, -lsel)), p1 = exp2f(fmaf(f.y, CE_LOG2E, -lsel));
             if (base + 2 * e == t) p0 -= 1.f;
             if (base + 2 * e + 1 == t) p1 -= 1.f;
+            zd = fmaf(p0, f.x, fmaf(p1, f.y, zd));
             __nv_bfloat162 h = __floats2bfloat162_rn(p0 * scale, p1 * scale);
             w[e] = *reinterpret_cast<uint32_t*>(&h);
         }
         zr[threadIdx.x + k * CE2_THREADS] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (zdot) {
+        const float v = block_reduce(zd, shm, false);
+        if (threadIdx.x == 0) zdot[row] = v * scale;
     }
 }
 
@@ -607,23 +627,24 @@ int rope_apply(T* qkv, long ld, int M, int T_, int H, int Dh, const float2* tabl
 
 template <typename T>
 int cross_entropy(T* logits, const int32_t* tgt, float* nll, int M, int V, float scale,
-                  uint32_t* flag, cudaStream_t s, const float2* lse_part, bool grad) {
+                  uint32_t* flag, cudaStream_t s, const float2* lse_part, bool grad, float* zdot) {
     if (M <= 0) return NC_OK;
     if constexpr (sizeof(T) == 2) {
         if (lse_part && V % (8 * CE2_THREADS) == 0 && V % 128 == 0 && (uintptr_t)logits % 16 == 0) {
-            ce_stats_kernel<<<M, CE2_THREADS, 0, s>>>(logits, lse_part, tgt, nll, V, scale, grad, flag);
+            ce_stats_kernel<<<M, CE2_THREADS, 0, s>>>(logits, lse_part, tgt, nll, V, scale, grad, flag,
+                                                      grad ? zdot : nullptr);
             note_launch();
             NC_LAUNCH_CHECK("cross_entropy");
             return NC_OK;
         }
         if (V % (8 * CE2_THREADS) == 0 && (uintptr_t)logits % 16 == 0) {
-            ce_online_kernel<<<M, CE2_THREADS, 0, s>>>(logits, tgt, nll, V, scale, grad, flag);
+            ce_online_kernel<<<M, CE2_THREADS, 0, s>>>(logits, tgt, nll, V, scale, grad, flag, grad ? zdot : nullptr);
             note_launch();
             NC_LAUNCH_CHECK("cross_entropy");
             return NC_OK;
         }
     }
-    ce_kernel<T><<<M, CE_THREADS, 0, s>>>(logits, tgt, nll, V, scale, grad, flag);
+    ce_kernel<T><<<M, CE_THREADS, 0, s>>>(logits, tgt, nll, V, scale, grad, flag, grad ? zdot : nullptr);
     note_launch();
     NC_LAUNCH_CHECK("cross_entropy");
     return NC_OK;
@@ -695,7 +716,7 @@ int cast_f32_bf16(const float* x, bf16* y, long n, cudaStream_t s) {
                                      T*, int, int, cudaStream_t);                               \
     template int rope_apply<T>(T*, long, int, int, int, int, const float2*, int, float, cudaStream_t); \
     template int cross_entropy<T>(T*, const int32_t*, float*, int, int, float, uint32_t*,       \
-                                  cudaStream_t, const float2*, bool);
+                                  cudaStream_t, const float2*, bool, float*);
 NC_INST(float)
 NC_INST(bf16)
 #undef NC_INST
