@@ -163,6 +163,38 @@ __device__ __forceinline__ void st_elem(void* base, long i, int dt, float v) {
     else reinterpret_cast<bf16*>(base)[i] = __float2bfloat16_rn(v);
 }
 
+// bf16 rows already rounded and packed (word k = columns 2k, 2k+1): the store side of
+// wst32's bf16 path, and the per-lane form.
+__device__ __forceinline__ void wst32_bf16w(uint8_t* stg, void* base, long off0, long ld, const uint32_t* w) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    __syncwarp();
+    bf16* out = reinterpret_cast<bf16*>(base) + off0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 8 * i + (lane >> 2), c = lane & 3;
+        *reinterpret_cast<uint4*>(out + (long)r * ld + 8 * c) =
+            *reinterpret_cast<const uint4*>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+    }
+    __syncwarp();
+}
+__device__ __forceinline__ void st32_bf16w(void* base, long i, const uint32_t* w) {
+    uint4* d = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(base) + i);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) d[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+// Rounds x, y to bf16, packs them (x in the low half) and returns the rounded values.
+__device__ __forceinline__ uint32_t round_pack2(float& x, float& y) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 f = __bfloat1622float2(h);
+    x = f.x;
+    y = f.y;
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Warp-cooperative row I/O.  Lane i holds 32 consecutive columns of row r0 + i
 // (rows ld elements apart, lane 0's first element at off0).  Going through the
 // warp's staging buffer (swizzled by 16-byte chunk, conflict-free), every global
@@ -183,28 +215,16 @@ __device__ __forceinline__ void wst32(uint8_t* stg, void* base, long off0, long 
             *reinterpret_cast<float4*>(out + (long)r * ld + 4 * c) =
                 *reinterpret_cast<const float4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
         }
-    } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * c + 2 * e], v[8 * c + 2 * e + 1]);
-                w[e] = *reinterpret_cast<uint32_t*>(&h);
-            }
-            *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-        }
         __syncwarp();
-        bf16* out = reinterpret_cast<bf16*>(base) + off0;
+    } else {
+        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = 8 * i + (lane >> 2), c = lane & 3;
-            *reinterpret_cast<uint4*>(out + (long)r * ld + 8 * c) =
-                *reinterpret_cast<const uint4*>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+        for (int k = 0; k < 16; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
         }
+        wst32_bf16w(stg, base, off0, ld, w);
     }
-    __syncwarp();
 }
 
 // Pieces of wst32's bf16 path: stage_bf16x16 puts 16 values (columns 16h..16h+15)
@@ -574,8 +594,13 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
             const int n0 = tn * BN + c * 32;
             if (n0 < p.N) {   // warp-uniform
                 float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * p.alpha));
+                for (int j = 0; j < 32; j += 2) {
+                    v[j] *= p.alpha;
+                    v[j + 1] *= p.alpha;
+                    w[j >> 1] = round_pack2(v[j], v[j + 1]);
+                }
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) c4[(j >> 1) & 3] = tc::fmax3(c4[(j >> 1) & 3], v[j], v[j + 1]);
                 const float cm = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
@@ -598,8 +623,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
                     se += x0 + x1;
                 }
                 const long ci = (long)b * p.sC + (long)row * p.ldc + n0;
-                if (rows_ok) wst32(stg, p.C, ci - (long)lane * p.ldc, p.ldc, NC_BF16, v);
-                else if (row < p.M) st32(p.C, ci, NC_BF16, v);
+                if (rows_ok) wst32_bf16w(stg, p.C, ci - (long)lane * p.ldc, p.ldc, w);
+                else if (row < p.M) st32_bf16w(p.C, ci, w);
             }
         }
         const int grp = (tn * BN + g * (BN / 2)) / 128;
@@ -621,16 +646,21 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
                 x_row(xb, NC_BF16, o);
             }
             if (row < p.M && n0 < p.N) {
+                uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * p.alpha));
+                for (int j = 0; j < 32; j += 2) {
+                    v[j] *= p.alpha;
+                    v[j + 1] *= p.alpha;
+                    w[j >> 1] = round_pack2(v[j], v[j + 1]);
+                }
                 const long ci = (long)b * p.sC + (long)row * p.ldc + n0;
                 const long ai = (long)b * p.sAux + (long)row * p.ldaux + n0;
                 {
                     if (!xb) ld32(p.aux, ai, NC_BF16, o);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) dot = fmaf(v[j], o[j], dot);
-                    if (xb && rows_ok) wst32(const_cast<uint8_t*>(xb), p.C, ci - (long)lane * p.ldc, p.ldc, NC_BF16, v);
-                    else st32(p.C, ci, NC_BF16, v);
+                    if (xb && rows_ok) wst32_bf16w(const_cast<uint8_t*>(xb), p.C, ci - (long)lane * p.ldc, p.ldc, w);
+                    else st32_bf16w(p.C, ci, w);
                 }
                 if ((c & 3) == 3) {
                     const int hh = n0 / 128, t = row % p.rope_T, bb = row / p.rope_T;
@@ -731,14 +761,18 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, int b, int spli
             if (n0 < p.N) {   // warp-uniform
                 const long ci = (long)row * p.ldc + n0;
                 if (!xb && row < p.M) ld32(p.aux, (long)row * p.ldaux + n0, NC_BF16, a);
+                uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float sq = a[j] > 0.f ? a[j] * rsqrtf(a[j]) : 0.f;
-                    v[j] = __bfloat162float(__float2bfloat16_rn(v[j] * p.alpha * (2.f * sq)));
-                    dot = fmaf(v[j], sq, dot);
+                for (int j = 0; j < 32; j += 2) {
+                    const float s0 = a[j] > 0.f ? a[j] * rsqrtf(a[j]) : 0.f;
+                    const float s1 = a[j + 1] > 0.f ? a[j + 1] * rsqrtf(a[j + 1]) : 0.f;
+                    float x0 = v[j] * p.alpha * (2.f * s0), x1 = v[j + 1] * p.alpha * (2.f * s1);
+                    w[j >> 1] = round_pack2(x0, x1);
+                    dot = fmaf(x0, s0, dot);
+                    dot = fmaf(x1, s1, dot);
                 }
-                if (rows_ok) wst32(xb ? const_cast<uint8_t*>(xb) : stg, p.C, ci - (long)lane * p.ldc, p.ldc, NC_BF16, v);
-                else if (row < p.M) st32(p.C, ci, NC_BF16, v);
+                if (rows_ok) wst32_bf16w(xb ? const_cast<uint8_t*>(xb) : stg, p.C, ci - (long)lane * p.ldc, p.ldc, w);
+                else if (row < p.M) st32_bf16w(p.C, ci, w);
             }
             if (p.aux_tma) x_ahead(x, mx, g * (BN / 64), cend, BN, tn, row, b, nt);
         }

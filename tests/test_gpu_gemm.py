@@ -76,3 +76,12 @@ def test_cta_pair_batched_square():
     # the Newton-Schulz shape class: batched square products, B stored [K, N]
     got, ref = _run(384, 384, 384, 0, 1, batch=3, c_dtype="bf16", beta=1.0)
     assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= 8e-3
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,batch", [(520, 320, 1), (300, 448, 2), (520, 776, 1)])
+def test_cta_pair_in_place_accumulate(M, N, ta, tb, batch):
+    # C += alpha A B^T in fp32 in place (the residual stream, accumulated weight gradients):
+    # C comes back in through the epilogue's auxiliary stream; ragged M and K, batched
+    got, ref = _run(M, N, 200, ta, tb, batch=batch, beta=1.0)
+    assert np.max(np.abs(got - ref)) / np.max(np.abs(ref)) <= 1e-4
