@@ -79,7 +79,7 @@ def test_cta_pair_batched_square():
 
 
 @pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("M,N,batch", [(520, 320, 1), (300, 448, 2), (520, 776, 1)])
+@pytest.mark.parametrize("M,N,batch", [(520, 320, 1), (304, 448, 2), (520, 776, 1)])
 def test_cta_pair_in_place_accumulate(M, N, ta, tb, batch):
     # C += alpha A B^T in fp32 in place (the residual stream, accumulated weight gradients):
     # C comes back in through the epilogue's auxiliary stream; ragged M and K, batched
