@@ -69,10 +69,10 @@ NOMINAL_BF16_TFLOPS = 2250.0
 ROOF = {"gemm": "tensor", "attn_fwd": "tensor", "attn_bwd": "tensor", "muon_ns": "tensor",
         "norm": "hbm", "rope": "hbm", "ce": "hbm", "embed": "hbm", "muon_elem": "hbm", "adamw": "hbm"}
 # dram read+write bytes per launch site of the dominant kernel class (the step's model
-# GEMMs), from an ncu capture of the current GEMM code on the step at 4 x 2048 rows (122 MB
+# GEMMs), from an ncu capture of the current GEMM code on the step at 4 x 2048 rows (131 MB
 # per site), scaled by the 8x rows of the 32 x 2048 step (the weights, 3-13 MB per site, do
 # not scale, so this slightly overstates); profiles/gemm_tc2_dram_b4.md.  None when not measured.
-GEMM_TRAFFIC_PER_LAUNCH = 0.98e9
+GEMM_TRAFFIC_PER_LAUNCH = 1.05e9
 # The reference arm times one bounded oracle sample per step (the driver runs
 # --steps 20 --warmup 5): a 512-token row and a sixteenth of the embedding's AdamW
 # keep each near ten seconds on the host.  The cpu_baseline of our own arm is one
