@@ -551,6 +551,16 @@ __global__ void __launch_bounds__(EB_COLS) eb_piece_kernel(const int32_t* tok, c
     }
 }
 
+// dwte[v] = 0 for the ids no row holds (count offsets[v+1] - offsets[v] = 0): the
+// overwrite (accumulate = 0) then writes every row of dwte exactly once, the held ids
+// by the piece sums.  One warp per id, 16-byte stores.
+__global__ void eb_zero_kernel(const int* offsets, float* dwte, int d, int V) {
+    const long v = (long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (v >= V || offsets[v + 1] != offsets[v]) return;
+    float4* row = reinterpret_cast<float4*>(dwte + v * d);
+    for (int c = threadIdx.x % 32; c < d / 4; c += 32) row[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // Tokens whose run of sorted rows crosses a piece border: the piece where the run
 // starts adds its own part (head or tail) and the heads of the pieces it runs into,
 // in order.  One CTA per (piece, 256 columns).
@@ -683,7 +693,11 @@ EmbedBwdWs embed_backward_ws(void* base, int M, int d, int V) {
 int embed_backward(const int32_t* tok, const float* g, float* dwte, int M, int d, int V,
                    int accumulate, const EmbedBwdWs& ws, cudaStream_t s) {
     const int nchunks = ceil_div(M, EB_CHUNK), npieces = ceil_div(M, EB_PIECE);
-    if (!accumulate) NC_TRY(cuda_check(cudaMemsetAsync(dwte, 0, (size_t)V * d * 4, s), "memset dwte"));
+    // overwrite: the ids no row holds are zeroed after the sort (below), the others are
+    // written by the piece sums; without rows, or with rows not 16-byte aligned, all at once
+    const bool zero_rows = !accumulate && M > 0 && d % 4 == 0 && (uintptr_t)dwte % 16 == 0;
+    if (!accumulate && !zero_rows)
+        NC_TRY(cuda_check(cudaMemsetAsync(dwte, 0, (size_t)V * d * 4, s), "memset dwte"));
     if (M <= 0) return NC_OK;
     NC_TRY(cuda_check(cudaMemsetAsync(ws.hist, 0, (size_t)nchunks * V * 4, s), "memset hist"));
     const int nb = ceil_div(V, EB_SCAN_T);
@@ -692,6 +706,10 @@ int embed_backward(const int32_t* tok, const float* g, float* dwte, int M, int d
     eb_colscan_kernel<<<nb, EB_SCAN_T, 0, s>>>(ws.hist, ws.offsets, ws.bsum, nchunks, V);
     eb_scan_kernel<<<1, 1024, (size_t)nb * 4, s>>>(ws.offsets, ws.bsum, nb, V);
     eb_scatter_kernel<<<ceil_div(M, 256), 256, 0, s>>>(tok, ws.hist, ws.rank, ws.offsets, ws.sorted, M, V);
+    if (zero_rows) {
+        eb_zero_kernel<<<ceil_div(V, 8), 256, 0, s>>>(ws.offsets, dwte, d, V);
+        note_launch();
+    }
     eb_piece_kernel<<<dim3(npieces, ceil_div(d, EB_COLS)), EB_COLS, 0, s>>>(
         tok, ws.sorted, ws.offsets, g, dwte, ws.head, ws.tail, d, V, accumulate);
     eb_fixup_kernel<<<dim3(npieces, ceil_div(d, 256)), 256, 0, s>>>(tok, ws.sorted, ws.offsets, ws.head, ws.tail, dwte, d, V, accumulate);
