@@ -193,6 +193,31 @@ def test_step_is_deterministic(inputs):
         assert np.array_equal(a, b)
 
 
+def test_fused_norm_backward_path_is_deterministic():
+    """Widths of 256 and 400 token rows run the CTA-pair products whose epilogues finish the
+    RMSNorm backward (row dots from the cross-entropy and the dh product, ragged last row
+    tile) and the embedding backward's overwrite: two passes give bit-identical results."""
+    import torch
+    from pretraining_step_03_b300.model import Model
+    depth, d, h, v, b, t = 2, 256, 2, 4096, 2, 200
+    params = synth.init_params(depth, d, h, v, seed=11)
+    tok, tgt = synth.zipf_rows(b, t, v, seed=12)
+    tb = synth.token_bytes_binomial(v, seed=2)
+    m = Model(depth, d, h, v, b, t, dtype="bf16")
+    m.set_params(params)
+    dt = m.device_i32
+    res = []
+    for _ in range(2):
+        out = m.forward_backward(dt(tok), dt(tgt), dt(tb), b, t)
+        torch.cuda.synchronize()
+        res.append((out.cpu().numpy().copy(), [m.get_grad(i) for i in range(m.n_params)]))
+    assert m.check_flag() == 0
+    assert np.array_equal(res[0][0], res[1][0])
+    for a, c in zip(res[0][1], res[1][1]):
+        assert np.array_equal(a, c)
+    m.close()
+
+
 def test_out_of_range_token_sets_flag(inputs):
     import torch
     params, tok, tgt, tb = inputs
