@@ -260,6 +260,14 @@ NC_API int nc_check_device_flag(nc_model* m, uint32_t* flags);
  * calls were made on.  Returns NC_ERR_DEVICE_FLAG when any bit was set. */
 NC_API int nc_check_kernel_flag(void* stream, uint32_t* flags);
 
+/* Failure-detection self-test: launches one CTA on `stream` that waits on an
+ * mbarrier nothing arrives on, through the library's bounded wait (about 4 s
+ * of %globaltimer), which then gives up; the kernel sets NC_FLAG_TIMEOUT in
+ * the per-device word of nc_check_kernel_flag() and returns, leaving the
+ * context usable.  No fault, trap or unbounded wait is involved.
+ * Asynchronous; returns NC_ERR_CUDA if the launch fails. */
+NC_API int nc_selftest_wait_timeout(void* stream);
+
 /*
  * Causal multi-head attention forward (section 预搜检: 10 heads of dim 128):
  * O = softmax(Q K^T / sqrt(D), keys s <= query t) V per (b, h).

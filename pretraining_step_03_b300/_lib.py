@@ -58,6 +58,7 @@ SIGNATURES = {
     "nc_set_state": (_I, [_V, _I, _I, _V, _SZ]),
     "nc_check_device_flag": (_I, [_V, ctypes.POINTER(ctypes.c_uint32)]),
     "nc_check_kernel_flag": (_I, [_V, ctypes.POINTER(ctypes.c_uint32)]),
+    "nc_selftest_wait_timeout": (_I, [_V]),
     "nc_attention_forward": (_I, [_V, _V, _V, _I, _V, _I, _V, _I, _I, _I, _I, _I, _V]),
     "nc_attention_workspace_bytes": (_SZ, [_I, _I, _I]),
     "nc_attention_backward": (_I, [_V, _V, _V, _I, _V, _V, _I, _V, _V, _V, _V, _I, _V, _I, _I, _I,
@@ -221,6 +222,10 @@ def nc_check_device_flag(m):
     if rc not in (NC_OK, NC_ERR_DEVICE_FLAG):
         _check(rc)
     return f.value
+
+
+def nc_selftest_wait_timeout(stream):
+    _check(lib().nc_selftest_wait_timeout(stream))
 
 
 def nc_check_kernel_flag(stream):

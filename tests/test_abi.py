@@ -60,3 +60,18 @@ def test_null_handles_are_rejected(lib):
     assert lib.nc_gemm_bf16(0, 1, 1, 1, None, 1, 0, 0, None, 1, 0, 0, None, 1, 0, 0, 1.0, 0.0, None, 0,
                             None) == L.NC_ERR_ARG
     assert "null" in L.nc_last_error()
+
+
+def test_arena_shortfall_is_reported_before_any_launch(lib):
+    """The library never allocates: an arena smaller than nc_arena_bytes is its allocation
+    failure, reported as NC_ERR_OOM on the host (the pointer is only checked for alignment,
+    never dereferenced, so no GPU is needed)."""
+    out = ctypes.c_void_p()
+    need = L.nc_arena_bytes(2, 128, 2, 512, 4, 64, L.NC_BF16)
+    rc = lib.nc_init_model(2, 128, 2, 512, 0, ctypes.c_void_p(1 << 20), need - 256, L.NC_BF16, 4, 64, None,
+                           ctypes.byref(out))
+    assert rc == L.NC_ERR_OOM
+    assert "arena" in L.nc_last_error()
+    rc = lib.nc_init_model(2, 128, 2, 512, 0, ctypes.c_void_p((1 << 20) + 8), need, L.NC_BF16, 4, 64, None,
+                           ctypes.byref(out))
+    assert rc == L.NC_ERR_ARG   # not 256-byte aligned
